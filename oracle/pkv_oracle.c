@@ -1,0 +1,297 @@
+/*
+ * pkv_oracle.c -- plain CPU reference for the paged KV-cache hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
+ * CPU-baseline leg of the benchmark may load this library.  The product path
+ * (the CUDA library and its Python binding) never calls it, links it or
+ * falls back to it.  It shares no code, header, table or helper with the
+ * CUDA path.
+ *
+ * Everything is computed in IEEE double from the exactly widened bf16 inputs,
+ * in the order the definitions below state, with no blocking, fusion or
+ * reordering.  Sources (web pages on a mini vLLM inference engine):
+ *
+ *  [P1] "跟着 Claude Code，我用 Python 实现了一个轻量级的 vLLM",
+ *       section "核心机制一：分页 KV Cache": the KV cache is cut into
+ *       fixed-size blocks of (for example) 16 tokens, allocated on demand.
+ *  [P2] "从零实现一个 mini vLLM--开篇",
+ *       section 2 "LLM 推理到底在慢什么": decode computes only the new
+ *       token's K/V, appends it to the cache, and attends over all
+ *       historical K/V;
+ *       section 5 "这个系列会怎么展开" (phases 4 and 5): each request owns
+ *       a block table; the sequence is logically contiguous, physically
+ *       scattered over blocks, and attention finds the real K and V through
+ *       the block table.
+ *
+ * Readings taken where the pages are silent (the same readings the CUDA
+ * library documents in its header):
+ *  - cache layout: k_cache and v_cache are each [num_blocks][num_kv_heads]
+ *    [block_size][head_dim] bf16; slot s lives in block s / block_size at
+ *    offset s % block_size;
+ *  - a negative slot means "no slot" (padding) and is skipped;
+ *  - q head h reads kv head h / (num_q_heads / num_kv_heads) (contiguous
+ *    GQA groups);
+ *  - context_lens[b] counts every cached token, including the one appended
+ *    in this step; there is no mask; context_len 0 gives an all-zero output;
+ *  - block-table entries past ceil(context_len / block_size) are never read.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* Return codes (bit mask). */
+#define ORACLE_OK 0
+#define ORACLE_BAD_ARGUMENT 1
+#define ORACLE_SLOT_OUT_OF_RANGE 2
+#define ORACLE_DUPLICATE_SLOT 4
+#define ORACLE_BLOCK_ID_OUT_OF_RANGE 8
+#define ORACLE_CONTEXT_LEN_OUT_OF_RANGE 16
+
+/* A bf16 value is the upper half of an IEEE binary32; widening is exact. */
+static double bf16_to_double(uint16_t bits) {
+    uint32_t word = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &word, sizeof f);
+    return (double)f;
+}
+
+static int cmp_i64(const void* a, const void* b) {
+    int64_t x = *(const int64_t*)a, y = *(const int64_t*)b;
+    return (x > y) - (x < y);
+}
+
+/*
+ * Append [P2 section 2; P1 section 核心机制一]: for every token i whose slot
+ * s = slot_mapping[i] is non-negative, copy the bits of k[i, h, :] into
+ * k_cache[s / block_size, h, s % block_size, :] for every kv head h, and the
+ * same for v.  An exact bit copy.  Slots past the pool are skipped and
+ * flagged; duplicate non-negative slots are flagged (the operation is only
+ * defined for distinct slots) and nothing is written then.
+ */
+int pkv_oracle_kv_append(const uint16_t* k, const uint16_t* v,
+                         const int64_t* slot_mapping, int64_t num_tokens,
+                         int32_t num_kv_heads, int32_t head_dim,
+                         uint16_t* k_cache, uint16_t* v_cache,
+                         int64_t num_blocks, int32_t block_size) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0)
+        return ORACLE_BAD_ARGUMENT;
+    if (num_tokens == 0) return ORACLE_OK;
+
+    /* Distinctness check on a sorted copy of the non-negative slots. */
+    int64_t* sorted = (int64_t*)malloc(sizeof(int64_t) * (size_t)num_tokens);
+    if (!sorted) return ORACLE_BAD_ARGUMENT;
+    int64_t n_valid = 0;
+    for (int64_t i = 0; i < num_tokens; ++i)
+        if (slot_mapping[i] >= 0) sorted[n_valid++] = slot_mapping[i];
+    qsort(sorted, (size_t)n_valid, sizeof(int64_t), cmp_i64);
+    for (int64_t i = 1; i < n_valid; ++i) {
+        if (sorted[i] == sorted[i - 1]) {
+            free(sorted);
+            return ORACLE_DUPLICATE_SLOT;
+        }
+    }
+    free(sorted);
+
+    int status = ORACLE_OK;
+    const int64_t num_slots = num_blocks * (int64_t)block_size;
+    for (int64_t i = 0; i < num_tokens; ++i) {
+        const int64_t s = slot_mapping[i];
+        if (s < 0) continue;
+        if (s >= num_slots) {
+            status |= ORACLE_SLOT_OUT_OF_RANGE;
+            continue;
+        }
+        const int64_t block = s / block_size;
+        const int64_t offset = s % block_size;
+        for (int32_t h = 0; h < num_kv_heads; ++h) {
+            const int64_t src = (i * num_kv_heads + h) * (int64_t)head_dim;
+            const int64_t dst = ((block * num_kv_heads + h) * block_size + offset) * (int64_t)head_dim;
+            for (int32_t d = 0; d < head_dim; ++d) {
+                k_cache[dst + d] = k[src + d];
+                v_cache[dst + d] = v[src + d];
+            }
+        }
+    }
+    return status;
+}
+
+typedef struct {
+    const uint16_t* q;
+    const uint16_t* k_cache;
+    const uint16_t* v_cache;
+    const int32_t* block_tables;
+    int32_t max_blocks_per_seq;
+    const int32_t* context_lens;
+    int32_t num_seqs;
+    int32_t num_q_heads;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int64_t num_blocks;
+    int32_t block_size;
+    double scale;
+} problem_t;
+
+/*
+ * Decode attention for one (sequence b, q head h) [P2 section 5, phases 4-5;
+ * P2 section 2]:
+ *   kv   = h / (Hq / Hkv)
+ *   K_t  = k_cache[block_tables[b, t / bs], kv, t % bs, :]   for t < L
+ *   V_t  = v_cache[block_tables[b, t / bs], kv, t % bs, :]
+ *   s_t  = scale * sum_d q[b, h, d] * K_t[d]
+ *   p_t  = exp(s_t - max_t s_t) / sum_u exp(s_u - max_t s_t)
+ *   out  = sum_t p_t * V_t
+ * Writes head_dim doubles to out_row.  L == 0 writes zeros.
+ */
+static int decode_one(const problem_t* P, int32_t b, int32_t h, double* out_row) {
+    const int32_t D = P->head_dim;
+    for (int32_t d = 0; d < D; ++d) out_row[d] = 0.0;
+    if (b < 0 || b >= P->num_seqs || h < 0 || h >= P->num_q_heads) return ORACLE_BAD_ARGUMENT;
+    const int32_t L = P->context_lens[b];
+    if (L < 0 || (int64_t)L > (int64_t)P->max_blocks_per_seq * P->block_size)
+        return ORACLE_CONTEXT_LEN_OUT_OF_RANGE;
+    if (L == 0) return ORACLE_OK;
+
+    const int32_t group = P->num_q_heads / P->num_kv_heads;
+    const int32_t kv = h / group;
+    const uint16_t* qrow = P->q + ((int64_t)b * P->num_q_heads + h) * D;
+
+    double* scores = (double*)malloc(sizeof(double) * (size_t)L);
+    const uint16_t** vrows = (const uint16_t**)malloc(sizeof(uint16_t*) * (size_t)L);
+    if (!scores || !vrows) {
+        free(scores);
+        free((void*)vrows);
+        return ORACLE_BAD_ARGUMENT;
+    }
+
+    /* Gather through the block table and form the scaled scores. */
+    for (int32_t t = 0; t < L; ++t) {
+        const int32_t logical_block = t / P->block_size;
+        const int32_t offset = t % P->block_size;
+        const int64_t phys = P->block_tables[(int64_t)b * P->max_blocks_per_seq + logical_block];
+        if (phys < 0 || phys >= P->num_blocks) {
+            free(scores);
+            free((void*)vrows);
+            for (int32_t d = 0; d < D; ++d) out_row[d] = 0.0;
+            return ORACLE_BLOCK_ID_OUT_OF_RANGE;
+        }
+        const int64_t row = ((phys * P->num_kv_heads + kv) * P->block_size + offset) * (int64_t)D;
+        const uint16_t* krow = P->k_cache + row;
+        vrows[t] = P->v_cache + row;
+        double dot = 0.0;
+        for (int32_t d = 0; d < D; ++d) dot += bf16_to_double(qrow[d]) * bf16_to_double(krow[d]);
+        scores[t] = P->scale * dot;
+    }
+
+    /* Softmax with the maximum subtracted. */
+    double m = scores[0];
+    for (int32_t t = 1; t < L; ++t)
+        if (scores[t] > m) m = scores[t];
+    double denom = 0.0;
+    for (int32_t t = 0; t < L; ++t) {
+        scores[t] = exp(scores[t] - m);
+        denom += scores[t];
+    }
+
+    /* Probability-weighted sum of the value rows. */
+    for (int32_t t = 0; t < L; ++t) {
+        const double p = scores[t] / denom;
+        for (int32_t d = 0; d < D; ++d) out_row[d] += p * bf16_to_double(vrows[t][d]);
+    }
+    free(scores);
+    free((void*)vrows);
+    return ORACLE_OK;
+}
+
+typedef struct {
+    const problem_t* P;
+    const int32_t* seq_idx;  /* NULL: item i is (i / Hq, i % Hq) */
+    const int32_t* head_idx;
+    int64_t begin, end;
+    double* out;             /* item i writes out[i * head_dim ...] */
+    int status;
+} job_t;
+
+static void* run_job(void* arg) {
+    job_t* J = (job_t*)arg;
+    const problem_t* P = J->P;
+    for (int64_t i = J->begin; i < J->end; ++i) {
+        int32_t b, h;
+        if (J->seq_idx) {
+            b = J->seq_idx[i];
+            h = J->head_idx[i];
+        } else {
+            b = (int32_t)(i / P->num_q_heads);
+            h = (int32_t)(i % P->num_q_heads);
+        }
+        J->status |= decode_one(P, b, h, J->out + i * P->head_dim);
+    }
+    return NULL;
+}
+
+static int run_items(const problem_t* P, const int32_t* seq_idx, const int32_t* head_idx,
+                     int64_t n_items, double* out, int32_t num_threads) {
+    if (P->num_kv_heads <= 0 || P->num_q_heads <= 0 || P->num_q_heads % P->num_kv_heads != 0 ||
+        P->head_dim <= 0 || P->block_size <= 0 || P->num_seqs < 0 || P->max_blocks_per_seq < 0)
+        return ORACLE_BAD_ARGUMENT;
+    if (n_items <= 0) return ORACLE_OK;
+    if (num_threads < 1) num_threads = 1;
+    if (num_threads > 256) num_threads = 256;
+    if ((int64_t)num_threads > n_items) num_threads = (int32_t)n_items;
+
+    job_t jobs[256];
+    pthread_t threads[256];
+    int started[256];
+    for (int32_t t = 0; t < num_threads; ++t) {
+        jobs[t].P = P;
+        jobs[t].seq_idx = seq_idx;
+        jobs[t].head_idx = head_idx;
+        jobs[t].begin = n_items * t / num_threads;
+        jobs[t].end = n_items * (t + 1) / num_threads;
+        jobs[t].out = out;
+        jobs[t].status = 0;
+        started[t] = 0;
+    }
+    for (int32_t t = 1; t < num_threads; ++t)
+        started[t] = (pthread_create(&threads[t], NULL, run_job, &jobs[t]) == 0);
+    run_job(&jobs[0]);
+    int status = jobs[0].status;
+    for (int32_t t = 1; t < num_threads; ++t) {
+        if (started[t]) pthread_join(threads[t], NULL);
+        else run_job(&jobs[t]);
+        status |= jobs[t].status;
+    }
+    return status;
+}
+
+/*
+ * Paged decode attention over every (sequence, q head): out is
+ * [num_seqs][num_q_heads][head_dim] doubles.  num_threads only splits the
+ * independent (b, h) items; each item is computed exactly as decode_one says.
+ */
+int pkv_oracle_paged_decode_attention(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
+                                      int32_t block_size, double scale, double* out, int32_t num_threads) {
+    problem_t P = {q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                   num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale};
+    return run_items(&P, NULL, NULL, (int64_t)num_seqs * num_q_heads, out, num_threads);
+}
+
+/*
+ * The same computation on a chosen sample of (sequence, q head) pairs: item i
+ * is (seq_idx[i], head_idx[i]) and writes out[i][0..head_dim).
+ */
+int pkv_oracle_paged_decode_sampled(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                    const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                    const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                    int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
+                                    int32_t block_size, double scale, const int32_t* seq_idx,
+                                    const int32_t* head_idx, int64_t n_samples, double* out,
+                                    int32_t num_threads) {
+    problem_t P = {q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                   num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale};
+    return run_items(&P, seq_idx, head_idx, n_samples, out, num_threads);
+}

@@ -1,0 +1,328 @@
+"""Pins for the CPU oracle: each test ties it to something other than itself.
+
+The pages print no worked numerical example, so the pins are closed forms,
+invariants of the definition, special cases that reduce to a library routine
+(torch's float64 scaled-dot-product attention on un-paged tensors, numpy
+indexing), and brute force on tiny inputs.  Each test names the mistake it
+would catch.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+
+import oracle
+from workloads import BLOCK_SIZE, BlockAllocator, make_decode_case, make_generator, randn_bf16
+
+pytestmark = pytest.mark.usefixtures("oracle_lib")
+
+
+def f64(x: torch.Tensor) -> torch.Tensor:
+    return x.to(torch.float64)
+
+
+def contiguous_kv(case_k, case_v, block_tables, context_lens, b):
+    """Un-paged K/V of sequence b, [Hkv, L, D] float64, via torch advanced indexing on a slot view."""
+    L = int(context_lens[b])
+    nb, hkv, bs, d = case_k.shape
+    pos = torch.arange(L)
+    slots = block_tables[b, pos // bs].to(torch.int64) * bs + pos % bs
+    kflat = case_k.permute(0, 2, 1, 3).reshape(nb * bs, hkv, d)
+    vflat = case_v.permute(0, 2, 1, 3).reshape(nb * bs, hkv, d)
+    return f64(kflat[slots]).permute(1, 0, 2), f64(vflat[slots]).permute(1, 0, 2)
+
+
+def sdpa_reference(q, k_cache, v_cache, block_tables, context_lens, scale):
+    """torch float64 SDPA per sequence on the un-paged K/V, GQA by repeat_interleave."""
+    B, hq, d = q.shape
+    hkv = k_cache.shape[1]
+    out = torch.zeros(B, hq, d, dtype=torch.float64)
+    for b in range(B):
+        if int(context_lens[b]) == 0:
+            continue
+        K, V = contiguous_kv(k_cache, v_cache, block_tables, context_lens, b)
+        K = K.repeat_interleave(hq // hkv, dim=0)
+        V = V.repeat_interleave(hq // hkv, dim=0)
+        o = F.scaled_dot_product_attention(f64(q[b]).unsqueeze(1), K, V, scale=scale)
+        out[b] = o.squeeze(1)
+    return out.numpy()
+
+
+def run_oracle(q, kc, vc, bt, cl, scale):
+    out, st = oracle.paged_decode_attention(q, kc, vc, bt, cl, scale)
+    assert st == oracle.OK
+    return out
+
+
+def bf16(x) -> torch.Tensor:
+    return torch.as_tensor(x, dtype=torch.float32).to(torch.bfloat16)
+
+
+# ---------------------------------------------------------------------------
+# Closed forms
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("scale,kscale", [(1.0, 1.0), (0.5, 2.0), (0.125, 8.0)])
+def test_closed_form_softmax_weights(scale, kscale):
+    """s_t = t with one-hot V_t: out[d] = e^d / sum_u e^u.  Catches a missing exp, a
+    wrong normalisation, a sign error in the softmax and a misapplied scale."""
+    D, L = 64, 20                        # 20 tokens: crosses a block edge
+    nb = 4
+    kc = torch.zeros(nb, 1, BLOCK_SIZE, D, dtype=torch.bfloat16)
+    vc = torch.zeros_like(kc)
+    table = torch.tensor([[2, 0]], dtype=torch.int32)  # logical block 0 -> physical 2, 1 -> 0
+    weights_exp = []
+    for t in range(L):
+        s = t % 5                         # scores 0..4 repeating
+        phys, off = int(table[0, t // BLOCK_SIZE]), t % BLOCK_SIZE
+        kc[phys, 0, off, 0] = bf16(s * kscale)
+        vc[phys, 0, off, t] = bf16(1.0)  # one-hot value at dim t
+        weights_exp.append(math.exp(s))
+    q = torch.zeros(1, 1, D, dtype=torch.bfloat16)
+    q[0, 0, 0] = 1.0
+    out = run_oracle(q, kc, vc, table, torch.tensor([L], dtype=torch.int32), scale)
+    total = sum(weights_exp)
+    expect = np.zeros(D)
+    expect[:L] = [w / total for w in weights_exp]
+    np.testing.assert_allclose(out[0, 0], expect, rtol=0, atol=1e-15)
+
+
+def test_single_token_returns_its_value_exactly():
+    """L = 1: the only weight is 1, so out = V_0 exactly.  Catches off-by-one token ranges."""
+    case = make_decode_case("tiny", seed=3, lengths=[1, 1, 1, 1])
+    out = run_oracle(case.q, case.k_cache, case.v_cache, case.block_tables, case.context_lens, case.scale)
+    for b in range(4):
+        phys = int(case.block_tables[b, 0])
+        v0 = f64(case.v_cache[phys, 0, 0]).numpy()
+        for h in range(2):
+            assert np.array_equal(out[b, h], v0)
+
+
+def test_zero_query_gives_mean_of_values():
+    """q = 0 makes every score equal: out = mean_t V_t (numpy mean).  Catches weights that
+    do not sum to one and tokens read twice or skipped."""
+    case = make_decode_case("tiny", seed=4)
+    q = torch.zeros_like(case.q)
+    out = run_oracle(q, case.k_cache, case.v_cache, case.block_tables, case.context_lens, case.scale)
+    for b in range(4):
+        _, V = contiguous_kv(case.k_cache, case.v_cache, case.block_tables, case.context_lens, b)
+        np.testing.assert_allclose(out[b, 0], V[0].numpy().mean(axis=0), rtol=0, atol=1e-14)
+
+
+def test_huge_scale_selects_argmax_value():
+    """As scale grows the softmax tends to a one-hot on the largest score.  Catches a
+    reversed softmax (that would pick the smallest score)."""
+    case = make_decode_case("tiny", seed=5)
+    out = run_oracle(case.q, case.k_cache, case.v_cache, case.block_tables, case.context_lens, 1e4)
+    for b in range(4):
+        K, V = contiguous_kv(case.k_cache, case.v_cache, case.block_tables, case.context_lens, b)
+        for h in range(2):
+            s = K[0].numpy() @ f64(case.q[b, h]).numpy()
+            top2 = np.sort(s)[-2:]
+            assert (top2[1] - top2[0]) * 1e4 > 60  # the second-best weight is below e^-60
+            np.testing.assert_allclose(out[b, h], V[0, int(np.argmax(s))].numpy(), rtol=0, atol=1e-20)
+
+
+def test_gqa_head_mapping_contiguous_groups():
+    """V constant c_j on kv head j gives out = c_j for every q head of group j, whatever
+    the weights.  With Hq = 8, Hkv = 4 this separates h // G from h % Hkv."""
+    g = make_generator(11)
+    hq, hkv, D, nb = 8, 4, 64, 6
+    kc = randn_bf16((nb, hkv, BLOCK_SIZE, D), g)
+    vc = torch.zeros_like(kc)
+    for j in range(hkv):
+        vc[:, j] = bf16(j + 1.0)
+    q = randn_bf16((2, hq, D), g)
+    table = torch.tensor([[5, 1, 3], [0, 2, -1]], dtype=torch.int32)
+    out = run_oracle(q, kc, vc, table, torch.tensor([40, 17], dtype=torch.int32), 0.125)
+    for h in range(hq):
+        np.testing.assert_allclose(out[:, h], np.full((2, D), h // (hq // hkv) + 1.0), rtol=0, atol=1e-13)
+
+
+def test_context_len_zero_gives_zeros():
+    case = make_decode_case("tiny", seed=6, lengths=[0, 5, 0, 16])
+    out = run_oracle(case.q, case.k_cache, case.v_cache, case.block_tables, case.context_lens, case.scale)
+    assert np.all(out[0] == 0) and np.all(out[2] == 0)
+    assert np.any(out[1] != 0) and np.any(out[3] != 0)
+
+
+# ---------------------------------------------------------------------------
+# Library routine on un-paged tensors; brute force on tiny inputs
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("seed", [0, 1])
+def test_tiny_workload_matches_torch_sdpa(seed):
+    """The tiny workload (lens 5, 16, 17, 40 over a permuted 16-block pool) against
+    torch float64 SDPA on the un-paged K/V.  Catches index, GQA, transposition and
+    block-table mistakes."""
+    c = make_decode_case("tiny", seed=seed)
+    out = run_oracle(c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens, c.scale)
+    ref = sdpa_reference(c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens, c.scale)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+
+
+def test_qwen_shape_sample_matches_torch_sdpa():
+    """Qwen3-0.6B head layout (16 q / 8 kv, D 128) on a few lengths around block edges."""
+    lens = [1, 15, 16, 17, 33, 130, 511]
+    c = make_decode_case("qwen3_0.6b", seed=7, lengths=lens)
+    out = run_oracle(c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens, c.scale)
+    ref = sdpa_reference(c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens, c.scale)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+
+
+def test_brute_force_every_length_up_to_three_blocks():
+    """Every length 0..48 (every offset in three blocks), GQA 2, D 64, vs SDPA."""
+    lens = list(range(0, 49))
+    spec = make_decode_case("tiny", seed=8, lengths=[1]).spec
+    from workloads import DecodeSpec
+    spec = DecodeSpec(**{**spec.__dict__, "pool_blocks": None, "pool_slack": 0.3})
+    c = make_decode_case(spec, seed=8, lengths=lens)
+    out = run_oracle(c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens, 0.3)
+    ref = sdpa_reference(c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens, 0.3)
+    np.testing.assert_allclose(out, ref, rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Invariants
+# ---------------------------------------------------------------------------
+def test_physical_block_relabelling_is_invisible():
+    """Paging changes where K/V live, not what is computed: relabel every physical block
+    by a permutation (cache and tables together) and the output is bit-identical.
+    Catches any use of a physical id where a logical position belongs."""
+    c = make_decode_case("tiny", seed=9)
+    base = run_oracle(c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens, c.scale)
+    g = make_generator(99)
+    perm = torch.randperm(c.num_blocks, generator=g)
+    kc2 = torch.empty_like(c.k_cache)
+    vc2 = torch.empty_like(c.v_cache)
+    kc2[perm] = c.k_cache
+    vc2[perm] = c.v_cache
+    bt2 = torch.where(c.block_tables >= 0, perm[c.block_tables.clamp(min=0).long()].to(torch.int32),
+                      c.block_tables)
+    out2 = run_oracle(c.q, kc2, vc2, bt2, c.context_lens, c.scale)
+    assert np.array_equal(base, out2)
+
+
+def test_unused_slots_and_table_entries_are_never_read():
+    """NaN in every slot no sequence owns (block tails and free blocks) and garbage in the
+    table past each sequence's blocks change nothing."""
+    c = make_decode_case("tiny", seed=10)
+    base = run_oracle(c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens, c.scale)
+    kc, vc = c.k_cache.clone(), c.v_cache.clone()
+    used = torch.zeros(c.num_blocks * BLOCK_SIZE, dtype=torch.bool)
+    for sid in range(4):
+        for p in range(c.allocator.length[sid]):
+            used[c.allocator.slot(sid, p)] = True
+    unused = (~used).view(c.num_blocks, BLOCK_SIZE)
+    nan = torch.tensor(float("nan"), dtype=torch.bfloat16)
+    kc.permute(0, 2, 1, 3)[unused] = nan
+    vc.permute(0, 2, 1, 3)[unused] = nan
+    bt = c.block_tables.clone()
+    bt[bt < 0] = 123456
+    out = run_oracle(c.q, kc, vc, bt, c.context_lens, c.scale)
+    assert np.isfinite(out).all()
+    assert np.array_equal(base, out)
+
+
+def test_identical_queries_in_a_group_give_identical_outputs():
+    c = make_decode_case("qwen3_0.6b", seed=12, lengths=[3, 40, 77])
+    q = c.q.clone()
+    q[:, 1] = q[:, 0]                    # heads 0 and 1 share kv head 0
+    out = run_oracle(q, c.k_cache, c.v_cache, c.block_tables, c.context_lens, c.scale)
+    assert np.array_equal(out[:, 0], out[:, 1])
+    assert not np.array_equal(out[:, 0], out[:, 2])
+
+
+def test_sampled_equals_full():
+    c = make_decode_case("qwen3_0.6b", seed=13, lengths=[5, 300, 64])
+    full = run_oracle(c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens, c.scale)
+    si = np.array([2, 0, 1, 1], dtype=np.int32)
+    hi = np.array([15, 3, 0, 9], dtype=np.int32)
+    samp, st = oracle.paged_decode_sampled(c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens,
+                                           c.scale, si, hi)
+    assert st == oracle.OK
+    assert np.array_equal(samp, full[si, hi])
+
+
+def test_bad_block_id_and_length_are_reported():
+    c = make_decode_case("tiny", seed=14)
+    bt = c.block_tables.clone()
+    bt[1, 0] = 99
+    _, st = oracle.paged_decode_attention(c.q, c.k_cache, c.v_cache, bt, c.context_lens, c.scale)
+    assert st & oracle.BLOCK_ID_OUT_OF_RANGE
+    cl = c.context_lens.clone()
+    cl[0] = 3 * BLOCK_SIZE + 1
+    _, st = oracle.paged_decode_attention(c.q, c.k_cache, c.v_cache, c.block_tables, cl, c.scale)
+    assert st & oracle.CONTEXT_LEN_OUT_OF_RANGE
+
+
+# ---------------------------------------------------------------------------
+# Append
+# ---------------------------------------------------------------------------
+def test_append_writes_exact_bits_at_the_slot_and_nothing_else():
+    """Append into a sentinel-filled pool, read back with numpy multi-dimensional indexing
+    cache[s // 16, h, s % 16, :].  Catches a swapped block / offset, a wrong head stride
+    and stray writes."""
+    g = make_generator(21)
+    nb, hkv, D, N = 7, 2, 64, 40
+    sentinel = torch.tensor(-7.25, dtype=torch.bfloat16)
+    kc = torch.full((nb, hkv, BLOCK_SIZE, D), float(sentinel), dtype=torch.bfloat16)
+    vc = kc.clone()
+    slots = torch.randperm(nb * BLOCK_SIZE, generator=g)[:N].to(torch.int64)
+    slots[3] = -1                       # padding: skipped
+    k = randn_bf16((N, hkv, D), g)
+    v = randn_bf16((N, hkv, D), g)
+    assert oracle.kv_append(k, v, slots, kc, vc) == oracle.OK
+    kb = kc.view(torch.int16).numpy()
+    vb = vc.view(torch.int16).numpy()
+    written = np.zeros((nb, BLOCK_SIZE), dtype=bool)
+    for i, s in enumerate(slots.tolist()):
+        if s < 0:
+            continue
+        blk, off = divmod(s, BLOCK_SIZE)
+        written[blk, off] = True
+        assert np.array_equal(kb[blk, :, off, :], k[i].view(torch.int16).numpy())
+        assert np.array_equal(vb[blk, :, off, :], v[i].view(torch.int16).numpy())
+    sbits = int(sentinel.view(torch.int16))
+    assert np.all(kb.transpose(0, 2, 1, 3)[~written] == sbits)
+    assert np.all(vb.transpose(0, 2, 1, 3)[~written] == sbits)
+
+
+def test_append_rejects_out_of_range_and_duplicate_slots():
+    g = make_generator(22)
+    nb, hkv, D = 2, 1, 64
+    kc = torch.zeros(nb, hkv, BLOCK_SIZE, D, dtype=torch.bfloat16)
+    vc = kc.clone()
+    k = randn_bf16((2, hkv, D), g)
+    st = oracle.kv_append(k, k, torch.tensor([5, nb * BLOCK_SIZE], dtype=torch.int64), kc, vc)
+    assert st & oracle.SLOT_OUT_OF_RANGE
+    assert torch.equal(kc[0, 0, 5], k[0, 0])
+    st = oracle.kv_append(k, k, torch.tensor([9, 9], dtype=torch.int64), kc, vc)
+    assert st & oracle.DUPLICATE_SLOT
+
+
+def test_append_then_attend_equals_contiguous_attention():
+    """Write each sequence token by token through the allocator's slots, then attend:
+    equals SDPA over the tokens as written.  Ties the append layout to the gather."""
+    g = make_generator(23)
+    hq, hkv, D, nb = 4, 2, 128, 24
+    lens = [1, 16, 17, 50]
+    alloc = BlockAllocator(nb, g)
+    kc = torch.zeros(nb, hkv, BLOCK_SIZE, D, dtype=torch.bfloat16)
+    vc = torch.zeros_like(kc)
+    tok_k = [randn_bf16((L, hkv, D), g) for L in lens]
+    tok_v = [randn_bf16((L, hkv, D), g) for L in lens]
+    for sid, L in enumerate(lens):
+        alloc.add_sequence(sid, 0)
+        for p in range(L):
+            s = alloc.append_token(sid)
+            assert oracle.kv_append(tok_k[sid][p:p + 1], tok_v[sid][p:p + 1],
+                                    torch.tensor([s], dtype=torch.int64), kc, vc) == oracle.OK
+    bt = alloc.block_table(list(range(len(lens))), 4)
+    q = randn_bf16((len(lens), hq, D), g)
+    out = run_oracle(q, kc, vc, bt, torch.tensor(lens, dtype=torch.int32), 0.09)
+    for b, L in enumerate(lens):
+        K = f64(tok_k[b]).permute(1, 0, 2).repeat_interleave(hq // hkv, dim=0)
+        V = f64(tok_v[b]).permute(1, 0, 2).repeat_interleave(hq // hkv, dim=0)
+        ref = F.scaled_dot_product_attention(f64(q[b]).unsqueeze(1), K, V, scale=0.09).squeeze(1)
+        np.testing.assert_allclose(out[b], ref.numpy(), rtol=0, atol=1e-12)
