@@ -1,0 +1,472 @@
+"""Benchmark of the paged KV-cache hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload llama3_8b]
+
+One step = one pass of the whole hot path over one batch: kv_append of this
+step's token for every sequence, then paged decode attention (partition
+kernel + merge kernel) over the block-table KV cache.  The default workload
+is one LLaMA-3-8B-shaped layer (B 128, 32 q / 8 kv heads, head_dim 128,
+context lengths uniform in 512..4096, block 16, ~1.2 GB of K+V): synthetic
+bf16 N(0, 1) data from a seeded generator.
+
+Reported (one JSON line on rank 0):
+  value       algorithmic GB/s of the step (attention + append bytes) with the
+              inputs resident in HBM, device-timed with CUDA events;
+  e2e         the same metric through the public API with this step's inputs
+              copied from pinned host memory and the output read back, inside
+              the timed region;
+  roofline    the partition kernel (dominant): algorithmic bytes per launch /
+              its mean duration (CUDA events on the launching stream) against
+              the measured HBM copy bandwidth;
+  cpu_baseline  the fp64 CPU oracle on the host cores, on the same workload.
+``--impl reference`` times that oracle as the reference arm.
+
+Multi-GPU: ``torchrun --nproc-per-node N bench.py --gpus N``: every rank runs
+an independent replica of the step on its own GPU (no collective on the
+path; weak scaling); value = all ranks' bytes / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import torch  # noqa: E402
+
+from workloads import SPECS, algorithmic_bytes, append_bytes, make_decode_case  # noqa: E402
+
+METRIC = "paged decode attention achieved HBM GB/s (% of GB300 peak); seq·layer/s"
+UNIT = "GB/s"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 126 * 2 ** 20
+
+
+def peaks() -> tuple[float, str]:
+    p = ROOT / "MEASURED_PEAKS.json"
+    try:
+        d = json.loads(p.read_text())
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# Distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            if backend == "nccl":
+                torch.cuda.set_device(self.local_rank)
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            if torch.cuda.is_available():
+                self.pg.barrier(device_ids=[self.local_rank])
+            else:
+                self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        return self._reduce(x, "max")
+
+    def sum(self, x: float) -> float:
+        return self._reduce(x, "sum")
+
+    def _reduce(self, x: float, op: str) -> float:
+        if not self.pg:
+            return x
+        dev = f"cuda:{self.local_rank}" if torch.cuda.is_available() else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX if op == "max" else self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+def aggregate(per_rank_units: float, per_rank_seconds: float, dist: Dist) -> tuple[float, float]:
+    """Whole-job throughput: units summed over ranks / the slowest rank's time."""
+    total_units = dist.sum(per_rank_units)
+    slowest = dist.max(per_rank_seconds)
+    return total_units / slowest, slowest
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: str):
+        self.proc = None
+        self.gpu = gpu_index
+        self.windows: list[tuple[float, float]] = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> list[list[str]]:
+        if not self.proc:
+            return []
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = []
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) >= 10:
+                rows.append(parts)
+        return rows
+
+    @staticmethod
+    def summarize(rows, t0: float, t1: float) -> dict | None:
+        import datetime as _dt
+        if not rows:
+            return None
+
+        def ts(r):
+            try:
+                return _dt.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except Exception:
+                return None
+
+        inside = [r for r in rows if ts(r) is not None and t0 <= ts(r) <= t1]
+        window = "timed region"
+        if not inside:
+            inside, window = rows, "warm-up + timed region (timed region shorter than one sample)"
+
+        def num(x):
+            try:
+                return float(x)
+            except Exception:
+                return None
+
+        sm = [num(r[2]) for r in inside if num(r[2]) is not None]
+        mx = [num(r[3]) for r in inside if num(r[3]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in inside:
+            for name, val in zip(names, r[6:10]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        power = [num(r[4]) for r in inside if num(r[4]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(inside), "window": window,
+                "power_w_max": max(power) if power else None}
+
+
+def nvidia_smi_id(dev: torch.device) -> str:
+    """nvidia-smi --id for a torch device (its PCI bus id; CUDA_VISIBLE_DEVICES may renumber)."""
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:
+        return str(dev.index or 0)
+
+
+# ---------------------------------------------------------------------------
+# CPU side: the oracle (baseline and reference arm)
+# ---------------------------------------------------------------------------
+def oracle_step_seconds(case_cpu, threads: int) -> float:
+    import oracle
+    kc, vc = case_cpu.k_cache, case_cpu.v_cache
+    t = time.perf_counter()
+    st = oracle.kv_append(case_cpu.new_k, case_cpu.new_v, case_cpu.slot_mapping, kc, vc)
+    _, st2 = oracle.paged_decode_attention(case_cpu.q, kc, vc, case_cpu.block_tables, case_cpu.context_lens,
+                                           case_cpu.scale, num_threads=threads)
+    dt = time.perf_counter() - t
+    if st != 0 or st2 != 0:
+        raise RuntimeError("oracle failed on the benchmark workload")
+    return dt
+
+
+def step_bytes(case) -> int:
+    s = case.spec
+    return (algorithmic_bytes(case.context_lens.cpu(), s.num_q_heads, s.num_kv_heads, s.head_dim)
+            + append_bytes(int(case.slot_mapping.numel()), s.num_kv_heads, s.head_dim))
+
+
+def cpu_baseline(case_cpu, target_s: float = 10.0, max_s: float = 30.0) -> dict:
+    threads = os.cpu_count() or 1
+    b = step_bytes(case_cpu)
+    times = []
+    t_start = time.perf_counter()
+    while True:
+        times.append(oracle_step_seconds(case_cpu, threads))
+        el = time.perf_counter() - t_start
+        if el >= target_s or el + times[-1] > max_s:
+            break
+    total = sum(times)
+    return {"value": round(b * len(times) / total / 1e9, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+            "sample": f"the full {case_cpu.spec.name} step (append + attention, all {case_cpu.spec.num_seqs} "
+                      f"sequences x {case_cpu.spec.num_q_heads} q heads) repeated {len(times)} times, fp64, "
+                      f"{threads} threads, {total:.1f} s",
+            "seconds_per_step": round(total / len(times), 4)}
+
+
+def run_reference(args, dist: Dist) -> dict | None:
+    """Reference arm: the fp64 CPU oracle on the host cores, rank 0 only."""
+    if dist.rank != 0:
+        return None
+    threads = os.cpu_count() or 1
+    spec = SPECS[args.workload]
+    # A bounded sample of the workload per step: the first n sequences (all q heads), with n sized so
+    # that the whole --warmup + --steps run stays near --reference-budget seconds (at most 1 s a step).
+    case = make_decode_case(args.workload, seed=0, num_seqs=spec.num_seqs)
+    probe = make_decode_case(args.workload, seed=0, lengths=case.context_lens[:8].tolist())
+    per_seq = oracle_step_seconds(probe, threads) / 8
+    budget = min(1.0, args.reference_budget / (args.steps + args.warmup))
+    n = max(1, min(spec.num_seqs, int(budget / max(per_seq, 1e-9))))
+    sample = make_decode_case(args.workload, seed=0, lengths=case.context_lens[:n].tolist())
+    for _ in range(args.warmup):
+        oracle_step_seconds(sample, threads)
+    secs = [oracle_step_seconds(sample, threads) for _ in range(args.steps)]
+    total = sum(secs)
+    b = step_bytes(sample)
+    value = b * args.steps / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, "sample_seqs": n, "num_q_heads": spec.num_q_heads,
+                   "num_kv_heads": spec.num_kv_heads, "head_dim": spec.head_dim, "block_size": 16},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
+                         "sample": f"first {n} of {spec.num_seqs} {args.workload} sequences (all q heads) per step"},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "seq_layer_per_s": round(n * args.steps / total, 2),
+    }
+    return line
+
+
+# ---------------------------------------------------------------------------
+# GPU side
+# ---------------------------------------------------------------------------
+def run_ours(args, dist: Dist) -> dict | None:
+    import numpy as np
+
+    import paged_kv_cache_275_gb300 as pkv
+    from paged_kv_cache_275_gb300 import build as _build
+    _build.build(quiet=True)
+    pkv.load()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device for --impl ours")
+    dev = torch.device("cuda", dist.local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    case_cpu = make_decode_case(args.workload, seed=0)
+    spec = case_cpu.spec
+    B, hq, hkv, D = spec.num_seqs, spec.num_q_heads, spec.num_kv_heads, spec.head_dim
+    g = case_cpu.to(dev)
+    out = torch.empty_like(g.q)
+    parts = args.partitions or pkv.default_partitions(B, hq, hkv, D, spec.max_blocks_per_seq)
+    ws = torch.empty(pkv.workspace_size(B, hq, hkv, D, spec.max_blocks_per_seq, parts), dtype=torch.uint8,
+                     device=dev)
+    pool_bytes = 2 * g.k_cache.numel() * 2
+
+    def append():
+        pkv.kv_append(g.new_k, g.new_v, g.slot_mapping, g.k_cache, g.v_cache, stream=stream)
+
+    def attend(phases):
+        pkv.paged_decode_attention(g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens, g.scale, out,
+                                   num_partitions=parts, phases=phases, workspace=ws, stream=stream)
+
+    # Parity on the same inputs before timing (sampled outputs against the oracle).
+    with torch.cuda.stream(stream):
+        append()
+        attend(pkv.PHASE_ALL)
+    stream.synchronize()
+    if pkv.get_and_clear_device_error(stream) != 0:
+        raise RuntimeError("device error during the parity run")
+    parity = None
+    if dist.rank == 0:
+        import oracle
+        kc, vc = case_cpu.k_cache.clone(), case_cpu.v_cache.clone()
+        oracle.kv_append(case_cpu.new_k, case_cpu.new_v, case_cpu.slot_mapping, kc, vc)
+        append_exact = bool(torch.equal(g.k_cache.cpu().view(torch.int16), kc.view(torch.int16))
+                            and torch.equal(g.v_cache.cpu().view(torch.int16), vc.view(torch.int16)))
+        rng = np.random.default_rng(0)
+        si = rng.integers(0, B, 256).astype(np.int32)
+        hi = rng.integers(0, hq, 256).astype(np.int32)
+        ref, st = oracle.paged_decode_sampled(case_cpu.q, kc, vc, case_cpu.block_tables, case_cpu.context_lens,
+                                              case_cpu.scale, si, hi)
+        got = out.cpu().to(torch.float64).numpy()[si, hi]
+        diff = got - ref
+        parity = {"append_bit_exact": append_exact, "sampled_outputs": int(si.size),
+                  "max_abs": float(np.abs(diff).max()),
+                  "rel_rms": float(np.sqrt(np.mean(diff ** 2)) / np.sqrt(np.mean(ref ** 2)))}
+        if not append_exact or st != 0 or parity["max_abs"] > 1e-2 or parity["rel_rms"] > 5e-3:
+            raise RuntimeError(f"parity check failed before timing: {parity}")
+        del kc, vc
+
+    bytes_attn = algorithmic_bytes(case_cpu.context_lens, hq, hkv, D)
+    bytes_step = bytes_attn + append_bytes(B, hkv, D)
+
+    def step(ev=None, i=0):
+        append()
+        if ev is not None:
+            ev[0][i].record(stream)
+        attend(pkv.PHASE_PARTITION)
+        if ev is not None:
+            ev[1][i].record(stream)
+        attend(pkv.PHASE_MERGE)
+
+    K, W = args.steps, args.warmup
+    sampler = ClockSampler(nvidia_smi_id(dev))
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            step()
+    stream.synchronize()
+    ev_part = ([torch.cuda.Event(enable_timing=True) for _ in range(K)],
+               [torch.cuda.Event(enable_timing=True) for _ in range(K)])
+    t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = pkv.kernel_launch_count()
+    dist.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    with torch.cuda.stream(stream):
+        t_begin.record(stream)
+        for i in range(K):
+            step(ev_part, i)
+        t_end.record(stream)
+    stream.synchronize()
+    torch.cuda.synchronize()
+    dist.barrier()
+    wall1 = time.time()
+    launches = pkv.kernel_launch_count() - launches0
+    elapsed = t_begin.elapsed_time(t_end) / 1e3
+    part_ms = [ev_part[0][i].elapsed_time(ev_part[1][i]) for i in range(K)]
+    if pkv.get_and_clear_device_error(stream) != 0:
+        raise RuntimeError("device error during the timed region")
+
+    # End to end through the public API: pinned host inputs in, output back to pinned host memory.
+    host = {name: getattr(case_cpu, name).pin_memory() for name in
+            ("q", "new_k", "new_v", "slot_mapping", "block_tables", "context_lens")}
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    dev_in = {name: getattr(g, name) for name in host}
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for name, t in host.items():
+            dev_in[name].copy_(t, non_blocking=True)
+        append()
+        attend(pkv.PHASE_ALL)
+        out_host.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            e2e_step()
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(K):
+            e2e_step()
+        e1.record(stream)
+    stream.synchronize()
+    dist.barrier()
+    e2e_elapsed = e0.elapsed_time(e1) / 1e3
+    if not torch.equal(out_host, out.cpu()):
+        raise RuntimeError("e2e output read-back mismatch")
+    rows = sampler.stop() if sampler else []
+
+    value, slowest = aggregate(bytes_step * K, elapsed, dist)
+    e2e_value, _ = aggregate(bytes_step * K, e2e_elapsed, dist)
+    seqs, _ = aggregate(B * K, elapsed, dist)
+    if dist.rank != 0:
+        return None
+
+    peak, peak_kind = peaks()
+    part_mean_s = statistics.fmean(part_ms) / 1e3
+    achieved = bytes_attn / part_mean_s / 1e9
+    clocks = ClockSampler.summarize(rows, wall0, wall1)
+    cpu = cpu_baseline(case_cpu, target_s=args.cpu_seconds) if args.cpu_seconds > 0 else None
+    line = {
+        "metric": METRIC, "value": round(value / 1e9, 2), "unit": UNIT, "n_gpus": dist.world, "steps": K,
+        "warmup": W, "ms_per_step": round(1e3 * slowest / K, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{spec.name}: {spec.description}", "num_seqs": B, "num_q_heads": hq,
+                   "num_kv_heads": hkv, "head_dim": D, "block_size": 16,
+                   "mean_context_len": round(float(case_cpu.context_lens.float().mean()), 1),
+                   "kv_pool_bytes": pool_bytes, "num_partitions": parts,
+                   "l2": f"inputs larger than L2: the {pool_bytes / 1e9:.2f} GB K/V pool streams through the "
+                         f"{L2_BYTES >> 20} MiB L2 every step; no flush",
+                   "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "single GPU"},
+        "pct_of_peak": {"measured": round(100 * value / 1e9 / peak, 2), "nominal_8TBps": round(
+            100 * value / 1e9 / NOMINAL_HBM_GBS, 2), "peak_kind": peak_kind},
+        "seq_layer_per_s": round(seqs, 1),
+        "step_bytes": bytes_step,
+        "roofline": {"kernel": "paged_decode_partition_kernel", "bound": "hbm", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "frac_of": f"{peak_kind} HBM copy bandwidth", "frac_nominal_8TBps": round(
+                         achieved / NOMINAL_HBM_GBS, 4),
+                     "traffic": args.traffic, "algorithmic_bytes_per_launch": bytes_attn,
+                     "mean_launch_us": round(part_mean_s * 1e6, 2)},
+        "e2e": {"value": round(e2e_value / 1e9, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * e2e_elapsed / K, 4)},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "parity": parity,
+        "cpu_baseline": cpu,
+    }
+    return line
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=sorted(SPECS), default="llama3_8b")
+    ap.add_argument("--partitions", type=int, default=0, help="num_partitions (0 = the library default)")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="CPU-baseline budget (0 skips it)")
+    ap.add_argument("--reference-budget", type=float, default=120.0,
+                    help="seconds the reference arm's warm-up + timed steps should take")
+    ap.add_argument("--traffic", type=float, default=None,
+                    help="DRAM bytes per partition launch from an ncu capture of the current kernel")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    dist = Dist()
+    try:
+        line = run_reference(args, dist) if args.impl == "reference" else run_ours(args, dist)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+    finally:
+        dist.close()
+    return 0
+
+
+if __name__ == "__main__":
+    raise SystemExit(main())

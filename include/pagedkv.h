@@ -1,0 +1,193 @@
+/*
+ * pagedkv.h -- C ABI of the paged KV-cache hot path on one GB300 (sm_103a).
+ *
+ * Two operations, after the pages on a mini vLLM inference engine:
+ *
+ *   kv_append               "从零实现一个 mini vLLM--开篇", section 2
+ *                           ("LLM 推理到底在慢什么"): in decode only the new
+ *                           token's K and V are computed and appended to the
+ *                           cache.  The cache is cut into fixed 16-token
+ *                           blocks ("跟着 Claude Code，我用 Python 实现了一个
+ *                           轻量级的 vLLM", section "核心机制一：分页 KV Cache").
+ *   paged_decode_attention  the same series, section 5 (phases 4 and 5): a
+ *                           request owns a block table; its tokens are
+ *                           logically contiguous and physically scattered, and
+ *                           attention finds the real K and V through the block
+ *                           table; every decode step attends over all cached
+ *                           tokens (section 2).  The result is the plain
+ *                           definition softmax(scale * q K^T) V per q head.
+ *
+ * Conventions (all tensors row-major and contiguous, caller-owned device
+ * memory; the library allocates nothing and keeps no pointer after a call):
+ *
+ *   block size         16 tokens (PKV_BLOCK_SIZE); other values are rejected.
+ *   k_cache, v_cache   bf16 [num_blocks][num_kv_heads][16][head_dim]: one
+ *                      (block, kv head) tile is one contiguous 16 * head_dim
+ *                      run.  Slot s is block s / 16, offset s % 16.
+ *   head_dim           64 or 128.
+ *   GQA                q head h reads kv head h / (num_q_heads / num_kv_heads);
+ *                      num_q_heads / num_kv_heads must be 1, 2, 4 or 8.
+ *   q, out             bf16 [num_seqs][num_q_heads][head_dim].
+ *   block_tables       int32 [num_seqs][max_blocks_per_seq]; entries past
+ *                      ceil(context_len / 16) are never read (may hold -1).
+ *   context_lens       int32 [num_seqs]: number of cached tokens of each
+ *                      sequence, including the token appended in this step
+ *                      (append first, then attend; no mask).
+ *   arithmetic         bf16 inputs widened exactly to fp32, fp32 accumulation
+ *                      and online softmax, one round-to-nearest-even to bf16.
+ *   alignment          every pointer argument 16-byte aligned.
+ *   streams            every call only enqueues work on `stream` (a
+ *                      cudaStream_t; NULL means the legacy default stream) and
+ *                      never synchronises, except
+ *                      pkv_get_and_clear_device_error.  The current CUDA
+ *                      device must own every pointer.
+ *
+ * Errors.  A call returns PKV_OK or an error status; on error nothing was
+ * enqueued and pkv_last_error_message() (per host thread) says why.
+ * Conditions only the device can see (a slot past the pool, a block id
+ * outside [0, num_blocks), a context length outside [0, 16 * max_blocks_per_seq],
+ * a pipeline wait that ran out of time) never fault: the element is skipped
+ * or clamped, its output is unspecified, and a bit is set in a sticky
+ * per-device error word that pkv_get_and_clear_device_error() returns.
+ */
+#ifndef PAGEDKV_H
+#define PAGEDKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PKV_BLOCK_SIZE 16
+
+typedef enum pkv_status {
+    PKV_OK = 0,
+    PKV_ERR_INVALID_ARGUMENT = 1, /* null / misaligned pointer, bad size, workspace too small */
+    PKV_ERR_UNSUPPORTED = 2,      /* head_dim, GQA group, block size or batch outside what is built */
+    PKV_ERR_CUDA = 3              /* a CUDA runtime call failed (message has the CUDA error) */
+} pkv_status;
+
+/* Bits of the sticky device error word. */
+#define PKV_DEVERR_SLOT_OUT_OF_RANGE 0x1u     /* kv_append: slot >= 16 * num_blocks (token skipped) */
+#define PKV_DEVERR_BLOCK_ID_OUT_OF_RANGE 0x2u /* attention: table entry outside [0, num_blocks) (block 0 read instead) */
+#define PKV_DEVERR_CONTEXT_LEN_NEGATIVE 0x4u  /* attention: context_len < 0 (treated as 0) */
+#define PKV_DEVERR_CONTEXT_LEN_TOO_LONG 0x8u  /* attention: context_len > 16 * max_blocks_per_seq (clamped) */
+#define PKV_DEVERR_PIPELINE_TIMEOUT 0x10u     /* attention: a shared-memory pipeline wait gave up (partition skipped) */
+
+/* Largest num_seqs one attention call accepts. */
+#define PKV_MAX_SEQS 4096
+
+/* Phases of one attention call (see pkv_paged_decode_attention_split). */
+#define PKV_PHASE_PARTITION 0x1
+#define PKV_PHASE_MERGE 0x2
+#define PKV_PHASE_ALL 0x3
+
+typedef struct CUstream_st* pkv_stream_t; /* the same type as cudaStream_t */
+
+/*
+ * Append this step's K and V into their paged slots.
+ *
+ * For every token i in [0, num_tokens) with s = slot_mapping[i] >= 0 and every
+ * kv head h, copies the bits of k[i][h][:] into k_cache[s / 16][h][s % 16][:]
+ * and v[i][h][:] into v_cache[s / 16][h][s % 16][:].  A negative slot is
+ * padding and is skipped.  Slots must be distinct (duplicates give an
+ * unspecified one of the writes).  Bit-exact: no arithmetic on the values.
+ *
+ *   k, v          device, bf16 [num_tokens][num_kv_heads][head_dim]
+ *   slot_mapping  device, int64 [num_tokens]
+ *   k_cache, v_cache  device, bf16 [num_blocks][num_kv_heads][16][head_dim], written in place
+ *   block_size    must be 16
+ *
+ * num_tokens == 0 is a no-op.  Device-side: slot >= 16 * num_blocks sets
+ * PKV_DEVERR_SLOT_OUT_OF_RANGE and the token is skipped.
+ */
+pkv_status pkv_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                         int32_t num_kv_heads, int32_t head_dim, void* k_cache, void* v_cache,
+                         int64_t num_blocks, int32_t block_size, pkv_stream_t stream);
+
+/*
+ * Bytes of device workspace one attention call needs.
+ *
+ * num_partitions is the number of contiguous, equal-length pieces the whole
+ * batch's (sequence, kv head, block) stream is cut into (one warp each; a
+ * piece that covers only part of a (sequence, kv head) pair leaves a partial
+ * softmax state that the merge phase combines).  0 picks the default for the
+ * current device: the number of warps the GPU keeps resident.  The same
+ * num_partitions must be passed to the attention call.  Requires a CUDA device
+ * when num_partitions == 0.
+ */
+pkv_status pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t head_dim, int32_t max_blocks_per_seq, int32_t num_partitions,
+                                     size_t* bytes);
+
+/* The default num_partitions for these shapes on the current device (what 0 means). */
+pkv_status pkv_decode_default_partitions(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t max_blocks_per_seq,
+                                         int32_t* num_partitions);
+
+/*
+ * Paged decode attention:
+ *
+ *   out[b][h][:] = sum_t softmax_t(scale * <q[b][h], K_t>) * V_t,   t < context_lens[b]
+ *   K_t = k_cache[block_tables[b][t / 16]][h / G][t % 16][:]  (G = num_q_heads / num_kv_heads)
+ *   V_t = v_cache[block_tables[b][t / 16]][h / G][t % 16][:]
+ *
+ * context_lens[b] == 0 writes zeros.  num_seqs == 0 is a no-op.
+ *
+ *   q             device, bf16 [num_seqs][num_q_heads][head_dim]
+ *   k_cache, v_cache  device, bf16 [num_blocks][num_kv_heads][16][head_dim]
+ *   block_tables  device, int32 [num_seqs][max_blocks_per_seq]
+ *   context_lens  device, int32 [num_seqs]
+ *   out           device, bf16 [num_seqs][num_q_heads][head_dim] (written)
+ *   workspace     device scratch of at least pkv_decode_workspace_size(..., 0, ...)
+ *                 bytes, 16-byte aligned, owned by the caller; its contents
+ *                 are scratch and need no initialisation.  Two calls that
+ *                 may run concurrently need two workspaces.
+ *
+ * Enqueues two kernels: the partition kernel (every warp streams one piece of
+ * the batch's block stream through a TMA-fed shared-memory ring and writes a
+ * finished output row or a partial softmax state) and the merge kernel.
+ */
+pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
+                                      int32_t block_size, float scale, void* out, void* workspace,
+                                      size_t workspace_bytes, pkv_stream_t stream);
+
+/*
+ * The same call with an explicit num_partitions (> 0, or 0 for the default)
+ * and a phase mask.  PKV_PHASE_PARTITION enqueues only the partition kernel,
+ * PKV_PHASE_MERGE only the merge kernel (which reads what the partition phase
+ * left in the workspace, so it must follow a partition phase with identical
+ * arguments on the same workspace), PKV_PHASE_ALL both.  The result does not
+ * depend on num_partitions beyond fp32 rounding.
+ */
+pkv_status pkv_paged_decode_attention_split(const void* q, const void* k_cache, const void* v_cache,
+                                            const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                            const int32_t* context_lens, int32_t num_seqs,
+                                            int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                            int64_t num_blocks, int32_t block_size, float scale, void* out,
+                                            void* workspace, size_t workspace_bytes, int32_t num_partitions,
+                                            int32_t phases, pkv_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's sticky
+ * error word (a mask of PKV_DEVERR_* bits; 0 = no device-side error since the
+ * last clear).
+ */
+pkv_status pkv_get_and_clear_device_error(uint32_t* bits, pkv_stream_t stream);
+
+/* Message of the last failed call on this host thread ("" if none).  Valid until the next call. */
+const char* pkv_last_error_message(void);
+
+/* Number of kernels this library has launched in this process (all devices). */
+uint64_t pkv_kernel_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDKV_H */

@@ -1,0 +1,219 @@
+"""ctypes binding of libpagedkv.so (include/pagedkv.h).
+
+Argument marshalling only: shapes are read from the tensors, pointers and the
+current CUDA stream are passed through, and every step of the computation
+runs in the library's kernels.  There is no CPU or PyTorch fallback: if the
+library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+from pathlib import Path
+
+import torch
+
+_PKG = Path(__file__).resolve().parent
+LIB_PATH = _PKG / "libpagedkv.so"
+
+OK = 0
+ERR_INVALID_ARGUMENT = 1
+ERR_UNSUPPORTED = 2
+ERR_CUDA = 3
+STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARGUMENT", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_CUDA"}
+
+DEVERR_SLOT_OUT_OF_RANGE = 0x1
+DEVERR_BLOCK_ID_OUT_OF_RANGE = 0x2
+DEVERR_CONTEXT_LEN_NEGATIVE = 0x4
+DEVERR_CONTEXT_LEN_TOO_LONG = 0x8
+DEVERR_PIPELINE_TIMEOUT = 0x10
+
+PHASE_PARTITION = 1
+PHASE_MERGE = 2
+PHASE_ALL = 3
+
+BLOCK_SIZE = 16
+MAX_SEQS = 4096
+
+# Every exported symbol of include/pagedkv.h.
+EXPORTS = (
+    "pkv_kv_append",
+    "pkv_decode_workspace_size",
+    "pkv_decode_default_partitions",
+    "pkv_paged_decode_attention",
+    "pkv_paged_decode_attention_split",
+    "pkv_get_and_clear_device_error",
+    "pkv_last_error_message",
+    "pkv_kernel_launch_count",
+)
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def load(path: Path | str | None = None) -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None and path is None:
+            return _lib
+        p = Path(path) if path else LIB_PATH
+        if not p.exists():
+            raise ImportError(f"{p} is missing: build it with `python -m paged_kv_cache_275_gb300.build` "
+                              "(there is no fallback path)")
+        lib = ctypes.CDLL(str(p))
+        V, I32, I64, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+        lib.pkv_kv_append.argtypes = [V, V, V, I64, I32, I32, V, V, I64, I32, V]
+        lib.pkv_decode_workspace_size.argtypes = [I32, I32, I32, I32, I32, I32, ctypes.POINTER(SZ)]
+        lib.pkv_decode_default_partitions.argtypes = [I32, I32, I32, I32, I32, ctypes.POINTER(I32)]
+        lib.pkv_paged_decode_attention.argtypes = [V, V, V, V, I32, V, I32, I32, I32, I32, I64, I32,
+                                                   ctypes.c_float, V, V, SZ, V]
+        lib.pkv_paged_decode_attention_split.argtypes = [V, V, V, V, I32, V, I32, I32, I32, I32, I64, I32,
+                                                         ctypes.c_float, V, V, SZ, I32, I32, V]
+        lib.pkv_get_and_clear_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), V]
+        for name in ("pkv_kv_append", "pkv_decode_workspace_size", "pkv_decode_default_partitions",
+                     "pkv_paged_decode_attention", "pkv_paged_decode_attention_split",
+                     "pkv_get_and_clear_device_error"):
+            getattr(lib, name).restype = ctypes.c_int
+        lib.pkv_last_error_message.argtypes = []
+        lib.pkv_last_error_message.restype = ctypes.c_char_p
+        lib.pkv_kernel_launch_count.argtypes = []
+        lib.pkv_kernel_launch_count.restype = ctypes.c_uint64
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _check(status: int) -> None:
+    if status != OK:
+        msg = load().pkv_last_error_message().decode(errors="replace")
+        raise PagedKVError(status, msg)
+
+
+def _stream_handle(stream: torch.cuda.Stream | None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _require(t: torch.Tensor, name: str, dtype: torch.dtype, ndim: int, device: torch.device | None = None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got shape {tuple(t.shape)}")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def kv_append(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor, k_cache: torch.Tensor,
+              v_cache: torch.Tensor, stream: torch.cuda.Stream | None = None) -> None:
+    """Scatter k/v [N, Hkv, D] bf16 into k_cache/v_cache [NB, Hkv, 16, D] at slot_mapping [N] int64 (in place)."""
+    _require(k_cache, "k_cache", torch.bfloat16, 4)
+    dev = k_cache.device
+    _require(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _require(k, "k", torch.bfloat16, 3, dev)
+    _require(v, "v", torch.bfloat16, 3, dev)
+    _require(slot_mapping, "slot_mapping", torch.int64, 1, dev)
+    nb, hkv, bs, d = k_cache.shape
+    if v_cache.shape != k_cache.shape:
+        raise ValueError("k_cache and v_cache shapes differ")
+    n = slot_mapping.shape[0]
+    if k.shape != (n, hkv, d) or v.shape != (n, hkv, d):
+        raise ValueError(f"k/v must be [{n}, {hkv}, {d}], got {tuple(k.shape)} / {tuple(v.shape)}")
+    with torch.cuda.device(dev):
+        _check(load().pkv_kv_append(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), n, hkv, d,
+                                    k_cache.data_ptr(), v_cache.data_ptr(), nb, bs, _stream_handle(stream)))
+
+
+def workspace_size(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int, max_blocks_per_seq: int,
+                   num_partitions: int = 0) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().pkv_decode_workspace_size(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                            num_partitions, ctypes.byref(out)))
+    return int(out.value)
+
+
+def default_partitions(num_seqs: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                       max_blocks_per_seq: int) -> int:
+    out = ctypes.c_int32(0)
+    _check(load().pkv_decode_default_partitions(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq,
+                                                ctypes.byref(out)))
+    return int(out.value)
+
+
+# One scratch buffer per (device, stream): calls on one stream run in order and may share it.
+_workspaces: dict[tuple[int, int], torch.Tensor] = {}
+
+
+def _workspace(device: torch.device, stream_handle: int, nbytes: int) -> torch.Tensor:
+    key = (device.index, stream_handle)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                           out: torch.Tensor, *, num_partitions: int = 0, phases: int = PHASE_ALL,
+                           workspace: torch.Tensor | None = None, stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """out[b, h] = softmax(scale * q[b, h] K^T) V over context_lens[b] tokens found through block_tables[b].
+
+    q, out: [B, Hq, D] bf16; k_cache, v_cache: [NB, Hkv, 16, D] bf16; block_tables: [B, W] int32;
+    context_lens: [B] int32.  Returns ``out``.
+    """
+    _require(q, "q", torch.bfloat16, 3)
+    dev = q.device
+    _require(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _require(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _require(block_tables, "block_tables", torch.int32, 2, dev)
+    _require(context_lens, "context_lens", torch.int32, 1, dev)
+    _require(out, "out", torch.bfloat16, 3, dev)
+    B, hq, d = q.shape
+    nb, hkv, bs, d2 = k_cache.shape
+    if v_cache.shape != k_cache.shape or d2 != d:
+        raise ValueError("cache shapes do not match q")
+    if out.shape != q.shape:
+        raise ValueError("out must have the shape of q")
+    if block_tables.shape[0] != B or context_lens.shape[0] != B:
+        raise ValueError("block_tables / context_lens batch mismatch")
+    W = block_tables.shape[1]
+    lib = load()
+    with torch.cuda.device(dev):
+        sh = _stream_handle(stream)
+        if B == 0:
+            return out
+        nbytes = workspace_size(B, hq, hkv, d, W, num_partitions)
+        if workspace is None:
+            workspace = _workspace(dev, sh, nbytes)
+        elif workspace.device != dev or workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError(f"workspace must be a {nbytes}-byte buffer on {dev}")
+        wsize = workspace.numel() * workspace.element_size()
+        _check(lib.pkv_paged_decode_attention_split(
+            q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), W,
+            context_lens.data_ptr(), B, hq, hkv, d, nb, bs, float(scale), out.data_ptr(), workspace.data_ptr(),
+            wsize, num_partitions, phases, sh))
+    return out
+
+
+def get_and_clear_device_error(stream: torch.cuda.Stream | None = None) -> int:
+    bits = ctypes.c_uint32(0)
+    _check(load().pkv_get_and_clear_device_error(ctypes.byref(bits), _stream_handle(stream)))
+    return int(bits.value)
+
+
+def kernel_launch_count() -> int:
+    return int(load().pkv_kernel_launch_count())

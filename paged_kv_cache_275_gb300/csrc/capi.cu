@@ -1,0 +1,294 @@
+// C ABI of the paged KV-cache hot path (declared in include/pagedkv.h).
+//
+// Host-side only: argument validation (every host-checkable error returns
+// before anything is enqueued), workspace layout, the default partition
+// count, kernel dispatch on the caller's stream, the per-device sticky error
+// word, and the per-thread error message.  No call allocates device memory.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "pagedkv.h"
+#include "pkv_internal.h"
+
+// Sticky device error word; one instance per device (module-scope __device__).
+static __device__ unsigned int g_pkv_device_error;
+
+namespace {
+
+thread_local char t_message[512] = "";
+std::atomic<uint64_t> g_launches{0};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_device_mu;
+unsigned* g_error_word[kMaxDevices] = {};
+int g_sm_count[kMaxDevices] = {};
+
+pkv_status fail(pkv_status status, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_message, sizeof t_message, fmt, ap);
+  va_end(ap);
+  return status;
+}
+
+pkv_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(PKV_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorString(e), cudaGetErrorName(e));
+}
+
+pkv_status ok() {
+  t_message[0] = '\0';
+  return PKV_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Error word address and SM count of the current device, looked up once per device.
+pkv_status device_state(unsigned** err, int* sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(PKV_ERR_UNSUPPORTED, "device ordinal %d out of range", dev);
+  std::lock_guard<std::mutex> lock(g_device_mu);
+  if (!g_error_word[dev]) {
+    void* addr = nullptr;
+    if ((e = cudaGetSymbolAddress(&addr, g_pkv_device_error)) != cudaSuccess)
+      return cuda_fail(e, "cudaGetSymbolAddress(device error word)");
+    int count = 0;
+    if ((e = cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute(multiProcessorCount)");
+    g_sm_count[dev] = count;
+    g_error_word[dev] = static_cast<unsigned*>(addr);
+  }
+  if (err) *err = g_error_word[dev];
+  if (sms) *sms = g_sm_count[dev];
+  return PKV_OK;
+}
+
+// Shape checks shared by the workspace query and the attention call.
+pkv_status check_decode_shapes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t max_blocks_per_seq) {
+  if (num_seqs < 0) return fail(PKV_ERR_INVALID_ARGUMENT, "num_seqs must be >= 0 (got %d)", num_seqs);
+  if (num_seqs > PKV_MAX_SEQS)
+    return fail(PKV_ERR_UNSUPPORTED, "num_seqs %d exceeds PKV_MAX_SEQS (%d)", num_seqs, PKV_MAX_SEQS);
+  if (num_q_heads <= 0 || num_kv_heads <= 0)
+    return fail(PKV_ERR_INVALID_ARGUMENT, "head counts must be positive (q %d, kv %d)", num_q_heads, num_kv_heads);
+  if (num_q_heads % num_kv_heads != 0)
+    return fail(PKV_ERR_INVALID_ARGUMENT, "num_q_heads %d is not a multiple of num_kv_heads %d", num_q_heads,
+                num_kv_heads);
+  const int group = num_q_heads / num_kv_heads;
+  if (group != 1 && group != 2 && group != 4 && group != 8)
+    return fail(PKV_ERR_UNSUPPORTED, "GQA group %d not built (1, 2, 4 or 8)", group);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim %d not built (64 or 128)", head_dim);
+  if (max_blocks_per_seq <= 0)
+    return fail(PKV_ERR_INVALID_ARGUMENT, "max_blocks_per_seq must be positive (got %d)", max_blocks_per_seq);
+  if (static_cast<int64_t>(num_seqs) * max_blocks_per_seq * num_kv_heads >= (int64_t{1} << 31) ||
+      static_cast<int64_t>(max_blocks_per_seq) * PKV_BLOCK_SIZE >= (int64_t{1} << 31))
+    return fail(PKV_ERR_UNSUPPORTED, "num_seqs * max_blocks_per_seq * num_kv_heads must stay below 2^31");
+  return PKV_OK;
+}
+
+constexpr int32_t kMaxPartitions = 1 << 20;
+
+pkv_status default_partitions(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim, int32_t group,
+                              int32_t max_blocks_per_seq, int32_t* out) {
+  int warps = 0;
+  const cudaError_t e = pkv::resident_partition_warps(head_dim, group, num_seqs, &warps);
+  if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
+  // Never more pieces than the block stream can have items.
+  const int64_t bound = static_cast<int64_t>(num_seqs) * num_kv_heads * max_blocks_per_seq;
+  int64_t n = warps;
+  if (n > bound) n = bound;
+  if (n > kMaxPartitions) n = kMaxPartitions;
+  if (n < 1) n = 1;
+  *out = static_cast<int32_t>(n);
+  return PKV_OK;
+}
+
+size_t workspace_bytes_for(int32_t num_seqs, int32_t head_dim, int32_t group, int32_t num_partitions) {
+  return pkv::workspace_header_bytes(num_seqs) +
+         static_cast<size_t>(num_partitions) * 2 * pkv::piece_floats(head_dim, group) * sizeof(float);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* pkv_last_error_message(void) { return t_message; }
+
+uint64_t pkv_kernel_launch_count(void) { return g_launches.load(); }
+
+pkv_status pkv_kv_append(const void* k, const void* v, const int64_t* slot_mapping, int64_t num_tokens,
+                         int32_t num_kv_heads, int32_t head_dim, void* k_cache, void* v_cache, int64_t num_blocks,
+                         int32_t block_size, pkv_stream_t stream) {
+  if (num_tokens < 0) return fail(PKV_ERR_INVALID_ARGUMENT, "num_tokens must be >= 0 (got %lld)", (long long)num_tokens);
+  if (num_kv_heads <= 0) return fail(PKV_ERR_INVALID_ARGUMENT, "num_kv_heads must be positive (got %d)", num_kv_heads);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim %d not built (64 or 128)", head_dim);
+  if (block_size != PKV_BLOCK_SIZE)
+    return fail(PKV_ERR_UNSUPPORTED, "block_size must be %d (got %d)", PKV_BLOCK_SIZE, block_size);
+  if (num_blocks <= 0 || num_blocks > (int64_t{1} << 40))
+    return fail(PKV_ERR_INVALID_ARGUMENT, "num_blocks out of range (got %lld)", (long long)num_blocks);
+  if (num_tokens > (int64_t{1} << 32))
+    return fail(PKV_ERR_UNSUPPORTED, "num_tokens %lld too large", (long long)num_tokens);
+  if (num_tokens == 0) return ok();
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache)
+    return fail(PKV_ERR_INVALID_ARGUMENT, "null pointer argument");
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return fail(PKV_ERR_INVALID_ARGUMENT, "k, v and the caches must be 16-byte aligned, slot_mapping 8-byte aligned");
+  unsigned* err = nullptr;
+  int sms = 0;
+  if (pkv_status st = device_state(&err, &sms); st != PKV_OK) return st;
+  pkv::AppendParams p{};
+  p.k = k;
+  p.v = v;
+  p.slot_mapping = slot_mapping;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.err = err;
+  p.num_tokens = num_tokens;
+  p.num_slots = num_blocks * PKV_BLOCK_SIZE;
+  p.num_kv_heads = num_kv_heads;
+  p.head_dim = head_dim;
+  const cudaError_t e = pkv::launch_kv_append(p, sms, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "kv_append launch");
+  g_launches.fetch_add(1);
+  return ok();
+}
+
+pkv_status pkv_decode_default_partitions(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                         int32_t head_dim, int32_t max_blocks_per_seq, int32_t* num_partitions) {
+  if (!num_partitions) return fail(PKV_ERR_INVALID_ARGUMENT, "num_partitions is null");
+  if (pkv_status st = check_decode_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
+      st != PKV_OK)
+    return st;
+  if (pkv_status st = default_partitions(num_seqs, num_kv_heads, head_dim, num_q_heads / num_kv_heads,
+                                         max_blocks_per_seq, num_partitions);
+      st != PKV_OK)
+    return st;
+  return ok();
+}
+
+pkv_status pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                     int32_t max_blocks_per_seq, int32_t num_partitions, size_t* bytes) {
+  if (!bytes) return fail(PKV_ERR_INVALID_ARGUMENT, "bytes is null");
+  if (pkv_status st = check_decode_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
+      st != PKV_OK)
+    return st;
+  if (num_partitions < 0 || num_partitions > kMaxPartitions)
+    return fail(PKV_ERR_INVALID_ARGUMENT, "num_partitions out of range (got %d)", num_partitions);
+  const int group = num_q_heads / num_kv_heads;
+  if (num_partitions == 0) {
+    if (pkv_status st = default_partitions(num_seqs, num_kv_heads, head_dim, group, max_blocks_per_seq,
+                                           &num_partitions);
+        st != PKV_OK)
+      return st;
+  }
+  *bytes = workspace_bytes_for(num_seqs, head_dim, group, num_partitions);
+  return ok();
+}
+
+pkv_status pkv_paged_decode_attention_split(const void* q, const void* k_cache, const void* v_cache,
+                                            const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                            const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                            int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
+                                            int32_t block_size, float scale, void* out, void* workspace,
+                                            size_t workspace_bytes, int32_t num_partitions, int32_t phases,
+                                            pkv_stream_t stream) {
+  if (pkv_status st = check_decode_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
+      st != PKV_OK)
+    return st;
+  if (block_size != PKV_BLOCK_SIZE)
+    return fail(PKV_ERR_UNSUPPORTED, "block_size must be %d (got %d)", PKV_BLOCK_SIZE, block_size);
+  if (num_blocks <= 0 || num_blocks > (int64_t{1} << 40))
+    return fail(PKV_ERR_INVALID_ARGUMENT, "num_blocks out of range (got %lld)", (long long)num_blocks);
+  if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID_ARGUMENT, "scale must be finite");
+  if (phases < 1 || phases > PKV_PHASE_ALL) return fail(PKV_ERR_INVALID_ARGUMENT, "phases must be 1, 2 or 3");
+  if (num_partitions < 0 || num_partitions > kMaxPartitions)
+    return fail(PKV_ERR_INVALID_ARGUMENT, "num_partitions out of range (got %d)", num_partitions);
+  if (num_seqs == 0) return ok();
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace)
+    return fail(PKV_ERR_INVALID_ARGUMENT, "null pointer argument");
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+    return fail(PKV_ERR_INVALID_ARGUMENT, "q, caches, out and workspace must be 16-byte aligned");
+  const int group = num_q_heads / num_kv_heads;
+  if (num_partitions == 0) {
+    if (pkv_status st = default_partitions(num_seqs, num_kv_heads, head_dim, group, max_blocks_per_seq,
+                                           &num_partitions);
+        st != PKV_OK)
+      return st;
+  }
+  const size_t need = workspace_bytes_for(num_seqs, head_dim, group, num_partitions);
+  if (workspace_bytes < need)
+    return fail(PKV_ERR_INVALID_ARGUMENT, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
+
+  unsigned* err = nullptr;
+  if (pkv_status st = device_state(&err, nullptr); st != PKV_OK) return st;
+  pkv::DecodeParams p{};
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.out = out;
+  p.ws_prefix = static_cast<int32_t*>(workspace);
+  p.ws_pieces = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + pkv::workspace_header_bytes(num_seqs));
+  p.err = err;
+  p.num_blocks = num_blocks;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_partitions = num_partitions;
+  p.qscale = scale * 1.4426950408889634f;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (phases & PKV_PHASE_PARTITION) {
+    const cudaError_t e = pkv::launch_decode_partition(p, head_dim, group, s);
+    if (e != cudaSuccess) return cuda_fail(e, "partition kernel launch");
+    g_launches.fetch_add(1);
+  }
+  if (phases & PKV_PHASE_MERGE) {
+    const cudaError_t e = pkv::launch_decode_merge(p, head_dim, group, s);
+    if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+    g_launches.fetch_add(1);
+  }
+  return ok();
+}
+
+pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks, int32_t block_size,
+                                      float scale, void* out, void* workspace, size_t workspace_bytes,
+                                      pkv_stream_t stream) {
+  return pkv_paged_decode_attention_split(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                                          num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size,
+                                          scale, out, workspace, workspace_bytes, 0, PKV_PHASE_ALL, stream);
+}
+
+pkv_status pkv_get_and_clear_device_error(uint32_t* bits, pkv_stream_t stream) {
+  if (!bits) return fail(PKV_ERR_INVALID_ARGUMENT, "bits is null");
+  unsigned* err = nullptr;
+  if (pkv_status st = device_state(&err, nullptr); st != PKV_OK) return st;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned host = 0;
+  if ((e = cudaMemcpyAsync(&host, err, sizeof host, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    return cuda_fail(e, "reading the device error word");
+  if ((e = cudaMemsetAsync(err, 0, sizeof(unsigned), s)) != cudaSuccess)
+    return cuda_fail(e, "clearing the device error word");
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  *bits = host;
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,759 @@
+// Paged decode attention for GB300 (sm_103a).
+//
+// What is computed ("从零实现一个 mini vLLM--开篇", sections 2 and 5):
+// for each sequence b and q head h, out = softmax(scale * q K^T) V over the
+// context_lens[b] cached tokens, whose K/V rows are found through the
+// sequence's block table (token t lives in block block_tables[b][t / 16] at
+// offset t % 16).  GQA: q head h reads kv head h / G.
+//
+// How (GB300-first; the pages give no kernel, only the PyTorch definition):
+//
+// * Decomposition.  The batch is one flat stream of (sequence, kv head,
+//   block) items, ordered sequence-major.  It is cut into num_partitions
+//   contiguous pieces of equal block count, one per warp, so every warp moves
+//   the same number of bytes whatever the length mix (a 131072-token sequence
+//   is spread over many warps; a 5-token one shares a warp with others).  A
+//   warp that covers a whole (sequence, kv head) pair writes its output rows
+//   directly; a pair cut by a piece boundary leaves a partial softmax state
+//   (m, l, acc) per piece, and the merge kernel combines them (split-K).
+// * Memory pipeline.  Each warp owns a ring of S shared-memory stages.  One
+//   lane issues cp.async.bulk (TMA bulk) copies of the block's K tile and V
+//   tile (each one contiguous 16 x head_dim bf16 run in the
+//   [block][kv head][16][head_dim] layout) plus, at the first block of a
+//   pair, the group's G q rows, completing on an mbarrier.  Block ids are
+//   fetched one refill ahead.  Every mbarrier wait has a time limit.
+// * Compute.  CUDA cores only (a GEMV with G <= 8 rows does not fill an MMA
+//   tile, and the kernel is bound by HBM).  A lane owns 8 consecutive dims
+//   (one 16-byte shared-memory load per row).  Partial dot products of all
+//   tokens of a block and all G heads are reduced across the lanes of a row
+//   with a transpose-reduction; the lanes' token order and q-head order are
+//   XOR-swizzled so every reduction level is a plain shuffle + add.  Packed
+//   fp32x2 FMAs (FFMA2) do the q.K and p.V products.  Online softmax in base
+//   2 with a lazy rescale: the running max is only raised when a block's max
+//   exceeds it by more than 2^8, which keeps the exp2 arguments bounded and
+//   skips the rescale of the accumulators on almost every block.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <mutex>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr unsigned kFull = 0xffffffffu;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescaleSlack = 8.0f;                       // base-2 units
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // a healthy wait is microseconds
+constexpr unsigned long long kDrainTimeoutNs = 200000000ull;
+
+constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x >> 1); }
+constexpr int cmin(int a, int b) { return a < b ? a : b; }
+
+// Geometry of one (head_dim D, group G) instance.
+template <int D, int G>
+struct Geo {
+  static constexpr int kLanesPerToken = D / 8;                 // lanes sharing one K/V row
+  static constexpr int kTokensPerStep = 32 / kLanesPerToken;   // rows one warp-wide load covers
+  static constexpr int kSteps = kBlockTokens / kTokensPerStep; // loads per 16-token tile
+  static constexpr int kSlots = kSteps * G;                    // partial scores per lane per block
+  static constexpr int kLevels = ilog2(kLanesPerToken);        // reduction levels across a row
+  static constexpr int kHalvings = cmin(kLevels, ilog2(kSlots));
+  static constexpr int kFinal = kSlots >> kHalvings;           // scores a lane holds after reduction
+  static constexpr int kTokenLevels = cmin(ilog2(kSteps), kHalvings);
+  static constexpr int kTileBytes = kBlockTokens * D * 2;
+  static constexpr int kQBytes = G * D * 2;
+  static constexpr int kStageBytes = 2 * kTileBytes + kQBytes;
+  static constexpr int kPTileBytes = kBlockTokens * G * 8;     // {p, p} per (token, head)
+  static constexpr int kPieceFloats = G * D + ((2 * G + 3) / 4) * 4;
+
+  // Swizzle of lane c: physical slot k holds logical item k ^ mask_of(c),
+  // item = token_step * G + head.  Level l of the reduction pairs lanes that
+  // differ in bit (kLanesPerToken >> l) and halves the slots.
+  __host__ __device__ static constexpr int mask_of(int c) {
+    int m = 0;
+    for (int l = 1; l <= kHalvings; ++l)
+      if (c & (kLanesPerToken >> l)) m |= (kSlots >> l);
+    return m;
+  }
+  // Lane bits whose value selects which heads a lane ends up holding.
+  __host__ __device__ static constexpr int head_bits() {
+    int bits = 0;
+    for (int l = kTokenLevels + 1; l <= kHalvings; ++l) bits |= (kLanesPerToken >> l);
+    return bits;
+  }
+  // Lane bits of the plain butterfly levels (lanes differing there hold copies).
+  __host__ __device__ static constexpr int copy_bits() {
+    int bits = 0;
+    for (int l = kHalvings + 1; l <= kLevels; ++l) bits |= (kLanesPerToken >> l);
+    return bits;
+  }
+  __host__ __device__ static constexpr int max_bits() { return 31 & ~head_bits(); }
+  __host__ __device__ static constexpr int sum_bits() { return 31 & ~head_bits() & ~copy_bits(); }
+  // A lane that holds head g (in slot g % kFinal).
+  __host__ __device__ static constexpr int src_lane(int g) {
+    for (int c = 0; c < kLanesPerToken; ++c) {
+      const int m = mask_of(c);
+      if (m / G == 0 && (m % G) == g - g % kFinal) return c;
+    }
+    return -1;
+  }
+  __host__ __device__ static constexpr bool valid() {
+    for (int g = 0; g < G; ++g)
+      if (src_lane(g) < 0) return false;
+    return kFinal <= G && (G % kFinal) == 0 && kSteps >= 1;
+  }
+};
+
+template <int D>
+struct Shape;
+template <>
+struct Shape<128> {
+  static constexpr int kWarps = 4;   // warps per CTA
+  static constexpr int kStages = 3;  // ring depth per warp
+};
+template <>
+struct Shape<64> {
+  static constexpr int kWarps = 4;
+  static constexpr int kStages = 4;
+};
+
+template <int D, int G>
+constexpr size_t static_smem_bytes() {
+  using T = Geo<D, G>;
+  constexpr int NW = Shape<D>::kWarps, S = Shape<D>::kStages;
+  return size_t(NW) * S * T::kStageBytes + size_t(NW) * T::kPTileBytes + size_t(NW) * S * 8;
+}
+template <int D, int G>
+size_t partition_smem_bytes(int num_seqs) {
+  return (static_smem_bytes<D, G>() + size_t(2 * num_seqs + 1) * 4 + 15) & ~size_t(15);
+}
+
+// ---------------------------------------------------------------------------
+// PTX wrappers (mbarrier, bulk copy, timers).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for phase `parity` of an mbarrier, giving up after `limit_ns`.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (uint32_t it = 1; it < (1u << 30); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 63u) == 0 && global_ns() - t0 > limit_ns) return false;
+  }
+  return false;
+}
+__device__ __forceinline__ uint4 lds128(const unsigned char* p) { return *reinterpret_cast<const uint4*>(p); }
+// Two bf16 in one 32-bit word -> two fp32 (exact: bf16 is the top half of fp32).
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+__device__ __forceinline__ uint32_t float2_to_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// ---------------------------------------------------------------------------
+// One 16-token block: scores, online-softmax update, p.V accumulation.
+// ---------------------------------------------------------------------------
+template <int D, int G, bool kMasked>
+__device__ __forceinline__ void process_block(const unsigned char* sK, const unsigned char* sV, float2* ptile, const float2 (&q)[G][4],
+                                              float2 (&acc)[G][4], float (&m_ref)[G],
+                                              float (&m_mine)[Geo<D, G>::kFinal],
+                                              float (&l_mine)[Geo<D, G>::kFinal], int c, int half, int mask,
+                                              int valid) {
+  using T = Geo<D, G>;
+  constexpr int kFinal = T::kFinal;
+  const int mj = mask / G;  // token-step part of the swizzle
+  constexpr int kRowBytes = D * 2;
+
+  // q . K_t partial sums over this lane's 8 dims, swizzled slots.
+  float part[T::kSlots];
+#pragma unroll
+  for (int jp = 0; jp < T::kSteps; ++jp) {
+    const int tok = T::kTokensPerStep * (jp ^ mj) + half;
+    const uint4 w = lds128(sK + tok * kRowBytes + c * 16);
+    const float2 k0 = bf16x2_to_float2(w.x), k1 = bf16x2_to_float2(w.y);
+    const float2 k2 = bf16x2_to_float2(w.z), k3 = bf16x2_to_float2(w.w);
+#pragma unroll
+    for (int gp = 0; gp < G; ++gp) {
+      float2 s2 = __fmul2_rn(q[gp][0], k0);
+      s2 = __ffma2_rn(q[gp][1], k1, s2);
+      s2 = __ffma2_rn(q[gp][2], k2, s2);
+      s2 = __ffma2_rn(q[gp][3], k3, s2);
+      part[jp * G + gp] = s2.x + s2.y;
+    }
+  }
+  // Transpose-reduction across the lanes of a row: each level halves the slots.
+#pragma unroll
+  for (int l = 1; l <= T::kHalvings; ++l) {
+    const int n = T::kSlots >> l;
+#pragma unroll
+    for (int i = 0; i < n; ++i) part[i] += __shfl_xor_sync(kFull, part[i + n], T::kLanesPerToken >> l);
+  }
+#pragma unroll
+  for (int l = T::kHalvings + 1; l <= T::kLevels; ++l) part[0] += __shfl_xor_sync(kFull, part[0], T::kLanesPerToken >> l);
+
+  // This lane now holds the full scores of logical items mask + k, k < kFinal.
+  float s[kFinal];
+  int tok_of[kFinal];
+#pragma unroll
+  for (int k = 0; k < kFinal; ++k) {
+    const int item = mask + k;
+    tok_of[k] = T::kTokensPerStep * (item / G) + half;
+    s[k] = part[k];
+    if (kMasked) s[k] = tok_of[k] < valid ? s[k] : -INFINITY;
+  }
+  // Block max per head.
+  float bm[kFinal];
+#pragma unroll
+  for (int k = 0; k < kFinal; ++k) {
+    bm[k] = s[k];
+#pragma unroll
+    for (int bit = 1; bit < 32; bit <<= 1)
+      if (T::max_bits() & bit) bm[k] = fmaxf(bm[k], __shfl_xor_sync(kFull, bm[k], bit));
+  }
+  float bm_all[G];
+  bool need = false;
+#pragma unroll
+  for (int g = 0; g < G; ++g) {
+    bm_all[g] = __shfl_sync(kFull, bm[g % kFinal], T::src_lane(g));
+    need |= bm_all[g] > m_ref[g] + kRescaleSlack;
+  }
+  if (need) {  // warp-uniform: every lane holds the same bm_all and m_ref
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float mn = fmaxf(m_ref[g], bm_all[g]);
+      const float a = exp2f(m_ref[g] - mn);
+      m_ref[g] = mn;
+      const float2 a2 = make_float2(a, a);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[g][i] = __fmul2_rn(acc[g][i], a2);
+    }
+#pragma unroll
+    for (int k = 0; k < kFinal; ++k) {
+      const float mn = fmaxf(m_mine[k], bm[k]);
+      l_mine[k] *= exp2f(m_mine[k] - mn);
+      m_mine[k] = mn;
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kFinal; ++k) {
+    const float p = exp2f(s[k] - m_mine[k]);
+    l_mine[k] += p;
+    ptile[tok_of[k] * G + (mask + k) % G] = make_float2(p, p);
+  }
+  __syncwarp();
+
+  // acc[g] += p_t,g * V_t over the block's tokens (this lane: its token parity, its 8 dims).
+#pragma unroll
+  for (int j = 0; j < T::kSteps; ++j) {
+    const int tok = T::kTokensPerStep * j + half;
+    uint4 w = lds128(sV + tok * kRowBytes + c * 16);
+    if (kMasked && tok >= valid) w = make_uint4(0u, 0u, 0u, 0u);  // never multiply a stale row
+    const float2 v0 = bf16x2_to_float2(w.x), v1 = bf16x2_to_float2(w.y);
+    const float2 v2 = bf16x2_to_float2(w.z), v3 = bf16x2_to_float2(w.w);
+    const float2* pp = ptile + tok * G;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const float2 p2 = pp[g];
+      acc[g][0] = __ffma2_rn(p2, v0, acc[g][0]);
+      acc[g][1] = __ffma2_rn(p2, v1, acc[g][1]);
+      acc[g][2] = __ffma2_rn(p2, v2, acc[g][2]);
+      acc[g][3] = __ffma2_rn(p2, v3, acc[g][3]);
+    }
+  }
+}
+
+// Walk of the flat (sequence, kv head, block) stream.
+struct Cursor {
+  int b, kvh, blk, nblk;
+};
+__device__ __forceinline__ void advance(Cursor& cur, const int* s_prefix, int num_seqs, int hkv) {
+  if (++cur.blk < cur.nblk) return;
+  cur.blk = 0;
+  if (++cur.kvh < hkv) return;
+  cur.kvh = 0;
+  do {
+    ++cur.b;
+    cur.nblk = s_prefix[cur.b + 1] - s_prefix[cur.b];
+  } while (cur.nblk == 0 && cur.b + 1 < num_seqs);
+}
+
+template <int D, int G, int NW, int S>
+__global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const DecodeParams p) {
+  using T = Geo<D, G>;
+  static_assert(T::valid(), "unsupported (head_dim, group) geometry");
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ int s_wsum[32];
+
+  const int B = p.num_seqs;
+  const int hkv = p.num_kv_heads;
+  unsigned char* stages = smem;
+  float2* ptiles = reinterpret_cast<float2*>(stages + size_t(NW) * S * T::kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(ptiles) + NW * T::kPTileBytes);
+  int* s_prefix = reinterpret_cast<int*>(bars + NW * S);
+  int* s_len = s_prefix + (B + 1);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  // --- CTA prologue: clamp lengths, block prefix over sequences -------------
+  if (tid == 0) s_prefix[0] = 0;
+  const int cap = p.max_blocks_per_seq * kBlockTokens;
+  int running = 0;
+  for (int base = 0; base < B; base += NW * 32) {
+    const int idx = base + tid;
+    int L = 0;
+    if (idx < B) {
+      L = __ldg(p.context_lens + idx);
+      if (L < 0) {
+        if (blockIdx.x == 0) atomicOr(p.err, kErrLenNegative);
+        L = 0;
+      }
+      if (L > cap) {
+        if (blockIdx.x == 0) atomicOr(p.err, kErrLenTooLong);
+        L = cap;
+      }
+      s_len[idx] = L;
+    }
+    int x = (L + kBlockTokens - 1) / kBlockTokens;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(kFull, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane == 31) s_wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+      int w = lane < NW ? s_wsum[lane] : 0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(kFull, w, off);
+        if (lane >= off) w += y;
+      }
+      if (lane < NW) s_wsum[lane] = w;
+    }
+    __syncthreads();
+    if (idx < B) s_prefix[idx + 1] = running + (warp > 0 ? s_wsum[warp - 1] : 0) + x;
+    running += s_wsum[NW - 1];
+    __syncthreads();
+  }
+  if (blockIdx.x == 0)
+    for (int i = tid; i <= B; i += NW * 32) p.ws_prefix[i] = s_prefix[i];
+
+  // --- per-warp ring ----------------------------------------------------------
+  unsigned char* ring_ptr = stages + size_t(warp) * S * T::kStageBytes;
+  const uint32_t ring = smem_addr(ring_ptr);
+  const uint32_t bar0 = smem_addr(bars + warp * S);
+  float2* ptile = ptiles + warp * (T::kPTileBytes / 8);
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < S; ++s) mbar_init(bar0 + 8 * s, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  const long long total = static_cast<long long>(hkv) * s_prefix[B];
+  const int gw = blockIdx.x * NW + warp;
+  if (gw >= p.num_partitions || total == 0) return;
+  const long long begin = gw * total / p.num_partitions;
+  const long long end = (gw + 1) * total / p.num_partitions;
+  if (begin == end) return;
+  const int n = static_cast<int>(end - begin);
+
+  // Locate the first item: largest b with hkv * prefix[b] <= begin.
+  Cursor cc;
+  {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (static_cast<long long>(hkv) * s_prefix[mid] <= begin) lo = mid;
+      else hi = mid - 1;
+    }
+    cc.b = lo;
+    cc.nblk = s_prefix[lo + 1] - s_prefix[lo];
+    const int off = static_cast<int>(begin - static_cast<long long>(hkv) * s_prefix[lo]);
+    cc.kvh = off / cc.nblk;
+    cc.blk = off - cc.kvh * cc.nblk;
+  }
+  Cursor pc = cc;  // producer cursor (used by lane 0)
+
+  const __nv_bfloat16* kbase = static_cast<const __nv_bfloat16*>(p.k_cache);
+  const __nv_bfloat16* vbase = static_cast<const __nv_bfloat16*>(p.v_cache);
+  const __nv_bfloat16* qbase = static_cast<const __nv_bfloat16*>(p.q);
+
+  auto block_id = [&](const Cursor& cur) -> int {
+    int id = __ldg(p.block_tables + static_cast<size_t>(cur.b) * p.max_blocks_per_seq + cur.blk);
+    if (id < 0 || id >= p.num_blocks) {
+      atomicOr(p.err, kErrBlockId);
+      id = 0;
+    }
+    return id;
+  };
+  auto issue = [&](int stage, const Cursor& cur, int id, bool with_q) {
+    const uint32_t dst = ring + stage * T::kStageBytes;
+    const uint32_t bar = bar0 + 8 * stage;
+    mbar_arrive_expect_tx(bar, 2 * T::kTileBytes + (with_q ? T::kQBytes : 0));
+    const size_t tile = (static_cast<size_t>(id) * hkv + cur.kvh) * (kBlockTokens * D);
+    bulk_load(dst, kbase + tile, T::kTileBytes, bar);
+    bulk_load(dst + T::kTileBytes, vbase + tile, T::kTileBytes, bar);
+    if (with_q)
+      bulk_load(dst + 2 * T::kTileBytes, qbase + (static_cast<size_t>(cur.b) * p.num_q_heads + cur.kvh * G) * D,
+                T::kQBytes, bar);
+  };
+
+  // Prologue: fetch the first S + 1 block ids together, fill the ring.
+  int next_id = 0;
+  if (lane == 0) {
+    int ids[S + 1];
+    Cursor cur = pc;
+#pragma unroll
+    for (int s = 0; s <= S; ++s) {
+      ids[s] = s < n ? block_id(cur) : 0;
+      if (s + 1 < n) advance(cur, s_prefix, B, hkv);
+    }
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+      if (s < n) {
+        issue(s, pc, ids[s], s == 0 || pc.blk == 0);
+        if (s + 1 < n) advance(pc, s_prefix, B, hkv);
+      }
+    }
+    next_id = ids[S];
+  }
+
+  const int c = lane & (T::kLanesPerToken - 1);
+  const int half = lane / T::kLanesPerToken;
+  const int mask = T::mask_of(c);
+  const int mg = mask % G;
+  const float qscale = p.qscale;
+
+  float2 q[G][4];
+  float2 acc[G][4];
+  float m_ref[G];
+  float m_mine[T::kFinal], l_mine[T::kFinal];
+  bool pair_from_start = false;
+  bool first_pair = true;
+
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int i = 0; i < n; ++i) {
+    const unsigned char* st_ptr = ring_ptr + stage * T::kStageBytes;
+    const bool landed = mbar_wait(bar0 + 8 * stage, phase, kWaitTimeoutNs);
+    if (!__all_sync(kFull, landed)) {
+      // Give up on this piece: flag it, let the copies already in flight land, leave.
+      if (lane == 0) atomicOr(p.err, kErrTimeout);
+      for (int x = i; x < n && x < i + S; ++x) mbar_wait(bar0 + 8 * (x % S), (x / S) & 1, kDrainTimeoutNs);
+      return;
+    }
+    if (i == 0 || cc.blk == 0) {
+      // First block of a pair in this piece: load the group's q rows from the stage.
+      const unsigned char* sq = st_ptr + 2 * T::kTileBytes;
+#pragma unroll
+      for (int gp = 0; gp < G; ++gp) {
+        const uint4 w = lds128(sq + (gp ^ mg) * (D * 2) + c * 16);
+        const float2 s2 = make_float2(qscale, qscale);
+        q[gp][0] = __fmul2_rn(bf16x2_to_float2(w.x), s2);
+        q[gp][1] = __fmul2_rn(bf16x2_to_float2(w.y), s2);
+        q[gp][2] = __fmul2_rn(bf16x2_to_float2(w.z), s2);
+        q[gp][3] = __fmul2_rn(bf16x2_to_float2(w.w), s2);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[gp][e] = make_float2(0.f, 0.f);
+        m_ref[gp] = -INFINITY;
+      }
+#pragma unroll
+      for (int k = 0; k < T::kFinal; ++k) {
+        m_mine[k] = -INFINITY;
+        l_mine[k] = 0.f;
+      }
+      pair_from_start = (cc.blk == 0);
+    }
+    const int valid = s_len[cc.b] - cc.blk * kBlockTokens;
+    if (valid >= kBlockTokens)
+      process_block<D, G, false>(st_ptr, st_ptr + T::kTileBytes, ptile, q, acc, m_ref, m_mine, l_mine, c, half,
+                                 mask, kBlockTokens);
+    else
+      process_block<D, G, true>(st_ptr, st_ptr + T::kTileBytes, ptile, q, acc, m_ref, m_mine, l_mine, c, half,
+                                mask, valid);
+    __syncwarp();
+
+    // Refill the stage just consumed with block i + S.
+    if (lane == 0 && i + S < n) {
+      fence_proxy_async_smem();
+      issue(stage, pc, next_id, pc.blk == 0);
+      if (i + S + 1 < n) {
+        advance(pc, s_prefix, B, hkv);
+        next_id = block_id(pc);
+      }
+    }
+
+    const bool last_of_pair = (cc.blk == cc.nblk - 1);
+    if (last_of_pair || i == n - 1) {
+      // Combine the token-parity lanes, then finish the pair or park its partial state.
+#pragma unroll
+      for (int off = T::kLanesPerToken; off < 32; off <<= 1)
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            acc[g][e].x += __shfl_xor_sync(kFull, acc[g][e].x, off);
+            acc[g][e].y += __shfl_xor_sync(kFull, acc[g][e].y, off);
+          }
+#pragma unroll
+      for (int k = 0; k < T::kFinal; ++k)
+#pragma unroll
+        for (int bit = 1; bit < 32; bit <<= 1)
+          if (T::sum_bits() & bit) l_mine[k] += __shfl_xor_sync(kFull, l_mine[k], bit);
+      float l_all[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) l_all[g] = __shfl_sync(kFull, l_mine[g % T::kFinal], T::src_lane(g));
+
+      if (pair_from_start && last_of_pair) {
+        if (half == 0) {
+          uint4* orow = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                                 (static_cast<size_t>(cc.b) * p.num_q_heads + cc.kvh * G) * D) +
+                        c;
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            const float inv = 1.0f / l_all[g];
+            uint4 o;
+            o.x = float2_to_bf16x2(acc[g][0].x * inv, acc[g][0].y * inv);
+            o.y = float2_to_bf16x2(acc[g][1].x * inv, acc[g][1].y * inv);
+            o.z = float2_to_bf16x2(acc[g][2].x * inv, acc[g][2].y * inv);
+            o.w = float2_to_bf16x2(acc[g][3].x * inv, acc[g][3].y * inv);
+            orow[g * (D / 8)] = o;
+          }
+        }
+      } else {
+        float* piece = p.ws_pieces + (static_cast<size_t>(gw) * 2 + (first_pair ? 0 : 1)) * T::kPieceFloats;
+        if (half == 0) {
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            float4* dst = reinterpret_cast<float4*>(piece + g * D + c * 8);
+            dst[0] = make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
+            dst[1] = make_float4(acc[g][2].x, acc[g][2].y, acc[g][3].x, acc[g][3].y);
+          }
+        }
+        if (lane == 0) {
+#pragma unroll
+          for (int g = 0; g < G; ++g) {
+            piece[G * D + g] = m_ref[g];
+            piece[G * D + G + g] = l_all[g];
+          }
+        }
+      }
+      first_pair = false;
+    }
+    if (i + 1 < n) advance(cc, s_prefix, B, hkv);
+    if (++stage == S) {
+      stage = 0;
+      phase ^= 1u;
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Merge: combine the partial states of every pair cut by a piece boundary,
+// write zeros for empty sequences.  One CTA per (sequence, kv head), one warp
+// per q head of the group.
+// ---------------------------------------------------------------------------
+template <int D, int G>
+__global__ void __launch_bounds__(G * 32) paged_decode_merge_kernel(const DecodeParams p) {
+  using T = Geo<D, G>;
+  constexpr int kPer = D / 32;  // dims per lane
+  const int hkv = p.num_kv_heads;
+  const int b = blockIdx.x / hkv;
+  const int kvh = blockIdx.x - b * hkv;
+  const int g = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int* prefix = p.ws_prefix;
+  const int nblk = prefix[b + 1] - prefix[b];
+  __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
+                        (static_cast<size_t>(b) * p.num_q_heads + kvh * G + g) * D + lane * kPer;
+  if (nblk == 0) {
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) orow[e] = __float2bfloat16_rn(0.f);
+    return;
+  }
+  const long long total = static_cast<long long>(hkv) * prefix[p.num_seqs];
+  const long long W = p.num_partitions;
+  const long long s = static_cast<long long>(hkv) * prefix[b] + static_cast<long long>(kvh) * nblk;
+  const long long e = s + nblk;
+  const long long wa = ((s + 1) * W - 1) / total;  // piece holding block s
+  const long long wb = (e * W - 1) / total;        // piece holding block e - 1
+  if (wa == wb) return;                            // whole pair in one piece: already written
+
+  float M = -INFINITY, l = 0.f;
+  float acc[kPer];
+#pragma unroll
+  for (int x = 0; x < kPer; ++x) acc[x] = 0.f;
+  for (long long w = wa; w <= wb; ++w) {
+    const long long st = w * total / W;
+    const long long en = (w + 1) * total / W;
+    if (st == en) continue;  // empty piece
+    const int slot = (w == wa && st < s) ? 1 : 0;
+    const float* piece = p.ws_pieces + (static_cast<size_t>(w) * 2 + slot) * T::kPieceFloats;
+    const float mw = piece[G * D + g];
+    const float lw = piece[G * D + G + g];
+    float a[kPer];
+    if constexpr (kPer == 4) {
+      const float4 v = *reinterpret_cast<const float4*>(piece + g * D + lane * 4);
+      a[0] = v.x; a[1] = v.y; a[2] = v.z; a[3] = v.w;
+    } else {
+      const float2 v = *reinterpret_cast<const float2*>(piece + g * D + lane * 2);
+      a[0] = v.x; a[1] = v.y;
+    }
+    const float mn = fmaxf(M, mw);
+    const float alpha = exp2f(M - mn);
+    const float beta = exp2f(mw - mn);
+    l = l * alpha + lw * beta;
+#pragma unroll
+    for (int x = 0; x < kPer; ++x) acc[x] = acc[x] * alpha + a[x] * beta;
+    M = mn;
+  }
+  const float inv = 1.0f / l;
+  if constexpr (kPer == 4) {
+    uint2 o;
+    o.x = float2_to_bf16x2(acc[0] * inv, acc[1] * inv);
+    o.y = float2_to_bf16x2(acc[2] * inv, acc[3] * inv);
+    *reinterpret_cast<uint2*>(orow) = o;
+  } else {
+    *reinterpret_cast<uint32_t*>(orow) = float2_to_bf16x2(acc[0] * inv, acc[1] * inv);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side: per-instance launch helpers.
+// ---------------------------------------------------------------------------
+template <int D, int G>
+struct Instance {
+  static constexpr int NW = Shape<D>::kWarps;
+  static constexpr int S = Shape<D>::kStages;
+  static void* partition_fn() { return reinterpret_cast<void*>(&paged_decode_partition_kernel<D, G, NW, S>); }
+
+  static cudaError_t prepare(int dev) {
+    // Opt in to the largest dynamic shared memory this instance can ask for, once per device.
+    static std::mutex mu;
+    static uint64_t done_mask = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    if (dev < 64 && (done_mask >> dev) & 1u) return cudaSuccess;
+    const int max_bytes = static_cast<int>(partition_smem_bytes<D, G>(4096));
+    cudaError_t e = cudaFuncSetAttribute(&paged_decode_partition_kernel<D, G, NW, S>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, max_bytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(&paged_decode_partition_kernel<D, G, NW, S>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
+    if (dev < 64) done_mask |= (uint64_t{1} << dev);
+    return cudaSuccess;
+  }
+
+  static cudaError_t resident_warps(int num_seqs, int* warps) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if ((e = prepare(dev)) != cudaSuccess) return e;
+    int sms = 0, per_sm = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, &paged_decode_partition_kernel<D, G, NW, S>,
+                                                      NW * 32, partition_smem_bytes<D, G>(num_seqs));
+    if (e != cudaSuccess) return e;
+    *warps = sms * (per_sm > 0 ? per_sm : 1) * NW;
+    return cudaSuccess;
+  }
+
+  static cudaError_t partition(const DecodeParams& p, cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if ((e = prepare(dev)) != cudaSuccess) return e;
+    const unsigned grid = static_cast<unsigned>((p.num_partitions + NW - 1) / NW);
+    paged_decode_partition_kernel<D, G, NW, S>
+        <<<grid, NW * 32, partition_smem_bytes<D, G>(p.num_seqs), stream>>>(p);
+    return cudaGetLastError();
+  }
+
+  static cudaError_t merge(const DecodeParams& p, cudaStream_t stream) {
+    const unsigned grid = static_cast<unsigned>(p.num_seqs) * static_cast<unsigned>(p.num_kv_heads);
+    paged_decode_merge_kernel<D, G><<<grid, G * 32, 0, stream>>>(p);
+    return cudaGetLastError();
+  }
+};
+
+template <typename F>
+cudaError_t dispatch(int head_dim, int group, F&& f) {
+  switch (head_dim * 16 + group) {
+    case 64 * 16 + 1: return f(Instance<64, 1>{});
+    case 64 * 16 + 2: return f(Instance<64, 2>{});
+    case 64 * 16 + 4: return f(Instance<64, 4>{});
+    case 64 * 16 + 8: return f(Instance<64, 8>{});
+    case 128 * 16 + 1: return f(Instance<128, 1>{});
+    case 128 * 16 + 2: return f(Instance<128, 2>{});
+    case 128 * 16 + 4: return f(Instance<128, 4>{});
+    case 128 * 16 + 8: return f(Instance<128, 8>{});
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+int piece_floats(int head_dim, int group) { return group * head_dim + ((2 * group + 3) / 4) * 4; }
+
+size_t workspace_header_bytes(int num_seqs) { return (static_cast<size_t>(num_seqs + 1) * 4 + 255) & ~size_t(255); }
+
+int partition_warps_per_cta(int head_dim, int) { return head_dim == 64 ? Shape<64>::kWarps : Shape<128>::kWarps; }
+
+cudaError_t resident_partition_warps(int head_dim, int group, int num_seqs, int* warps) {
+  return dispatch(head_dim, group, [&](auto inst) { return decltype(inst)::resident_warps(num_seqs, warps); });
+}
+
+cudaError_t launch_decode_partition(const DecodeParams& p, int head_dim, int group, cudaStream_t stream) {
+  return dispatch(head_dim, group, [&](auto inst) { return decltype(inst)::partition(p, stream); });
+}
+
+cudaError_t launch_decode_merge(const DecodeParams& p, int head_dim, int group, cudaStream_t stream) {
+  return dispatch(head_dim, group, [&](auto inst) { return decltype(inst)::merge(p, stream); });
+}
+
+}  // namespace pkv

@@ -1,0 +1,68 @@
+// Internal interface between the C ABI layer (capi.cu) and the kernel
+// translation units.  Not installed; the public ABI is include/pagedkv.h.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+namespace pkv {
+
+constexpr int kBlockTokens = 16;  // tokens per KV block
+
+// Bits of the sticky device error word (same values as PKV_DEVERR_*).
+constexpr unsigned kErrSlot = 0x1u;
+constexpr unsigned kErrBlockId = 0x2u;
+constexpr unsigned kErrLenNegative = 0x4u;
+constexpr unsigned kErrLenTooLong = 0x8u;
+constexpr unsigned kErrTimeout = 0x10u;
+
+struct AppendParams {
+  const void* k;
+  const void* v;
+  const int64_t* slot_mapping;
+  void* k_cache;
+  void* v_cache;
+  unsigned* err;
+  int64_t num_tokens;
+  int64_t num_slots;  // 16 * num_blocks
+  int num_kv_heads;
+  int head_dim;
+};
+
+struct DecodeParams {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  void* out;
+  int32_t* ws_prefix;  // workspace: int32 [num_seqs + 1] block prefix over sequences
+  float* ws_pieces;    // workspace: fp32 partial states, [num_partitions][2][piece_floats]
+  unsigned* err;
+  int64_t num_blocks;
+  int num_seqs;
+  int num_q_heads;
+  int num_kv_heads;
+  int max_blocks_per_seq;
+  int num_partitions;
+  float qscale;  // scale * log2(e): scores are kept in base-2 units
+};
+
+// kv_append kernel launch.
+cudaError_t launch_kv_append(const AppendParams& p, int num_sms, cudaStream_t stream);
+
+// Number of fp32 values in one partial-state piece for these shapes.
+int piece_floats(int head_dim, int group);
+// Bytes of the workspace header (block prefix) for num_seqs sequences.
+size_t workspace_header_bytes(int num_seqs);
+// Warps per CTA of the partition kernel for these shapes.
+int partition_warps_per_cta(int head_dim, int group);
+// Resident partition-kernel warps on the current device (the default num_partitions).
+cudaError_t resident_partition_warps(int head_dim, int group, int num_seqs, int* warps);
+// Decode kernels.  `group` = num_q_heads / num_kv_heads.
+cudaError_t launch_decode_partition(const DecodeParams& p, int head_dim, int group, cudaStream_t stream);
+cudaError_t launch_decode_merge(const DecodeParams& p, int head_dim, int group, cudaStream_t stream);
+
+}  // namespace pkv

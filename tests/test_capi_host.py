@@ -1,0 +1,147 @@
+"""The C ABI on the CPU: the library loads, exports every declared symbol, and
+rejects every host-checkable error before any CUDA call (no GPU needed).
+
+Pointers passed here are fake but 16-byte aligned; every call below fails its
+host-side validation first, so none is dereferenced and nothing is launched.
+"""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parents[1]
+HEADER = ROOT / "include" / "pagedkv.h"
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_275_gb300 import build
+    build.build(quiet=True)
+    from paged_kv_cache_275_gb300 import _capi
+    return _capi.load()
+
+
+def declared_functions() -> list[str]:
+    text = HEADER.read_text()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_calls():
+    names = declared_functions()
+    for required in ("pkv_kv_append", "pkv_paged_decode_attention", "pkv_decode_workspace_size",
+                     "pkv_get_and_clear_device_error", "pkv_last_error_message"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from paged_kv_cache_275_gb300 import EXPORTS
+    names = declared_functions()
+    assert sorted(EXPORTS) == names
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_exported_symbols_are_c_linkage():
+    import subprocess
+    from paged_kv_cache_275_gb300 import LIB_PATH
+    out = subprocess.run(["nm", "-D", "--defined-only", str(LIB_PATH)], capture_output=True, text=True).stdout
+    syms = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in declared_functions():
+        assert name in syms, f"{name} is not exported unmangled"
+
+
+FAKE = 0x10000  # aligned, never dereferenced
+
+
+def msg(lib) -> str:
+    return lib.pkv_last_error_message().decode()
+
+
+def append(lib, **kw):
+    args = dict(k=FAKE, v=FAKE, slots=FAKE, n=4, hkv=8, d=128, kc=FAKE, vc=FAKE, nb=10, bs=16, stream=None)
+    args.update(kw)
+    return lib.pkv_kv_append(args["k"], args["v"], args["slots"], args["n"], args["hkv"], args["d"], args["kc"],
+                             args["vc"], args["nb"], args["bs"], args["stream"])
+
+
+def test_append_rejects_bad_arguments(lib):
+    assert append(lib, d=96) == 2 and "head_dim" in msg(lib)
+    assert append(lib, bs=32) == 2 and "block_size" in msg(lib)
+    assert append(lib, hkv=0) == 1
+    assert append(lib, n=-1) == 1
+    assert append(lib, nb=0) == 1
+    assert append(lib, k=None) == 1 and "null" in msg(lib)
+    assert append(lib, kc=FAKE + 8) == 1 and "aligned" in msg(lib)
+    assert append(lib, slots=FAKE + 4) == 1
+
+
+def test_append_zero_tokens_is_a_noop(lib):
+    assert append(lib, n=0, k=None, v=None) == 0
+    assert msg(lib) == ""
+
+
+def attention(lib, **kw):
+    a = dict(q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, W=8, cl=FAKE, B=4, hq=32, hkv=8, d=128, nb=100, bs=16, scale=0.088,
+             out=FAKE, ws=FAKE, wsb=16, parts=64, phases=3, stream=None)
+    a.update(kw)
+    return lib.pkv_paged_decode_attention_split(a["q"], a["kc"], a["vc"], a["bt"], a["W"], a["cl"], a["B"], a["hq"],
+                                                a["hkv"], a["d"], a["nb"], a["bs"], a["scale"], a["out"], a["ws"],
+                                                a["wsb"], a["parts"], a["phases"], a["stream"])
+
+
+def test_attention_rejects_bad_arguments(lib):
+    assert attention(lib, hq=30) == 1 and "multiple" in msg(lib)
+    assert attention(lib, hq=24, hkv=2) == 2 and "group" in msg(lib)        # G = 12
+    assert attention(lib, d=256) == 2
+    assert attention(lib, bs=8) == 2
+    assert attention(lib, B=-1) == 1
+    assert attention(lib, B=5000) == 2 and "PKV_MAX_SEQS" in msg(lib)
+    assert attention(lib, W=0) == 1
+    assert attention(lib, nb=0) == 1
+    assert attention(lib, scale=float("inf")) == 1
+    assert attention(lib, phases=0) == 1 and attention(lib, phases=4) == 1
+    assert attention(lib, parts=-3) == 1
+    assert attention(lib, out=None) == 1
+    assert attention(lib, q=FAKE + 2) == 1
+    assert attention(lib, ws=FAKE + 8) == 1
+    assert attention(lib, wsb=16) == 1 and "workspace too small" in msg(lib)
+
+
+def test_attention_zero_sequences_is_a_noop(lib):
+    assert attention(lib, B=0, q=None, out=None) == 0
+
+
+def test_workspace_size_with_explicit_partitions(lib):
+    n = ctypes.c_size_t(0)
+    assert lib.pkv_decode_workspace_size(128, 32, 8, 128, 256, 1000, ctypes.byref(n)) == 0
+    header = ((128 + 1) * 4 + 255) // 256 * 256
+    piece = 4 * 128 + 8                                  # G * D + round_up(2G, 4) floats
+    assert n.value == header + 1000 * 2 * piece * 4
+    n1 = ctypes.c_size_t(0)
+    assert lib.pkv_decode_workspace_size(4, 2, 1, 64, 3, 12, ctypes.byref(n1)) == 0
+    assert n1.value == 256 + 12 * 2 * (2 * 64 + 4) * 4
+    assert lib.pkv_decode_workspace_size(4, 2, 1, 64, 3, -1, ctypes.byref(n1)) == 1
+
+
+def test_launch_counter_starts_at_zero_without_launches(lib):
+    assert lib.pkv_kernel_launch_count() == 0
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    import paged_kv_cache_275_gb300 as pkv
+    q = torch.zeros(1, 2, 64, dtype=torch.bfloat16)
+    kc = torch.zeros(1, 1, 16, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="CUDA"):
+        pkv.paged_decode_attention(q, kc, kc, torch.zeros(1, 1, dtype=torch.int32), torch.ones(1, dtype=torch.int32),
+                                   0.1, q.clone())
+    with pytest.raises(ValueError, match="CUDA"):
+        pkv.kv_append(q[:, :1], q[:, :1], torch.zeros(1, dtype=torch.int64), kc, kc)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    from paged_kv_cache_275_gb300 import _capi
+    with pytest.raises(ImportError, match="no fallback"):
+        _capi.load(tmp_path / "libpagedkv.so")
