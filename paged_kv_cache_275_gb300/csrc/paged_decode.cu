@@ -45,7 +45,6 @@ namespace pkv {
 namespace {
 
 constexpr unsigned kFull = 0xffffffffu;
-constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescaleSlack = 8.0f;                       // base-2 units
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // a healthy wait is microseconds
 constexpr unsigned long long kDrainTimeoutNs = 200000000ull;
