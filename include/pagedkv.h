@@ -173,6 +173,34 @@ pkv_status pkv_paged_decode_attention_split(const void* q, const void* k_cache, 
                                             void* workspace, size_t workspace_bytes, int32_t num_partitions,
                                             int32_t phases, pkv_stream_t stream);
 
+/* Bytes of the built-in scratch area behind pkv_paged_decode_attention_static (per device). */
+#define PKV_STATIC_WORKSPACE_BYTES (8u * 1024u * 1024u)
+
+/*
+ * Decode attention without a caller workspace, for callers that cannot
+ * allocate device memory: for example a plugin running inside a host process
+ * that owns every device allocation, or a serving loop in which a cudaMalloc
+ * would implicitly synchronise the device and stall its other streams.  The
+ * source pages have no counterpart to this entry point.
+ *
+ * Same arguments, shapes and result as pkv_paged_decode_attention, minus the
+ * workspace.  Scratch comes from one fixed array of PKV_STATIC_WORKSPACE_BYTES
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits.  Shapes whose scratch need is larger return
+ * PKV_ERR_UNSUPPORTED with a message (at the default partition count every
+ * built shape needs about 5 MB on a 152-SM GB300).  The first call on a device,
+ * with that device current, looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture.
+ * Every call shares the array and it keeps the last call's contents (nothing
+ * in it needs to start at zero), so calls that may overlap on the GPU race:
+ * serialise them on one stream.  Calls no allocating routine.
+ */
+pkv_status pkv_paged_decode_attention_static(const void* q, const void* k_cache, const void* v_cache,
+                                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                             const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                                             int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
+                                             int32_t block_size, float scale, void* out, pkv_stream_t stream);
+
 /*
  * Synchronises `stream`, then returns and clears the current device's sticky
  * error word (a mask of PKV_DEVERR_* bits; 0 = no device-side error since the

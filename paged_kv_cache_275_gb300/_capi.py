@@ -42,6 +42,7 @@ EXPORTS = (
     "pkv_decode_default_partitions",
     "pkv_paged_decode_attention",
     "pkv_paged_decode_attention_split",
+    "pkv_paged_decode_attention_static",
     "pkv_get_and_clear_device_error",
     "pkv_last_error_message",
     "pkv_kernel_launch_count",
@@ -77,10 +78,12 @@ def load(path: Path | str | None = None) -> ctypes.CDLL:
                                                    ctypes.c_float, V, V, SZ, V]
         lib.pkv_paged_decode_attention_split.argtypes = [V, V, V, V, I32, V, I32, I32, I32, I32, I64, I32,
                                                          ctypes.c_float, V, V, SZ, I32, I32, V]
+        lib.pkv_paged_decode_attention_static.argtypes = [V, V, V, V, I32, V, I32, I32, I32, I32, I64, I32,
+                                                          ctypes.c_float, V, V]
         lib.pkv_get_and_clear_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), V]
         for name in ("pkv_kv_append", "pkv_decode_workspace_size", "pkv_decode_default_partitions",
                      "pkv_paged_decode_attention", "pkv_paged_decode_attention_split",
-                     "pkv_get_and_clear_device_error"):
+                     "pkv_paged_decode_attention_static", "pkv_get_and_clear_device_error"):
             getattr(lib, name).restype = ctypes.c_int
         lib.pkv_last_error_message.argtypes = []
         lib.pkv_last_error_message.restype = ctypes.c_char_p

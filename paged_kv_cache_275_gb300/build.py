@@ -23,7 +23,7 @@ CSRC = PKG / "csrc"
 INCLUDE = ROOT / "include"
 BUILD = PKG / "_build"
 LIB = PKG / "libpagedkv.so"
-SOURCES = ["capi.cu", "kv_append.cu", "paged_decode.cu"]
+SOURCES = ["capi.cu", "kv_append.cu", "paged_decode.cu", "static_workspace.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -46,8 +46,18 @@ def _inputs() -> list[Path]:
     return [CSRC / s for s in SOURCES] + list(CSRC.glob("*.h")) + list(INCLUDE.glob("*.h"))
 
 
+STAMP = BUILD / "flags.txt"
+
+
+def extra_flags() -> list[str]:
+    """Extra nvcc flags from PKV_NVCC_FLAGS (launch-shape tuning, e.g. -DPKV_D128_WARPS=6)."""
+    return os.environ.get("PKV_NVCC_FLAGS", "").split()
+
+
 def needs_build() -> bool:
     if not LIB.exists():
+        return True
+    if (STAMP.read_text() if STAMP.exists() else "") != " ".join(extra_flags()):
         return True
     t = LIB.stat().st_mtime
     return any(p.stat().st_mtime > t for p in _inputs())
@@ -55,7 +65,7 @@ def needs_build() -> bool:
 
 def compile_flags(ptxas_verbose: bool = False) -> list[str]:
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", str(INCLUDE), "-I", str(CSRC),
-                    "--expt-relaxed-constexpr"]
+                    "--expt-relaxed-constexpr"] + extra_flags()
     if ptxas_verbose:
         flags += ["-Xptxas", "-v"]
     return flags
@@ -90,6 +100,7 @@ def build(force: bool = False, ptxas_verbose: bool = False, quiet: bool = False)
         sys.stderr.write(r.stdout + r.stderr)
         raise RuntimeError("nvcc link failed")
     os.replace(tmp, LIB)
+    STAMP.write_text(" ".join(extra_flags()))
     return LIB
 
 

@@ -118,6 +118,8 @@ size_t workspace_bytes_for(int32_t num_seqs, int32_t head_dim, int32_t group, in
 
 }  // namespace
 
+void pkv::set_error_message(const char* message) { snprintf(t_message, sizeof t_message, "%s", message); }
+
 extern "C" {
 
 const char* pkv_last_error_message(void) { return t_message; }

@@ -50,6 +50,9 @@ struct DecodeParams {
   float qscale;  // scale * log2(e): scores are kept in base-2 units
 };
 
+// Set the per-host-thread message returned by pkv_last_error_message().
+void set_error_message(const char* message);
+
 // kv_append kernel launch.
 cudaError_t launch_kv_append(const AppendParams& p, int num_sms, cudaStream_t stream);
 
