@@ -107,17 +107,30 @@ struct Geo {
   }
 };
 
+// Launch shape per head_dim (warps per CTA, ring stages per warp); overridable at build time.
+#ifndef PKV_D128_WARPS
+#define PKV_D128_WARPS 4
+#endif
+#ifndef PKV_D128_STAGES
+#define PKV_D128_STAGES 3
+#endif
+#ifndef PKV_D64_WARPS
+#define PKV_D64_WARPS 4
+#endif
+#ifndef PKV_D64_STAGES
+#define PKV_D64_STAGES 4
+#endif
 template <int D>
 struct Shape;
 template <>
 struct Shape<128> {
-  static constexpr int kWarps = 4;   // warps per CTA
-  static constexpr int kStages = 3;  // ring depth per warp
+  static constexpr int kWarps = PKV_D128_WARPS;
+  static constexpr int kStages = PKV_D128_STAGES;
 };
 template <>
 struct Shape<64> {
-  static constexpr int kWarps = 4;
-  static constexpr int kStages = 4;
+  static constexpr int kWarps = PKV_D64_WARPS;
+  static constexpr int kStages = PKV_D64_STAGES;
 };
 
 template <int D, int G>
@@ -242,23 +255,23 @@ __device__ __forceinline__ void process_block(const unsigned char* sK, const uns
     s[k] = part[k];
     if (kMasked) s[k] = tok_of[k] < valid ? s[k] : -INFINITY;
   }
-  // Block max per head.
-  float bm[kFinal];
+  // The running max of a head is raised only when some score of the block beats it by more
+  // than the slack; one vote decides, and the per-head block max is formed only then.
+  bool beats = false;
 #pragma unroll
-  for (int k = 0; k < kFinal; ++k) {
-    bm[k] = s[k];
+  for (int k = 0; k < kFinal; ++k) beats |= s[k] > m_mine[k] + kRescaleSlack;
+  if (__any_sync(kFull, beats)) {  // warp-uniform
+    float bm[kFinal];
 #pragma unroll
-    for (int bit = 1; bit < 32; bit <<= 1)
-      if (T::max_bits() & bit) bm[k] = fmaxf(bm[k], __shfl_xor_sync(kFull, bm[k], bit));
-  }
-  float bm_all[G];
-  bool need = false;
+    for (int k = 0; k < kFinal; ++k) {
+      bm[k] = s[k];
 #pragma unroll
-  for (int g = 0; g < G; ++g) {
-    bm_all[g] = __shfl_sync(kFull, bm[g % kFinal], T::src_lane(g));
-    need |= bm_all[g] > m_ref[g] + kRescaleSlack;
-  }
-  if (need) {  // warp-uniform: every lane holds the same bm_all and m_ref
+      for (int bit = 1; bit < 32; bit <<= 1)
+        if (T::max_bits() & bit) bm[k] = fmaxf(bm[k], __shfl_xor_sync(kFull, bm[k], bit));
+    }
+    float bm_all[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) bm_all[g] = __shfl_sync(kFull, bm[g % kFinal], T::src_lane(g));
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       const float mn = fmaxf(m_ref[g], bm_all[g]);
@@ -677,8 +690,12 @@ struct Instance {
     static uint64_t done_mask = 0;
     std::lock_guard<std::mutex> lock(mu);
     if (dev < 64 && (done_mask >> dev) & 1u) return cudaSuccess;
-    const int max_bytes = static_cast<int>(partition_smem_bytes<D, G>(4096));
-    cudaError_t e = cudaFuncSetAttribute(&paged_decode_partition_kernel<D, G, NW, S>,
+    int optin = 0;
+    cudaError_t e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e != cudaSuccess) return e;
+    int max_bytes = static_cast<int>(partition_smem_bytes<D, G>(4096));
+    if (max_bytes > optin) max_bytes = optin;
+    e = cudaFuncSetAttribute(&paged_decode_partition_kernel<D, G, NW, S>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, max_bytes);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(&paged_decode_partition_kernel<D, G, NW, S>,
