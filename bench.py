@@ -457,6 +457,67 @@ def run_ours(args, dist: Dist) -> dict | None:
     return line
 
 
+# ---------------------------------------------------------------------------
+# Component measurements (not the headline step): block copy, block manager
+# ---------------------------------------------------------------------------
+def run_component(args) -> dict:
+    import numpy as np
+
+    import paged_kv_cache_275_gb300 as pkv
+    from paged_kv_cache_275_gb300 import build as _build
+    from workloads import make_generator, randn_bf16
+    _build.build(quiet=True)
+    peak, peak_kind = peaks()
+    if args.component == "block_manager":
+        # Host allocator throughput on a decode trace: 256 sequences, 1000 append steps.
+        longest = 1000 + 3 * 255 + args.warmup + args.steps
+        bm = pkv.BlockManager(256 * (longest // 16 + 2))
+        ids = np.arange(256, dtype=np.int64)
+        for i in range(256):
+            bm.add_sequence(i, 1000 + 3 * i)
+        for _ in range(args.warmup):
+            bm.append_slots(ids)
+        t = time.perf_counter()
+        for _ in range(args.steps):
+            bm.append_slots(ids)
+        dt = time.perf_counter() - t
+        return {"component": "block_manager", "metric": "append slots per second (host, one thread)",
+                "value": round(256 * args.steps / dt, 1), "unit": "slot/s", "steps": args.steps,
+                "us_per_batch_of_256": round(1e6 * dt / args.steps, 2), "kind": "C ABI through ctypes"}
+    # copy_blocks: copy-on-write of 4096 distinct block pairs of the Qwen3/LLaMA-3 kv layout.
+    dev = torch.device("cuda", 0)
+    g = make_generator(7)
+    nb, hkv, d, n = 16384, 8, 128, 4096
+    kc = randn_bf16((nb, hkv, 16, d), make_generator(8, "cuda"), "cuda")
+    vc = randn_bf16((nb, hkv, 16, d), make_generator(9, "cuda"), "cuda")
+    perm = torch.randperm(nb, generator=g)
+    pairs = torch.stack([perm[:n], perm[n:2 * n]], dim=1).to(torch.int64).to(dev)
+    ref_k = kc[pairs[:, 0]].clone()
+    pkv.copy_blocks(kc, vc, pairs)
+    torch.cuda.synchronize()
+    if not torch.equal(kc[pairs[:, 1]], ref_k) or pkv.get_and_clear_device_error() != 0:
+        raise RuntimeError("copy_blocks parity failed before timing")
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        pkv.copy_blocks(kc, vc, pairs)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        pkv.copy_blocks(kc, vc, pairs)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    sec = e0.elapsed_time(e1) / 1e3 / args.steps
+    moved = n * 2 * (hkv * 16 * d * 2) * 2          # K and V blocks, read + written
+    gbs = moved / sec / 1e9
+    return {"component": "copy_blocks", "metric": "block copy HBM GB/s (read + write)", "value": round(gbs, 1),
+            "unit": "GB/s", "steps": args.steps, "warmup": args.warmup, "us_per_launch": round(sec * 1e6, 2),
+            "config": {"pairs": n, "block_bytes_k_plus_v": 2 * hkv * 16 * d * 2, "pool_blocks": nb},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "frac_of": f"{peak_kind} HBM copy bandwidth",
+                         "algorithmic_bytes_per_launch": moved, "traffic": None}}
+
+
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -470,9 +531,14 @@ def main(argv=None) -> int:
                     help="seconds the reference arm's warm-up + timed steps should take")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per partition launch from an ncu capture of the current kernel")
+    ap.add_argument("--component", choices=("copy_blocks", "block_manager"), default=None,
+                    help="measure one component instead of the decode step")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.component:
+        print(json.dumps(run_component(args)), flush=True)
+        return 0
     dist = Dist()
     try:
         line = run_reference(args, dist) if args.impl == "reference" else run_ours(args, dist)

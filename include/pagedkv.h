@@ -66,7 +66,8 @@ typedef enum pkv_status {
     PKV_OK = 0,
     PKV_ERR_INVALID_ARGUMENT = 1, /* null / misaligned pointer, bad size, workspace too small */
     PKV_ERR_UNSUPPORTED = 2,      /* head_dim, GQA group, block size or batch outside what is built */
-    PKV_ERR_CUDA = 3              /* a CUDA runtime call failed (message has the CUDA error) */
+    PKV_ERR_CUDA = 3,             /* a CUDA runtime call failed (message has the CUDA error) */
+    PKV_ERR_NO_FREE_BLOCKS = 4    /* block manager: the pool cannot supply the blocks a call needs (nothing changed) */
 } pkv_status;
 
 /* Bits of the sticky device error word. */
@@ -75,6 +76,7 @@ typedef enum pkv_status {
 #define PKV_DEVERR_CONTEXT_LEN_NEGATIVE 0x4u  /* attention: context_len < 0 (treated as 0) */
 #define PKV_DEVERR_CONTEXT_LEN_TOO_LONG 0x8u  /* attention: context_len > 16 * max_blocks_per_seq (clamped) */
 #define PKV_DEVERR_PIPELINE_TIMEOUT 0x10u     /* attention: a shared-memory pipeline wait gave up (partition skipped) */
+#define PKV_DEVERR_COPY_OUT_OF_RANGE 0x20u    /* copy_blocks: a source or destination block outside the pool (pair skipped) */
 
 /* Largest num_seqs one attention call accepts. */
 #define PKV_MAX_SEQS 4096
@@ -200,6 +202,71 @@ pkv_status pkv_paged_decode_attention_static(const void* q, const void* k_cache,
                                              const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
                                              int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
                                              int32_t block_size, float scale, void* out, pkv_stream_t stream);
+
+/*
+ * Copy whole KV blocks inside the pool: the copy half of copy-on-write for
+ * blocks shared between sequences.  The pages let requests share a prompt's
+ * KV blocks ("v0版本介绍", section "为什么需要推理框架") and plan a prefix
+ * cache ("从零实现一个 mini vLLM--开篇", section 4); a block shared by several
+ * sequences must be copied before one of them appends into it.
+ *
+ * For every pair i: k_cache[dst_i][:][:][:] = k_cache[src_i][:][:][:] and the
+ * same for v_cache (every kv head, all 16 slots), bit-exact.
+ *
+ *   src_dst     device, int64 [num_pairs][2] = (src, dst) block ids
+ *   k_cache, v_cache  device, bf16 [num_blocks][num_kv_heads][16][head_dim]
+ *
+ * Destinations must be distinct and no destination may be a source of
+ * another pair.  num_pairs == 0 is a no-op.  Device-side: a block id outside
+ * [0, num_blocks) sets PKV_DEVERR_COPY_OUT_OF_RANGE and that pair is skipped.
+ */
+pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_dst, int32_t num_pairs,
+                           int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks, pkv_stream_t stream);
+
+/*
+ * Host block manager: the paged cache's allocator ("跟着 Claude Code，我用
+ * Python 实现了一个轻量级的 vLLM", section "核心机制一：分页 KV Cache": fixed
+ * 16-token blocks taken on demand and all returned when a sequence ends;
+ * "从零实现一个 mini vLLM--开篇", section 5, phase 4: one block table per
+ * request; "v0版本介绍", section "为什么需要推理框架": a new block is taken only
+ * when the current one is full, and requests may share prompt blocks).
+ *
+ * Host memory only; every call on one manager is serialised by a lock inside
+ * it.  Blocks carry a reference count: a fork shares all of the parent's
+ * blocks, and appending into a shared, partly filled last block first moves
+ * the sequence onto a fresh block (copy-on-write) and reports the (src, dst)
+ * copy the caller must run with pkv_copy_blocks before the append.  The free
+ * list is first-in first-out: blocks are taken from its front, and a
+ * sequence's released blocks join its back in block-table order.  A call
+ * that fails changes nothing.
+ */
+typedef struct pkv_block_manager pkv_block_manager;
+
+/* Pool of num_blocks blocks.  initial_free_order (NULL = 0, 1, 2, ...) is a
+   permutation of [0, num_blocks) giving the initial free list. */
+pkv_status pkv_bm_create(int64_t num_blocks, const int64_t* initial_free_order, pkv_block_manager** out);
+pkv_status pkv_bm_destroy(pkv_block_manager* bm);
+/* Number of blocks on the free list. */
+pkv_status pkv_bm_num_free(pkv_block_manager* bm, int64_t* num_free);
+/* New sequence (an unused id >= 0) holding num_tokens tokens, ceil(num_tokens / 16)
+   blocks.  slots (NULL or [num_tokens]) receives the slot of every position. */
+pkv_status pkv_bm_add_sequence(pkv_block_manager* bm, int64_t seq_id, int64_t num_tokens, int64_t* slots);
+/* Grow each listed sequence (ids distinct) by one token.  slots[i] receives
+   its new token's slot.  Copy-on-write pairs go to copies[0 .. 2 * *num_copies)
+   as (src, dst); there are at most num_seqs of them. */
+pkv_status pkv_bm_append_slots(pkv_block_manager* bm, const int64_t* seq_ids, int32_t num_seqs, int64_t* slots,
+                               int64_t* copies, int32_t* num_copies);
+/* child_id (an unused id) shares every block of parent_id and has its length. */
+pkv_status pkv_bm_fork(pkv_block_manager* bm, int64_t parent_id, int64_t child_id);
+/* Release a sequence: each of its blocks loses one reference, and blocks left
+   with none go back to the free list. */
+pkv_status pkv_bm_free_sequence(pkv_block_manager* bm, int64_t seq_id);
+/* Block tables and lengths of the listed sequences: tables is
+   [num_seqs][width] int32 padded with -1; lengths is [num_seqs] int32. */
+pkv_status pkv_bm_block_tables(pkv_block_manager* bm, const int64_t* seq_ids, int32_t num_seqs, int32_t width,
+                               int32_t* tables, int32_t* lengths);
+/* Reference count of one block (0 = free). */
+pkv_status pkv_bm_ref_count(pkv_block_manager* bm, int64_t block, int32_t* count);
 
 /*
  * Synchronises `stream`, then returns and clears the current device's sticky

@@ -67,6 +67,8 @@ def _load():
         lib.pkv_oracle_paged_decode_sampled.argtypes = [P, P, P, P, i32, P, i32, i32, i32, i32, i64, i32,
                                                         dbl, P, P, i64, P, i32]
         lib.pkv_oracle_paged_decode_sampled.restype = ctypes.c_int
+        lib.pkv_oracle_copy_blocks.argtypes = [P, P, P, i64, i32, i32, i64, i32]
+        lib.pkv_oracle_copy_blocks.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -170,3 +172,11 @@ def paged_decode_sampled(q, k_cache, v_cache, block_tables, context_lens, scale:
         _ptr(qq), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(cl), B, hq, hkv, d, nb, bs, float(scale),
         _ptr(si), _ptr(hi), si.shape[0], _ptr(out), num_threads or default_threads())
     return out, st
+
+
+def copy_blocks(k_cache, v_cache, src_dst) -> int:
+    """Oracle block copy, in place on CPU caches ([NB, Hkv, bs, D] bf16); src_dst: [n, 2] int64."""
+    kc, vc = _as_u16(k_cache), _as_u16(v_cache)
+    pairs = _as(src_dst, np.int64).reshape(-1, 2)
+    num_blocks, hkv, bs, d = kc.shape
+    return _load().pkv_oracle_copy_blocks(_ptr(kc), _ptr(vc), _ptr(pairs), pairs.shape[0], hkv, d, num_blocks, bs)

@@ -295,3 +295,30 @@ int pkv_oracle_paged_decode_sampled(const uint16_t* q, const uint16_t* k_cache, 
                    num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale};
     return run_items(&P, seq_idx, head_idx, n_samples, out, num_threads);
 }
+
+/*
+ * Block copy for copy-on-write of shared blocks ("v0版本介绍", section
+ * "为什么需要推理框架": requests may share a prompt's KV blocks; a shared block
+ * is copied before one of its users appends into it): for every pair i,
+ * k_cache[dst_i][:][:][:] = k_cache[src_i][:][:][:], the same for v_cache.
+ * Pairs are applied in order.  Out-of-range ids are skipped and flagged.
+ */
+int pkv_oracle_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, const int64_t* src_dst, int64_t num_pairs,
+                           int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks, int32_t block_size) {
+    if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0)
+        return ORACLE_BAD_ARGUMENT;
+    const int64_t per_block = (int64_t)num_kv_heads * block_size * head_dim;
+    int status = ORACLE_OK;
+    for (int64_t i = 0; i < num_pairs; ++i) {
+        const int64_t src = src_dst[2 * i], dst = src_dst[2 * i + 1];
+        if (src < 0 || src >= num_blocks || dst < 0 || dst >= num_blocks) {
+            status |= ORACLE_BLOCK_ID_OUT_OF_RANGE;
+            continue;
+        }
+        for (int64_t e = 0; e < per_block; ++e) {
+            k_cache[dst * per_block + e] = k_cache[src * per_block + e];
+            v_cache[dst * per_block + e] = v_cache[src * per_block + e];
+        }
+    }
+    return status;
+}

@@ -20,13 +20,16 @@ OK = 0
 ERR_INVALID_ARGUMENT = 1
 ERR_UNSUPPORTED = 2
 ERR_CUDA = 3
-STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARGUMENT", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_CUDA"}
+ERR_NO_FREE_BLOCKS = 4
+STATUS_NAMES = {0: "PKV_OK", 1: "PKV_ERR_INVALID_ARGUMENT", 2: "PKV_ERR_UNSUPPORTED", 3: "PKV_ERR_CUDA",
+                4: "PKV_ERR_NO_FREE_BLOCKS"}
 
 DEVERR_SLOT_OUT_OF_RANGE = 0x1
 DEVERR_BLOCK_ID_OUT_OF_RANGE = 0x2
 DEVERR_CONTEXT_LEN_NEGATIVE = 0x4
 DEVERR_CONTEXT_LEN_TOO_LONG = 0x8
 DEVERR_PIPELINE_TIMEOUT = 0x10
+DEVERR_COPY_OUT_OF_RANGE = 0x20
 
 PHASE_PARTITION = 1
 PHASE_MERGE = 2
@@ -43,6 +46,16 @@ EXPORTS = (
     "pkv_paged_decode_attention",
     "pkv_paged_decode_attention_split",
     "pkv_paged_decode_attention_static",
+    "pkv_copy_blocks",
+    "pkv_bm_create",
+    "pkv_bm_destroy",
+    "pkv_bm_num_free",
+    "pkv_bm_add_sequence",
+    "pkv_bm_append_slots",
+    "pkv_bm_fork",
+    "pkv_bm_free_sequence",
+    "pkv_bm_block_tables",
+    "pkv_bm_ref_count",
     "pkv_get_and_clear_device_error",
     "pkv_last_error_message",
     "pkv_kernel_launch_count",
@@ -80,10 +93,23 @@ def load(path: Path | str | None = None) -> ctypes.CDLL:
                                                          ctypes.c_float, V, V, SZ, I32, I32, V]
         lib.pkv_paged_decode_attention_static.argtypes = [V, V, V, V, I32, V, I32, I32, I32, I32, I64, I32,
                                                           ctypes.c_float, V, V]
+        lib.pkv_copy_blocks.argtypes = [V, V, V, I32, I32, I32, I64, V]
+        lib.pkv_bm_create.argtypes = [I64, V, ctypes.POINTER(V)]
+        lib.pkv_bm_destroy.argtypes = [V]
+        lib.pkv_bm_num_free.argtypes = [V, ctypes.POINTER(I64)]
+        lib.pkv_bm_add_sequence.argtypes = [V, I64, I64, V]
+        lib.pkv_bm_append_slots.argtypes = [V, V, I32, V, V, ctypes.POINTER(I32)]
+        lib.pkv_bm_fork.argtypes = [V, I64, I64]
+        lib.pkv_bm_free_sequence.argtypes = [V, I64]
+        lib.pkv_bm_block_tables.argtypes = [V, V, I32, I32, V, V]
+        lib.pkv_bm_ref_count.argtypes = [V, I64, ctypes.POINTER(I32)]
         lib.pkv_get_and_clear_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), V]
         for name in ("pkv_kv_append", "pkv_decode_workspace_size", "pkv_decode_default_partitions",
                      "pkv_paged_decode_attention", "pkv_paged_decode_attention_split",
-                     "pkv_paged_decode_attention_static", "pkv_get_and_clear_device_error"):
+                     "pkv_paged_decode_attention_static", "pkv_get_and_clear_device_error", "pkv_copy_blocks",
+                     "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_num_free", "pkv_bm_add_sequence",
+                     "pkv_bm_append_slots", "pkv_bm_fork", "pkv_bm_free_sequence", "pkv_bm_block_tables",
+                     "pkv_bm_ref_count"):
             getattr(lib, name).restype = ctypes.c_int
         lib.pkv_last_error_message.argtypes = []
         lib.pkv_last_error_message.restype = ctypes.c_char_p
@@ -220,3 +246,90 @@ def get_and_clear_device_error(stream: torch.cuda.Stream | None = None) -> int:
 
 def kernel_launch_count() -> int:
     return int(load().pkv_kernel_launch_count())
+
+
+def copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor, src_dst: torch.Tensor,
+                stream: torch.cuda.Stream | None = None) -> None:
+    """k_cache[dst] = k_cache[src] and v_cache[dst] = v_cache[src] for every row (src, dst) of src_dst [n, 2] int64."""
+    _require(k_cache, "k_cache", torch.bfloat16, 4)
+    dev = k_cache.device
+    _require(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _require(src_dst, "src_dst", torch.int64, 2, dev)
+    if v_cache.shape != k_cache.shape or src_dst.shape[1] != 2:
+        raise ValueError("caches must match and src_dst must be [n, 2]")
+    nb, hkv, _, d = k_cache.shape
+    with torch.cuda.device(dev):
+        _check(load().pkv_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(), src_dst.data_ptr(), src_dst.shape[0],
+                                      hkv, d, nb, _stream_handle(stream)))
+
+
+class BlockManager:
+    """Host block manager of the C ABI (pkv_bm_*): allocation, append slots, fork, free, copy-on-write."""
+
+    def __init__(self, num_blocks: int, initial_free_order=None):
+        import numpy as np
+        self._lib = load()
+        self._h = ctypes.c_void_p()
+        order = None
+        if initial_free_order is not None:
+            order = np.ascontiguousarray(np.asarray(initial_free_order, dtype=np.int64))
+            if order.shape != (num_blocks,):
+                raise ValueError("initial_free_order must hold num_blocks entries")
+        ptr = order.ctypes.data if order is not None else None
+        _check(self._lib.pkv_bm_create(int(num_blocks), ptr, ctypes.byref(self._h)))
+        self.num_blocks = int(num_blocks)
+
+    def close(self) -> None:
+        if self._h:
+            _check(self._lib.pkv_bm_destroy(self._h))
+            self._h = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def num_free(self) -> int:
+        n = ctypes.c_int64(0)
+        _check(self._lib.pkv_bm_num_free(self._h, ctypes.byref(n)))
+        return int(n.value)
+
+    def add_sequence(self, seq_id: int, num_tokens: int):
+        import numpy as np
+        slots = np.zeros(max(1, num_tokens), dtype=np.int64)
+        _check(self._lib.pkv_bm_add_sequence(self._h, int(seq_id), int(num_tokens), slots.ctypes.data))
+        return slots[:num_tokens]
+
+    def append_slots(self, seq_ids):
+        """Returns (slots [n] int64, copies [k, 2] int64 as (src, dst))."""
+        import numpy as np
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        n = ids.shape[0]
+        slots = np.zeros(max(1, n), dtype=np.int64)
+        copies = np.zeros(max(1, 2 * n), dtype=np.int64)
+        k = ctypes.c_int32(0)
+        _check(self._lib.pkv_bm_append_slots(self._h, ids.ctypes.data, n, slots.ctypes.data, copies.ctypes.data,
+                                             ctypes.byref(k)))
+        return slots[:n], copies[:2 * k.value].reshape(-1, 2)
+
+    def fork(self, parent_id: int, child_id: int) -> None:
+        _check(self._lib.pkv_bm_fork(self._h, int(parent_id), int(child_id)))
+
+    def free_sequence(self, seq_id: int) -> None:
+        _check(self._lib.pkv_bm_free_sequence(self._h, int(seq_id)))
+
+    def block_tables(self, seq_ids, width: int):
+        """Returns (tables [n, width] int32 padded with -1, lengths [n] int32)."""
+        import numpy as np
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64))
+        n = ids.shape[0]
+        tables = np.zeros((max(1, n), width), dtype=np.int32)
+        lens = np.zeros(max(1, n), dtype=np.int32)
+        _check(self._lib.pkv_bm_block_tables(self._h, ids.ctypes.data, n, width, tables.ctypes.data, lens.ctypes.data))
+        return tables[:n], lens[:n]
+
+    def ref_count(self, block: int) -> int:
+        c = ctypes.c_int32(0)
+        _check(self._lib.pkv_bm_ref_count(self._h, int(block), ctypes.byref(c)))
+        return int(c.value)

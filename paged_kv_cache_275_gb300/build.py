@@ -23,7 +23,8 @@ CSRC = PKG / "csrc"
 INCLUDE = ROOT / "include"
 BUILD = PKG / "_build"
 LIB = PKG / "libpagedkv.so"
-SOURCES = ["capi.cu", "kv_append.cu", "paged_decode.cu", "static_workspace.cu"]
+SOURCES = ["capi.cu", "kv_append.cu", "paged_decode.cu", "static_workspace.cu", "copy_blocks.cu",
+           "block_manager.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -43,7 +44,7 @@ def _nvcc() -> str:
 
 
 def _inputs() -> list[Path]:
-    return [CSRC / s for s in SOURCES] + list(CSRC.glob("*.h")) + list(INCLUDE.glob("*.h"))
+    return [CSRC / s for s in SOURCES] + list(CSRC.glob("*.h")) + list(INCLUDE.glob("*.h")) + [Path(__file__)]
 
 
 STAMP = BUILD / "flags.txt"

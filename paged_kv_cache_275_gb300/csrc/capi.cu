@@ -165,6 +165,34 @@ pkv_status pkv_kv_append(const void* k, const void* v, const int64_t* slot_mappi
   return ok();
 }
 
+pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_dst, int32_t num_pairs,
+                           int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks, pkv_stream_t stream) {
+  if (num_pairs < 0) return fail(PKV_ERR_INVALID_ARGUMENT, "num_pairs must be >= 0 (got %d)", num_pairs);
+  if (num_pairs > (1 << 30)) return fail(PKV_ERR_UNSUPPORTED, "num_pairs %d too large", num_pairs);
+  if (num_kv_heads <= 0) return fail(PKV_ERR_INVALID_ARGUMENT, "num_kv_heads must be positive (got %d)", num_kv_heads);
+  if (head_dim != 64 && head_dim != 128)
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim %d not built (64 or 128)", head_dim);
+  if (num_blocks <= 0 || num_blocks > (int64_t{1} << 40))
+    return fail(PKV_ERR_INVALID_ARGUMENT, "num_blocks out of range (got %lld)", (long long)num_blocks);
+  if (num_pairs == 0) return ok();
+  if (!k_cache || !v_cache || !src_dst) return fail(PKV_ERR_INVALID_ARGUMENT, "null pointer argument");
+  if (!aligned16(k_cache) || !aligned16(v_cache) || (reinterpret_cast<uintptr_t>(src_dst) & 7u))
+    return fail(PKV_ERR_INVALID_ARGUMENT, "caches must be 16-byte aligned, src_dst 8-byte aligned");
+  unsigned* err = nullptr;
+  if (pkv_status st = device_state(&err, nullptr); st != PKV_OK) return st;
+  pkv::CopyParams p{};
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.src_dst = src_dst;
+  p.err = err;
+  p.num_blocks = num_blocks;
+  p.chunks_per_block = static_cast<int64_t>(num_kv_heads) * PKV_BLOCK_SIZE * head_dim / 8;
+  const cudaError_t e = pkv::launch_copy_blocks(p, num_pairs, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "copy_blocks launch");
+  g_launches.fetch_add(1);
+  return ok();
+}
+
 pkv_status pkv_decode_default_partitions(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                          int32_t head_dim, int32_t max_blocks_per_seq, int32_t* num_partitions) {
   if (!num_partitions) return fail(PKV_ERR_INVALID_ARGUMENT, "num_partitions is null");

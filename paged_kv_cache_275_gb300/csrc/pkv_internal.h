@@ -17,6 +17,7 @@ constexpr unsigned kErrBlockId = 0x2u;
 constexpr unsigned kErrLenNegative = 0x4u;
 constexpr unsigned kErrLenTooLong = 0x8u;
 constexpr unsigned kErrTimeout = 0x10u;
+constexpr unsigned kErrCopyRange = 0x20u;
 
 struct AppendParams {
   const void* k;
@@ -49,6 +50,18 @@ struct DecodeParams {
   int num_partitions;
   float qscale;  // scale * log2(e): scores are kept in base-2 units
 };
+
+struct CopyParams {
+  void* k_cache;
+  void* v_cache;
+  const int64_t* src_dst;  // [num_pairs][2]
+  unsigned* err;
+  int64_t num_blocks;
+  int64_t chunks_per_block;  // 16-byte chunks in one block (all kv heads)
+};
+
+// copy_blocks kernel launch (one CTA per pair and K/V).
+cudaError_t launch_copy_blocks(const CopyParams& p, int num_pairs, cudaStream_t stream);
 
 // Set the per-host-thread message returned by pkv_last_error_message().
 void set_error_message(const char* message);
