@@ -69,6 +69,10 @@ def _load():
         lib.pkv_oracle_paged_decode_sampled.restype = ctypes.c_int
         lib.pkv_oracle_copy_blocks.argtypes = [P, P, P, i64, i32, i32, i64, i32]
         lib.pkv_oracle_copy_blocks.restype = ctypes.c_int
+        lib.pkv_oracle_float_to_bf16.argtypes = [P, P, i64]
+        lib.pkv_oracle_float_to_bf16.restype = ctypes.c_int
+        lib.pkv_oracle_rope.argtypes = [P, i64, i32, i32, P, P, i64]
+        lib.pkv_oracle_rope.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -180,3 +184,52 @@ def copy_blocks(k_cache, v_cache, src_dst) -> int:
     pairs = _as(src_dst, np.int64).reshape(-1, 2)
     num_blocks, hkv, bs, d = kc.shape
     return _load().pkv_oracle_copy_blocks(_ptr(kc), _ptr(vc), _ptr(pairs), pairs.shape[0], hkv, d, num_blocks, bs)
+
+
+def float_to_bf16(x) -> np.ndarray:
+    """fp32 values -> bf16 bit patterns (uint16), round to nearest even."""
+    a = _as(x, np.float32).ravel()
+    out = np.zeros(a.shape, dtype=np.uint16)
+    _load().pkv_oracle_float_to_bf16(_ptr(a), _ptr(out), a.size)
+    return out
+
+
+def rope(x, positions, cos_sin) -> int:
+    """Oracle rotate-half RoPE, in place on a CPU bf16 tensor x [n, heads, D]; cos_sin [max_pos, D] fp32."""
+    xx = _as_u16(x)
+    pos = _as(positions, np.int64)
+    cs = _as(cos_sin, np.float32)
+    n, heads, d = xx.shape
+    if pos.shape != (n,) or cs.ndim != 2 or cs.shape[1] != d:
+        raise ValueError("positions must be [n] and cos_sin [max_position, head_dim]")
+    return _load().pkv_oracle_rope(_ptr(xx), n, heads, d, _ptr(pos), _ptr(cs), cs.shape[0])
+
+
+def decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale, cos_sin=None,
+                num_threads: int | None = None):
+    """One decode step by composition: RoPE of q and the new k at position L - 1, append of the new
+    k / v at that position's slot (through the block table), then attention.  Returns
+    (out float64 [B, Hq, D], status); k_cache / v_cache are updated in place.
+    """
+    import torch
+    lens = _as(context_lens, np.int64)
+    bt = _as(block_tables, np.int64)
+    B = lens.shape[0]
+    live = lens > 0
+    pos = np.where(live, lens - 1, 0)
+    q = q.clone()
+    k_new = k_new.clone()
+    if cos_sin is not None:
+        st = rope(q, pos, cos_sin) | rope(k_new, pos, cos_sin)
+        if st:
+            return None, st
+    bs = k_cache.shape[2]
+    slots = np.full(B, -1, dtype=np.int64)
+    for b in range(B):
+        if live[b]:
+            p = int(pos[b])
+            slots[b] = int(bt[b, p // bs]) * bs + p % bs
+    st = kv_append(k_new, v_new.contiguous(), torch.from_numpy(slots), k_cache, v_cache)
+    if st:
+        return None, st
+    return paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, num_threads)

@@ -322,3 +322,63 @@ int pkv_oracle_copy_blocks(uint16_t* k_cache, uint16_t* v_cache, const int64_t* 
     }
     return status;
 }
+
+/*
+ * fp32 -> bf16, round to nearest, ties to even (the definition: keep the top 16
+ * bits of the binary32 after adding half of the dropped range, plus one more
+ * when the kept part is odd).  NaN stays a quiet NaN.
+ */
+static uint16_t float_to_bf16_rne(float f) {
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((u >> 16) | 0x0040u);
+    const uint32_t lsb = (u >> 16) & 1u;
+    u += 0x7fffu + lsb;
+    return (uint16_t)(u >> 16);
+}
+
+int pkv_oracle_float_to_bf16(const float* in, uint16_t* out, int64_t n) {
+    for (int64_t i = 0; i < n; ++i) out[i] = float_to_bf16_rne(in[i]);
+    return ORACLE_OK;
+}
+
+/*
+ * Rotary position embedding of the new token's q and k before they are used
+ * ("跟着 Claude Code，我用 Python 实现了一个轻量级的 vLLM", section "核心机制五":
+ * a full-attention layer is QKV projection + RoPE + KV cache + SDPA).  The
+ * pages do not spell RoPE out; the reading is the rotate-half form of the
+ * LLaMA / Qwen models they name: for i < D/2, with c = cos_sin[pos][i] and
+ * s = cos_sin[pos][D/2 + i],
+ *     x'[i]       = x[i] * c - x[i + D/2] * s
+ *     x'[i + D/2] = x[i + D/2] * c + x[i] * s
+ * Each product, difference and sum is one fp32 operation rounded to nearest
+ * (this file is built without FMA contraction), and the result is rounded to
+ * bf16, in place.  x is [n][heads][head_dim] bf16; positions is [n].
+ */
+int pkv_oracle_rope(uint16_t* x, int64_t n, int32_t heads, int32_t head_dim, const int64_t* positions,
+                    const float* cos_sin, int64_t max_position) {
+    if (n < 0 || heads <= 0 || head_dim <= 0 || (head_dim & 1)) return ORACLE_BAD_ARGUMENT;
+    const int32_t half = head_dim / 2;
+    for (int64_t r = 0; r < n; ++r) {
+        const int64_t pos = positions[r];
+        if (pos < 0 || pos >= max_position) return ORACLE_CONTEXT_LEN_OUT_OF_RANGE;
+        const float* cs = cos_sin + pos * head_dim;
+        for (int32_t h = 0; h < heads; ++h) {
+            uint16_t* row = x + (r * heads + h) * (int64_t)head_dim;
+            for (int32_t i = 0; i < half; ++i) {
+                const float x1 = (float)bf16_to_double(row[i]);
+                const float x2 = (float)bf16_to_double(row[i + half]);
+                const float c = cs[i], s = cs[half + i];
+                const float a = x1 * c;
+                const float b = x2 * s;
+                const float r1 = a - b;
+                const float e = x2 * c;
+                const float f = x1 * s;
+                const float r2 = e + f;
+                row[i] = float_to_bf16_rne(r1);
+                row[i + half] = float_to_bf16_rne(r2);
+            }
+        }
+    }
+    return ORACLE_OK;
+}

@@ -29,6 +29,9 @@ MUTATIONS = {
         "const int64_t dst = ((block * num_kv_heads + h) * block_size + offset) * (int64_t)head_dim;",
         "const int64_t dst = ((block * block_size + offset) * num_kv_heads + h) * (int64_t)head_dim;"),
     "append_value_from_k": ("v_cache[dst + d] = v[src + d];", "v_cache[dst + d] = k[src + d];"),
+    "rope_sign": ("const float r1 = a - b;", "const float r1 = a + b;"),
+    "rope_cos_sin_swapped": ("const float c = cs[i], s = cs[half + i];", "const float c = cs[half + i], s = cs[i];"),
+    "bf16_truncates": ("u += 0x7fffu + lsb;", "u += 0u;"),
     "table_row_stride": ("P->block_tables[(int64_t)b * P->max_blocks_per_seq + logical_block]",
                          "P->block_tables[(int64_t)b * P->block_size + logical_block]"),
 }

@@ -326,3 +326,62 @@ def test_append_then_attend_equals_contiguous_attention():
         V = f64(tok_v[b]).permute(1, 0, 2).repeat_interleave(hq // hkv, dim=0)
         ref = F.scaled_dot_product_attention(f64(q[b]).unsqueeze(1), K, V, scale=0.09).squeeze(1)
         np.testing.assert_allclose(out[b], ref.numpy(), rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
+# RoPE and bf16 rounding (decode step)
+# ---------------------------------------------------------------------------
+def test_bf16_rounding_matches_torch_including_ties():
+    """Round-to-nearest-even written from the definition equals torch's fp32 -> bf16 cast."""
+    g = make_generator(51)
+    x = torch.randn(200000, generator=g, dtype=torch.float32) * torch.exp(torch.randn(200000, generator=g) * 4)
+    ties = (torch.arange(0, 4096, dtype=torch.int32) << 16 | 0x8000).view(torch.float32)  # exact halfway
+    odd = ((torch.arange(0, 4096, dtype=torch.int32) << 16) | 0x18000).view(torch.float32)
+    x = torch.cat([x, ties, odd, torch.tensor([0.0, -0.0, float("inf"), -float("inf"), 3.4e38, 1e-40])])
+    got = oracle.float_to_bf16(x)
+    want = x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, want)
+
+
+def test_rope_position_zero_is_identity():
+    from workloads import rope_cos_sin
+    g = make_generator(52)
+    x = randn_bf16((5, 3, 128), g)
+    y = x.clone()
+    assert oracle.rope(y, np.zeros(5, np.int64), rope_cos_sin(8, 128)) == oracle.OK
+    assert torch.equal(x, y)
+
+
+@pytest.mark.parametrize("d,theta", [(128, 1e6), (64, 1e4)])
+def test_rope_matches_float64_rotate_half(d, theta):
+    """Against an independent float64 rotate_half on the same table, rounded once to bf16:
+    equal, or one bf16 ulp apart where the fp32 steps round across a boundary (rare)."""
+    from workloads import rope_cos_sin
+    g = make_generator(53)
+    n, heads = 64, 4
+    table = rope_cos_sin(5000, d, theta)
+    pos = torch.randint(0, 5000, (n,), generator=g)
+    x = randn_bf16((n, heads, d), g)
+    y = x.clone()
+    assert oracle.rope(y, pos.numpy(), table) == oracle.OK
+    xf = x.to(torch.float64)
+    c = table[pos, : d // 2].to(torch.float64)[:, None, :]
+    s = table[pos, d // 2:].to(torch.float64)[:, None, :]
+    x1, x2 = xf[..., : d // 2], xf[..., d // 2:]
+    ref = torch.cat([x1 * c - x2 * s, x2 * c + x1 * s], dim=-1).to(torch.float32).to(torch.bfloat16)
+    a = y.view(torch.int16).to(torch.int32)
+    b = ref.view(torch.int16).to(torch.int32)
+    assert (a - b).abs().max().item() <= 1
+    assert (a != b).float().mean().item() < 0.01
+
+
+def test_decode_step_without_rope_is_append_then_attend():
+    c = make_decode_case("qwen3_0.6b", seed=54, lengths=[1, 17, 40, 300])
+    kc, vc = c.k_cache.clone(), c.v_cache.clone()
+    out, st = oracle.decode_step(c.q, c.new_k, c.new_v, kc, vc, c.block_tables, c.context_lens, c.scale)
+    assert st == oracle.OK
+    kc2, vc2 = c.k_cache.clone(), c.v_cache.clone()
+    assert oracle.kv_append(c.new_k, c.new_v, c.slot_mapping, kc2, vc2) == oracle.OK
+    ref = run_oracle(c.q, kc2, vc2, c.block_tables, c.context_lens, c.scale)
+    assert torch.equal(kc, kc2) and torch.equal(vc, vc2)
+    assert np.array_equal(out, ref)

@@ -353,3 +353,13 @@ class TraceGenerator:
                 slot_mapping=torch.tensor(slots, dtype=torch.int64),
                 block_tables=self.alloc.block_table(self.running, self.width),
                 context_lens=torch.tensor([self.alloc.length[s] for s in self.running], dtype=torch.int32))
+
+
+def rope_cos_sin(max_position: int, head_dim: int, theta: float = 10000.0) -> torch.Tensor:
+    """The rotary table the decode step reads: [max_position, head_dim] fp32 with cos in the first half
+    and sin in the second, angle(pos, i) = pos * theta^(-2i / head_dim), computed in fp64, rounded once.
+    (An input table like a weight: Qwen3 uses theta 1e6, LLaMA-3 5e5.)"""
+    half = head_dim // 2
+    inv = theta ** (-2.0 * torch.arange(half, dtype=torch.float64) / head_dim)
+    ang = torch.arange(max_position, dtype=torch.float64)[:, None] * inv[None, :]
+    return torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).to(torch.float32).contiguous()
