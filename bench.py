@@ -268,6 +268,48 @@ def run_reference(args, dist: Dist) -> dict | None:
 # ---------------------------------------------------------------------------
 # GPU side
 # ---------------------------------------------------------------------------
+def fused_step_timing(pkv, g, spec, out, ws, stream, K: int, W: int, bytes_step: int) -> dict:
+    """The same step through pkv_decode_step (RoPE + append + attention in two launches), timed with
+    CUDA events as launched and as a replayed CUDA graph."""
+    from workloads import rope_cos_sin
+    table = rope_cos_sin(spec.max_blocks_per_seq * 16, spec.head_dim, 5e5).to(g.q.device)
+
+    def step():
+        pkv.decode_step(g.q, g.new_k, g.new_v, g.k_cache, g.v_cache, g.block_tables, g.context_lens, g.scale, out,
+                        table, workspace=ws, stream=stream)
+
+    def timed(fn, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        stream.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / n
+
+    with torch.cuda.stream(stream):
+        for _ in range(W):
+            step()
+        sec = timed(step, K)
+    res = {"value": round(bytes_step / sec / 1e9, 2), "unit": "GB/s", "ms_per_step": round(sec * 1e3, 4),
+           "launches_per_step": 2, "rope": "rotate-half, theta 5e5"}
+    try:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        with torch.cuda.stream(stream):
+            for _ in range(W):
+                graph.replay()
+            gsec = timed(graph.replay, K)
+        res["graph"] = {"value": round(bytes_step / gsec / 1e9, 2), "ms_per_step": round(gsec * 1e3, 4)}
+    except Exception as e:  # report, do not fail the headline
+        res["graph"] = {"error": f"{type(e).__name__}: {e}"[:200]}
+    if pkv.get_and_clear_device_error(stream) != 0:
+        raise RuntimeError("device error during the fused-step timing")
+    return res
+
+
 def run_ours(args, dist: Dist) -> dict | None:
     import numpy as np
 
@@ -413,6 +455,7 @@ def run_ours(args, dist: Dist) -> dict | None:
     e2e_elapsed = e0.elapsed_time(e1) / 1e3
     if not torch.equal(out_host, out.cpu()):
         raise RuntimeError("e2e output read-back mismatch")
+    fused = fused_step_timing(pkv, g, spec, out, ws, stream, K, W, bytes_step)
     rows = sampler.stop() if sampler else []
 
     value, slowest = aggregate(bytes_step * K, elapsed, dist)
@@ -452,6 +495,7 @@ def run_ours(args, dist: Dist) -> dict | None:
         "gpu_launches": launches,
         "clocks": clocks,
         "parity": parity,
+        "fused_step": fused,
         "cpu_baseline": cpu,
     }
     return line

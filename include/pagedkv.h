@@ -77,6 +77,7 @@ typedef enum pkv_status {
 #define PKV_DEVERR_CONTEXT_LEN_TOO_LONG 0x8u  /* attention: context_len > 16 * max_blocks_per_seq (clamped) */
 #define PKV_DEVERR_PIPELINE_TIMEOUT 0x10u     /* attention: a shared-memory pipeline wait gave up (partition skipped) */
 #define PKV_DEVERR_COPY_OUT_OF_RANGE 0x20u    /* copy_blocks: a source or destination block outside the pool (pair skipped) */
+#define PKV_DEVERR_POSITION_OUT_OF_TABLE 0x40u /* decode_step: context_len - 1 >= max_position (last table row used) */
 
 /* Largest num_seqs one attention call accepts. */
 #define PKV_MAX_SEQS 4096
@@ -202,6 +203,43 @@ pkv_status pkv_paged_decode_attention_static(const void* q, const void* k_cache,
                                              const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
                                              int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
                                              int32_t block_size, float scale, void* out, pkv_stream_t stream);
+
+/*
+ * One fused decode step: RoPE, append and attention in the two attention
+ * kernels, with no separate append launch.  "跟着 Claude Code，我用 Python 实现了
+ * 一个轻量级的 vLLM", section "核心机制五": a full-attention layer runs QKV
+ * projection + RoPE + KV cache + SDPA; "从零实现一个 mini vLLM--开篇",
+ * section 2: decode appends the new token's K/V, then attends over all of it.
+ *
+ * For every sequence b with L = context_lens[b] >= 1 (L counts the new token,
+ * at position L - 1):
+ *   q'      = RoPE(q[b], L - 1)               rounded to bf16
+ *   k'      = RoPE(k_new[b], L - 1)           rounded to bf16
+ *   slot    = block_tables[b][(L-1) / 16] * 16 + (L-1) % 16
+ *   k_cache / v_cache at slot := k', v_new[b]   (all kv heads)
+ *   out[b]  = paged decode attention of q' over the L tokens (as
+ *             pkv_paged_decode_attention)
+ * RoPE is the rotate-half form: for i < D/2, with c = cos_sin[pos][i] and
+ * s = cos_sin[pos][D/2 + i], x'[i] = x[i] c - x[i + D/2] s and
+ * x'[i + D/2] = x[i + D/2] c + x[i] s, each product and sum one fp32 operation
+ * rounded to nearest (no fused multiply-add).  cos_sin == NULL skips RoPE (the
+ * step is then exactly pkv_kv_append + pkv_paged_decode_attention).
+ *
+ *   q             device, bf16 [num_seqs][num_q_heads][head_dim] (not modified)
+ *   k_new, v_new  device, bf16 [num_seqs][num_kv_heads][head_dim]
+ *   cos_sin       device, fp32 [max_position][head_dim], or NULL
+ *   workspace     as for pkv_paged_decode_attention (same size)
+ * The block holding position L - 1 must belong to sequence b alone (run the
+ * block manager's copy-on-write first).  L == 0 writes zeros and appends
+ * nothing.  Device-side: L - 1 >= max_position sets
+ * PKV_DEVERR_POSITION_OUT_OF_TABLE and uses the last table row.
+ */
+pkv_status pkv_decode_step(const void* q, const void* k_new, const void* v_new, const float* cos_sin,
+                           int64_t max_position, void* k_cache, void* v_cache, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                           int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
+                           int32_t block_size, float scale, void* out, void* workspace, size_t workspace_bytes,
+                           pkv_stream_t stream);
 
 /*
  * Copy whole KV blocks inside the pool: the copy half of copy-on-write for

@@ -30,6 +30,7 @@ DEVERR_CONTEXT_LEN_NEGATIVE = 0x4
 DEVERR_CONTEXT_LEN_TOO_LONG = 0x8
 DEVERR_PIPELINE_TIMEOUT = 0x10
 DEVERR_COPY_OUT_OF_RANGE = 0x20
+DEVERR_POSITION_OUT_OF_TABLE = 0x40
 
 PHASE_PARTITION = 1
 PHASE_MERGE = 2
@@ -47,6 +48,7 @@ EXPORTS = (
     "pkv_paged_decode_attention_split",
     "pkv_paged_decode_attention_static",
     "pkv_copy_blocks",
+    "pkv_decode_step",
     "pkv_bm_create",
     "pkv_bm_destroy",
     "pkv_bm_num_free",
@@ -94,6 +96,8 @@ def load(path: Path | str | None = None) -> ctypes.CDLL:
         lib.pkv_paged_decode_attention_static.argtypes = [V, V, V, V, I32, V, I32, I32, I32, I32, I64, I32,
                                                           ctypes.c_float, V, V]
         lib.pkv_copy_blocks.argtypes = [V, V, V, I32, I32, I32, I64, V]
+        lib.pkv_decode_step.argtypes = [V, V, V, V, I64, V, V, V, I32, V, I32, I32, I32, I32, I64, I32,
+                                        ctypes.c_float, V, V, SZ, V]
         lib.pkv_bm_create.argtypes = [I64, V, ctypes.POINTER(V)]
         lib.pkv_bm_destroy.argtypes = [V]
         lib.pkv_bm_num_free.argtypes = [V, ctypes.POINTER(I64)]
@@ -106,7 +110,7 @@ def load(path: Path | str | None = None) -> ctypes.CDLL:
         lib.pkv_get_and_clear_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), V]
         for name in ("pkv_kv_append", "pkv_decode_workspace_size", "pkv_decode_default_partitions",
                      "pkv_paged_decode_attention", "pkv_paged_decode_attention_split",
-                     "pkv_paged_decode_attention_static", "pkv_get_and_clear_device_error", "pkv_copy_blocks",
+                     "pkv_paged_decode_attention_static", "pkv_get_and_clear_device_error", "pkv_copy_blocks", "pkv_decode_step",
                      "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_num_free", "pkv_bm_add_sequence",
                      "pkv_bm_append_slots", "pkv_bm_fork", "pkv_bm_free_sequence", "pkv_bm_block_tables",
                      "pkv_bm_ref_count"):
@@ -333,3 +337,44 @@ class BlockManager:
         c = ctypes.c_int32(0)
         _check(self._lib.pkv_bm_ref_count(self._h, int(block), ctypes.byref(c)))
         return int(c.value)
+
+
+def decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cache: torch.Tensor,
+                v_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                out: torch.Tensor, cos_sin: torch.Tensor | None = None, *, workspace: torch.Tensor | None = None,
+                stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Fused decode step: RoPE (if cos_sin [max_pos, D] fp32 is given) of q and k_new at position
+    context_len - 1, append of k_new / v_new at that position, attention.  Returns ``out``."""
+    _require(q, "q", torch.bfloat16, 3)
+    dev = q.device
+    for name, t in (("k_new", k_new), ("v_new", v_new)):
+        _require(t, name, torch.bfloat16, 3, dev)
+    _require(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _require(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _require(block_tables, "block_tables", torch.int32, 2, dev)
+    _require(context_lens, "context_lens", torch.int32, 1, dev)
+    _require(out, "out", torch.bfloat16, 3, dev)
+    B, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    if k_new.shape != (B, hkv, d) or v_new.shape != (B, hkv, d) or out.shape != q.shape:
+        raise ValueError("k_new / v_new must be [B, Hkv, D] and out the shape of q")
+    cs_ptr, max_pos = None, 0
+    if cos_sin is not None:
+        _require(cos_sin, "cos_sin", torch.float32, 2, dev)
+        if cos_sin.shape[1] != d:
+            raise ValueError("cos_sin must be [max_position, head_dim]")
+        cs_ptr, max_pos = cos_sin.data_ptr(), cos_sin.shape[0]
+    W = block_tables.shape[1]
+    with torch.cuda.device(dev):
+        sh = _stream_handle(stream)
+        if B == 0:
+            return out
+        nbytes = workspace_size(B, hq, hkv, d, W, 0)
+        if workspace is None:
+            workspace = _workspace(dev, sh, nbytes)
+        wsize = workspace.numel() * workspace.element_size()
+        _check(load().pkv_decode_step(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), cs_ptr, max_pos,
+                                      k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), W,
+                                      context_lens.data_ptr(), B, hq, hkv, d, nb, bs, float(scale), out.data_ptr(),
+                                      workspace.data_ptr(), wsize, sh))
+    return out

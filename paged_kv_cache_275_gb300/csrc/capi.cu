@@ -118,6 +118,87 @@ size_t workspace_bytes_for(int32_t num_seqs, int32_t head_dim, int32_t group, in
 
 }  // namespace
 
+// Fused-step inputs of decode_impl (null for plain attention).
+struct FusedStep {
+  const void* k_new;
+  const void* v_new;
+  const float* cos_sin;
+  int64_t max_position;
+};
+
+static pkv_status decode_impl(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                              int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                              int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
+                              int32_t block_size, float scale, void* out, void* workspace, size_t workspace_bytes,
+                              int32_t num_partitions, int32_t phases, pkv_stream_t stream, const FusedStep* fused) {
+  if (pkv_status st = check_decode_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
+      st != PKV_OK)
+    return st;
+  if (block_size != PKV_BLOCK_SIZE)
+    return fail(PKV_ERR_UNSUPPORTED, "block_size must be %d (got %d)", PKV_BLOCK_SIZE, block_size);
+  if (num_blocks <= 0 || num_blocks > (int64_t{1} << 40))
+    return fail(PKV_ERR_INVALID_ARGUMENT, "num_blocks out of range (got %lld)", (long long)num_blocks);
+  if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID_ARGUMENT, "scale must be finite");
+  if (phases < 1 || phases > PKV_PHASE_ALL) return fail(PKV_ERR_INVALID_ARGUMENT, "phases must be 1, 2 or 3");
+  if (num_partitions < 0 || num_partitions > kMaxPartitions)
+    return fail(PKV_ERR_INVALID_ARGUMENT, "num_partitions out of range (got %d)", num_partitions);
+  if (num_seqs == 0) return ok();
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace)
+    return fail(PKV_ERR_INVALID_ARGUMENT, "null pointer argument");
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(workspace) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
+    return fail(PKV_ERR_INVALID_ARGUMENT, "q, caches, out and workspace must be 16-byte aligned");
+  const int group = num_q_heads / num_kv_heads;
+  if (num_partitions == 0) {
+    if (pkv_status st = default_partitions(num_seqs, num_kv_heads, head_dim, group, max_blocks_per_seq,
+                                           &num_partitions);
+        st != PKV_OK)
+      return st;
+  }
+  const size_t need = workspace_bytes_for(num_seqs, head_dim, group, num_partitions);
+  if (workspace_bytes < need)
+    return fail(PKV_ERR_INVALID_ARGUMENT, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
+
+  unsigned* err = nullptr;
+  if (pkv_status st = device_state(&err, nullptr); st != PKV_OK) return st;
+  pkv::DecodeParams p{};
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.out = out;
+  p.ws_prefix = static_cast<int32_t*>(workspace);
+  p.ws_pieces = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + pkv::workspace_header_bytes(num_seqs));
+  p.err = err;
+  p.num_blocks = num_blocks;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.num_partitions = num_partitions;
+  p.qscale = scale * 1.4426950408889634f;
+  if (fused) {
+    p.k_new = fused->k_new;
+    p.v_new = fused->v_new;
+    p.cos_sin = fused->cos_sin;
+    p.max_position = fused->max_position;
+  }
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (phases & PKV_PHASE_PARTITION) {
+    const cudaError_t e = pkv::launch_decode_partition(p, head_dim, group, s);
+    if (e != cudaSuccess) return cuda_fail(e, "partition kernel launch");
+    g_launches.fetch_add(1);
+  }
+  if (phases & PKV_PHASE_MERGE) {
+    const cudaError_t e = pkv::launch_decode_merge(p, head_dim, group, s);
+    if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+    g_launches.fetch_add(1);
+  }
+  return ok();
+}
+
+
 void pkv::set_error_message(const char* message) { snprintf(t_message, sizeof t_message, "%s", message); }
 
 extern "C" {
@@ -232,65 +313,29 @@ pkv_status pkv_paged_decode_attention_split(const void* q, const void* k_cache, 
                                             int32_t block_size, float scale, void* out, void* workspace,
                                             size_t workspace_bytes, int32_t num_partitions, int32_t phases,
                                             pkv_stream_t stream) {
-  if (pkv_status st = check_decode_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
-      st != PKV_OK)
-    return st;
-  if (block_size != PKV_BLOCK_SIZE)
-    return fail(PKV_ERR_UNSUPPORTED, "block_size must be %d (got %d)", PKV_BLOCK_SIZE, block_size);
-  if (num_blocks <= 0 || num_blocks > (int64_t{1} << 40))
-    return fail(PKV_ERR_INVALID_ARGUMENT, "num_blocks out of range (got %lld)", (long long)num_blocks);
-  if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID_ARGUMENT, "scale must be finite");
-  if (phases < 1 || phases > PKV_PHASE_ALL) return fail(PKV_ERR_INVALID_ARGUMENT, "phases must be 1, 2 or 3");
-  if (num_partitions < 0 || num_partitions > kMaxPartitions)
-    return fail(PKV_ERR_INVALID_ARGUMENT, "num_partitions out of range (got %d)", num_partitions);
-  if (num_seqs == 0) return ok();
-  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out || !workspace)
-    return fail(PKV_ERR_INVALID_ARGUMENT, "null pointer argument");
-  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) || !aligned16(workspace) ||
-      (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
-    return fail(PKV_ERR_INVALID_ARGUMENT, "q, caches, out and workspace must be 16-byte aligned");
-  const int group = num_q_heads / num_kv_heads;
-  if (num_partitions == 0) {
-    if (pkv_status st = default_partitions(num_seqs, num_kv_heads, head_dim, group, max_blocks_per_seq,
-                                           &num_partitions);
-        st != PKV_OK)
-      return st;
-  }
-  const size_t need = workspace_bytes_for(num_seqs, head_dim, group, num_partitions);
-  if (workspace_bytes < need)
-    return fail(PKV_ERR_INVALID_ARGUMENT, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
+  return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
+                     num_kv_heads, head_dim, num_blocks, block_size, scale, out, workspace, workspace_bytes,
+                     num_partitions, phases, stream, nullptr);
+}
 
-  unsigned* err = nullptr;
-  if (pkv_status st = device_state(&err, nullptr); st != PKV_OK) return st;
-  pkv::DecodeParams p{};
-  p.q = q;
-  p.k_cache = k_cache;
-  p.v_cache = v_cache;
-  p.block_tables = block_tables;
-  p.context_lens = context_lens;
-  p.out = out;
-  p.ws_prefix = static_cast<int32_t*>(workspace);
-  p.ws_pieces = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + pkv::workspace_header_bytes(num_seqs));
-  p.err = err;
-  p.num_blocks = num_blocks;
-  p.num_seqs = num_seqs;
-  p.num_q_heads = num_q_heads;
-  p.num_kv_heads = num_kv_heads;
-  p.max_blocks_per_seq = max_blocks_per_seq;
-  p.num_partitions = num_partitions;
-  p.qscale = scale * 1.4426950408889634f;
-  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (phases & PKV_PHASE_PARTITION) {
-    const cudaError_t e = pkv::launch_decode_partition(p, head_dim, group, s);
-    if (e != cudaSuccess) return cuda_fail(e, "partition kernel launch");
-    g_launches.fetch_add(1);
+pkv_status pkv_decode_step(const void* q, const void* k_new, const void* v_new, const float* cos_sin,
+                           int64_t max_position, void* k_cache, void* v_cache, const int32_t* block_tables,
+                           int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                           int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
+                           int32_t block_size, float scale, void* out, void* workspace, size_t workspace_bytes,
+                           pkv_stream_t stream) {
+  if (num_seqs > 0) {
+    if (!k_new || !v_new) return fail(PKV_ERR_INVALID_ARGUMENT, "null pointer argument");
+    if (!aligned16(k_new) || !aligned16(v_new) || (cos_sin && !aligned16(cos_sin)))
+      return fail(PKV_ERR_INVALID_ARGUMENT, "k_new, v_new and cos_sin must be 16-byte aligned");
+    if (cos_sin && max_position <= 0)
+      return fail(PKV_ERR_INVALID_ARGUMENT, "max_position must be positive with a rotary table (got %lld)",
+                  (long long)max_position);
   }
-  if (phases & PKV_PHASE_MERGE) {
-    const cudaError_t e = pkv::launch_decode_merge(p, head_dim, group, s);
-    if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
-    g_launches.fetch_add(1);
-  }
-  return ok();
+  const FusedStep fused{k_new, v_new, cos_sin, cos_sin ? max_position : 0};
+  return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs, num_q_heads,
+                     num_kv_heads, head_dim, num_blocks, block_size, scale, out, workspace, workspace_bytes, 0,
+                     PKV_PHASE_ALL, stream, &fused);
 }
 
 pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,

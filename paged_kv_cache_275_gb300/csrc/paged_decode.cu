@@ -316,6 +316,42 @@ __device__ __forceinline__ void process_block(const unsigned char* sK, const uns
   }
 }
 
+// ---------------------------------------------------------------------------
+// Fused decode step helpers: rotate-half RoPE of one lane's 8 dims.
+// ---------------------------------------------------------------------------
+// x: this lane's 8 values (dims 8c .. 8c+7 of a head row), y: the 8 values D/2
+// away (the rotation partner).  Lanes of the first half rotate x*cos - y*sin,
+// lanes of the second half x*cos + y*sin, with the frequencies of dims
+// (8c + e) mod D/2.  Every product and sum is one fp32 operation rounded to
+// nearest, then the result is rounded to bf16 -- the same steps as the oracle.
+template <int D>
+__device__ __forceinline__ uint4 rope_chunk(uint4 x, uint4 y, const float* cs_row, int c) {
+  const int fbase = (8 * c) % (D / 2);
+  const bool second = (8 * c) >= (D / 2);
+  const uint32_t xw[4] = {x.x, x.y, x.z, x.w};
+  const uint32_t yw[4] = {y.x, y.y, y.z, y.w};
+  uint32_t ow[4];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const float2 xv = bf16x2_to_float2(xw[w]);
+    const float2 yv = bf16x2_to_float2(yw[w]);
+    float r[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const float xe = h ? xv.y : xv.x;
+      const float ye = h ? yv.y : yv.x;
+      const int f = fbase + 2 * w + h;
+      const float cosv = __ldg(cs_row + f);
+      const float sinv = __ldg(cs_row + D / 2 + f);
+      const float a = __fmul_rn(xe, cosv);
+      const float b = __fmul_rn(ye, sinv);
+      r[h] = second ? __fadd_rn(a, b) : __fsub_rn(a, b);
+    }
+    ow[w] = float2_to_bf16x2(r[0], r[1]);
+  }
+  return make_uint4(ow[0], ow[1], ow[2], ow[3]);
+}
+
 // Walk of the flat (sequence, kv head, block) stream.
 struct Cursor {
   int b, kvh, blk, nblk;
@@ -499,12 +535,25 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
       for (int x = i; x < n && x < i + S; ++x) mbar_wait(bar0 + 8 * (x % S), (x / S) & 1, kDrainTimeoutNs);
       return;
     }
+    const int seq_len = s_len[cc.b];
     if (i == 0 || cc.blk == 0) {
-      // First block of a pair in this piece: load the group's q rows from the stage.
+      // First block of a pair in this piece: load the group's q rows from the stage
+      // (rotated to position len - 1 first when the step is fused with RoPE).
       const unsigned char* sq = st_ptr + 2 * T::kTileBytes;
+      const float* cs_row = nullptr;
+      if (p.cos_sin != nullptr) {
+        int64_t pos = seq_len - 1;
+        if (pos >= p.max_position) {
+          if (lane == 0) atomicOr(p.err, kErrPosition);
+          pos = p.max_position - 1;
+        }
+        cs_row = p.cos_sin + pos * D;
+      }
 #pragma unroll
       for (int gp = 0; gp < G; ++gp) {
-        const uint4 w = lds128(sq + (gp ^ mg) * (D * 2) + c * 16);
+        uint4 w = lds128(sq + (gp ^ mg) * (D * 2) + c * 16);
+        if (cs_row != nullptr)
+          w = rope_chunk<D>(w, lds128(sq + (gp ^ mg) * (D * 2) + ((c * 16 + D) % (D * 2))), cs_row, c);
         const float2 s2 = make_float2(qscale, qscale);
         q[gp][0] = __fmul2_rn(bf16x2_to_float2(w.x), s2);
         q[gp][1] = __fmul2_rn(bf16x2_to_float2(w.y), s2);
@@ -521,7 +570,34 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
       }
       pair_from_start = (cc.blk == 0);
     }
-    const int valid = s_len[cc.b] - cc.blk * kBlockTokens;
+    const int valid = seq_len - cc.blk * kBlockTokens;
+    if (p.k_new != nullptr && cc.blk == cc.nblk - 1) {
+      // Fused step: this block holds position len - 1, the step's new token.  Put its
+      // (rotated) K row and its V row into the staged tiles and append them to the cache.
+      const int row = (seq_len - 1) % kBlockTokens;
+      if (half == 0) {
+        const size_t src = (static_cast<size_t>(cc.b) * hkv + cc.kvh) * D;
+        const uint4* kn = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.k_new) + src);
+        const uint4* vn = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.v_new) + src);
+        uint4 kw = __ldg(kn + c);
+        const uint4 vw = __ldg(vn + c);
+        if (p.cos_sin != nullptr) {
+          int64_t pos = seq_len - 1;
+          if (pos >= p.max_position) pos = p.max_position - 1;
+          kw = rope_chunk<D>(kw, __ldg(kn + (c + D / 16) % (D / 8)), p.cos_sin + pos * D, c);
+        }
+        unsigned char* st_w = ring_ptr + stage * T::kStageBytes;
+        *reinterpret_cast<uint4*>(st_w + row * (D * 2) + c * 16) = kw;
+        *reinterpret_cast<uint4*>(st_w + T::kTileBytes + row * (D * 2) + c * 16) = vw;
+        int id = __ldg(p.block_tables + static_cast<size_t>(cc.b) * p.max_blocks_per_seq + cc.blk);
+        if (id >= 0 && id < p.num_blocks) {
+          const size_t dst = ((static_cast<size_t>(id) * hkv + cc.kvh) * kBlockTokens + row) * D;
+          reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(const_cast<void*>(p.k_cache)) + dst)[c] = kw;
+          reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(const_cast<void*>(p.v_cache)) + dst)[c] = vw;
+        }
+      }
+      __syncwarp();
+    }
     if (valid >= kBlockTokens)
       process_block<D, G, false>(st_ptr, st_ptr + T::kTileBytes, ptile, q, acc, m_ref, m_mine, l_mine, c, half,
                                  mask, kBlockTokens);

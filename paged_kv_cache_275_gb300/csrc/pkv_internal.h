@@ -18,6 +18,7 @@ constexpr unsigned kErrLenNegative = 0x4u;
 constexpr unsigned kErrLenTooLong = 0x8u;
 constexpr unsigned kErrTimeout = 0x10u;
 constexpr unsigned kErrCopyRange = 0x20u;
+constexpr unsigned kErrPosition = 0x40u;
 
 struct AppendParams {
   const void* k;
@@ -49,6 +50,12 @@ struct DecodeParams {
   int max_blocks_per_seq;
   int num_partitions;
   float qscale;  // scale * log2(e): scores are kept in base-2 units
+  // Fused decode step (all null for plain attention): this step's token of every
+  // (sequence, kv head), appended at position context_len - 1, and the rotary table.
+  const void* k_new;     // bf16 [num_seqs][num_kv_heads][head_dim] or null
+  const void* v_new;     // bf16 [num_seqs][num_kv_heads][head_dim]
+  const float* cos_sin;  // fp32 [max_position][head_dim] (cos | sin) or null: no RoPE
+  int64_t max_position;
 };
 
 struct CopyParams {
