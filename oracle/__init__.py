@@ -73,6 +73,9 @@ def _load():
         lib.pkv_oracle_float_to_bf16.restype = ctypes.c_int
         lib.pkv_oracle_rope.argtypes = [P, i64, i32, i32, P, P, i64]
         lib.pkv_oracle_rope.restype = ctypes.c_int
+        lib.pkv_oracle_paged_prefill_attention.argtypes = [P, P, P, P, i32, P, P, i32, i32, i32, i32, i64, i32,
+                                                           dbl, P, i32]
+        lib.pkv_oracle_paged_prefill_attention.restype = ctypes.c_int
         _lib = lib
     return _lib
 
@@ -233,3 +236,23 @@ def decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, s
     if st:
         return None, st
     return paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, num_threads)
+
+
+def paged_prefill_attention(q, k_cache, v_cache, block_tables, context_lens, query_start, scale: float,
+                            num_threads: int | None = None) -> tuple[np.ndarray, int]:
+    """Oracle chunked prefill: q [T, Hq, D] bf16, query_start [B + 1]; returns (out [T, Hq, D] float64, status)."""
+    qq = _as_u16(q)
+    kc, vc = _as_u16(k_cache), _as_u16(v_cache)
+    bt = _as(block_tables, np.int32)
+    cl = _as(context_lens, np.int32)
+    qs = _as(query_start, np.int32)
+    T, hq, d = qq.shape
+    num_blocks, hkv, bs, d2 = kc.shape
+    B = cl.shape[0]
+    if d2 != d or qs.shape != (B + 1,) or bt.shape[0] != B or int(qs[-1]) != T:
+        raise ValueError("shape mismatch")
+    out = np.zeros((T, hq, d), dtype=np.float64)
+    st = _load().pkv_oracle_paged_prefill_attention(
+        _ptr(qq), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(cl), _ptr(qs), B, hq, hkv, d, num_blocks, bs,
+        float(scale), _ptr(out), num_threads or default_threads())
+    return out, st

@@ -133,29 +133,27 @@ typedef struct {
     double scale;
 } problem_t;
 
+/* GQA: q head h reads kv head h / (Hq / Hkv) (contiguous groups). */
+static int32_t kv_head_of(const problem_t* P, int32_t h) {
+    const int32_t group = P->num_q_heads / P->num_kv_heads;
+    const int32_t kv = h / group;
+    return kv;
+}
+
 /*
- * Decode attention for one (sequence b, q head h) [P2 section 5, phases 4-5;
- * P2 section 2]:
- *   kv   = h / (Hq / Hkv)
+ * Attention of one query row over the first L cached tokens of sequence b,
+ * kv head kv [P2 section 5, phases 4-5; P2 section 2]:
  *   K_t  = k_cache[block_tables[b, t / bs], kv, t % bs, :]   for t < L
  *   V_t  = v_cache[block_tables[b, t / bs], kv, t % bs, :]
- *   s_t  = scale * sum_d q[b, h, d] * K_t[d]
+ *   s_t  = scale * sum_d qrow[d] * K_t[d]
  *   p_t  = exp(s_t - max_t s_t) / sum_u exp(s_u - max_t s_t)
  *   out  = sum_t p_t * V_t
  * Writes head_dim doubles to out_row.  L == 0 writes zeros.
  */
-static int decode_one(const problem_t* P, int32_t b, int32_t h, double* out_row) {
+static int attend_one(const problem_t* P, int32_t b, int32_t kv, const uint16_t* qrow, int32_t L, double* out_row) {
     const int32_t D = P->head_dim;
     for (int32_t d = 0; d < D; ++d) out_row[d] = 0.0;
-    if (b < 0 || b >= P->num_seqs || h < 0 || h >= P->num_q_heads) return ORACLE_BAD_ARGUMENT;
-    const int32_t L = P->context_lens[b];
-    if (L < 0 || (int64_t)L > (int64_t)P->max_blocks_per_seq * P->block_size)
-        return ORACLE_CONTEXT_LEN_OUT_OF_RANGE;
     if (L == 0) return ORACLE_OK;
-
-    const int32_t group = P->num_q_heads / P->num_kv_heads;
-    const int32_t kv = h / group;
-    const uint16_t* qrow = P->q + ((int64_t)b * P->num_q_heads + h) * D;
 
     double* scores = (double*)malloc(sizeof(double) * (size_t)L);
     const uint16_t** vrows = (const uint16_t**)malloc(sizeof(uint16_t*) * (size_t)L);
@@ -202,6 +200,18 @@ static int decode_one(const problem_t* P, int32_t b, int32_t h, double* out_row)
     free(scores);
     free((void*)vrows);
     return ORACLE_OK;
+}
+
+/* Decode: q row (b, h) attends over all context_lens[b] cached tokens. */
+static int decode_one(const problem_t* P, int32_t b, int32_t h, double* out_row) {
+    const int32_t D = P->head_dim;
+    for (int32_t d = 0; d < D; ++d) out_row[d] = 0.0;
+    if (b < 0 || b >= P->num_seqs || h < 0 || h >= P->num_q_heads) return ORACLE_BAD_ARGUMENT;
+    const int32_t L = P->context_lens[b];
+    if (L < 0 || (int64_t)L > (int64_t)P->max_blocks_per_seq * P->block_size)
+        return ORACLE_CONTEXT_LEN_OUT_OF_RANGE;
+    const uint16_t* qrow = P->q + ((int64_t)b * P->num_q_heads + h) * D;
+    return attend_one(P, b, kv_head_of(P, h), qrow, L, out_row);
 }
 
 typedef struct {
@@ -381,4 +391,89 @@ int pkv_oracle_rope(uint16_t* x, int64_t n, int32_t heads, int32_t head_dim, con
         }
     }
     return ORACLE_OK;
+}
+
+/*
+ * Chunked prefill ("从零实现一个 mini vLLM--开篇", section 2: prefill runs the
+ * whole prompt at once and stores every layer's K and V; section 5 lists
+ * chunked prefill as a later topic).  Sequence b appends C_b new tokens,
+ * C_b = query_start[b+1] - query_start[b], after P_b = context_lens[b] - C_b
+ * cached ones (context_lens counts them all, the chunk's K/V already
+ * appended).  Query row t = query_start[b] + i (i < C_b) sits at position
+ * P_b + i and, causally, attends over the first P_b + i + 1 cached tokens.
+ * q and out are [T][Hq][D] with T = query_start[num_seqs].
+ */
+typedef struct {
+    const problem_t* P;
+    const int32_t* query_start;
+    int64_t begin, end;  /* items t * Hq + h */
+    double* out;
+    int status;
+} prefill_job_t;
+
+static int prefill_one(const problem_t* P, const int32_t* query_start, int64_t item, double* out_row) {
+    const int32_t D = P->head_dim;
+    const int64_t t = item / P->num_q_heads;
+    const int32_t h = (int32_t)(item % P->num_q_heads);
+    int32_t b = 0;
+    while (b < P->num_seqs && (int64_t)query_start[b + 1] <= t) ++b;
+    for (int32_t d = 0; d < D; ++d) out_row[d] = 0.0;
+    if (b >= P->num_seqs) return ORACLE_BAD_ARGUMENT;
+    const int32_t C = query_start[b + 1] - query_start[b];
+    const int32_t Lb = P->context_lens[b];
+    const int32_t i = (int32_t)(t - query_start[b]);
+    if (C < 0 || Lb < C || (int64_t)Lb > (int64_t)P->max_blocks_per_seq * P->block_size)
+        return ORACLE_CONTEXT_LEN_OUT_OF_RANGE;
+    const int32_t prefix = Lb - C;
+    const uint16_t* qrow = P->q + (t * P->num_q_heads + h) * D;
+    return attend_one(P, b, kv_head_of(P, h), qrow, prefix + i + 1, out_row);
+}
+
+static void* run_prefill_job(void* arg) {
+    prefill_job_t* J = (prefill_job_t*)arg;
+    for (int64_t it = J->begin; it < J->end; ++it)
+        J->status |= prefill_one(J->P, J->query_start, it, J->out + it * J->P->head_dim);
+    return NULL;
+}
+
+int pkv_oracle_paged_prefill_attention(const uint16_t* q, const uint16_t* k_cache, const uint16_t* v_cache,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* context_lens, const int32_t* query_start, int32_t num_seqs,
+                                       int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                       int64_t num_blocks, int32_t block_size, double scale, double* out,
+                                       int32_t num_threads) {
+    problem_t P = {q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                   num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale};
+    if (num_kv_heads <= 0 || num_q_heads <= 0 || num_q_heads % num_kv_heads != 0 || head_dim <= 0 ||
+        block_size <= 0 || num_seqs < 0)
+        return ORACLE_BAD_ARGUMENT;
+    for (int32_t b = 0; b < num_seqs; ++b)
+        if (query_start[b + 1] < query_start[b]) return ORACLE_BAD_ARGUMENT;
+    const int64_t items = (int64_t)query_start[num_seqs] * num_q_heads;
+    if (items <= 0) return ORACLE_OK;
+    if (num_threads < 1) num_threads = 1;
+    if (num_threads > 256) num_threads = 256;
+    if ((int64_t)num_threads > items) num_threads = (int32_t)items;
+    prefill_job_t jobs[256];
+    pthread_t threads[256];
+    int started[256];
+    for (int32_t k = 0; k < num_threads; ++k) {
+        jobs[k].P = &P;
+        jobs[k].query_start = query_start;
+        jobs[k].begin = items * k / num_threads;
+        jobs[k].end = items * (k + 1) / num_threads;
+        jobs[k].out = out;
+        jobs[k].status = 0;
+        started[k] = 0;
+    }
+    for (int32_t k = 1; k < num_threads; ++k)
+        started[k] = (pthread_create(&threads[k], NULL, run_prefill_job, &jobs[k]) == 0);
+    run_prefill_job(&jobs[0]);
+    int status = jobs[0].status;
+    for (int32_t k = 1; k < num_threads; ++k) {
+        if (started[k]) pthread_join(threads[k], NULL);
+        else run_prefill_job(&jobs[k]);
+        status |= jobs[k].status;
+    }
+    return status;
 }

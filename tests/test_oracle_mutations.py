@@ -32,6 +32,7 @@ MUTATIONS = {
     "rope_sign": ("const float r1 = a - b;", "const float r1 = a + b;"),
     "rope_cos_sin_swapped": ("const float c = cs[i], s = cs[half + i];", "const float c = cs[half + i], s = cs[i];"),
     "bf16_truncates": ("u += 0x7fffu + lsb;", "u += 0u;"),
+    "prefill_causal_off_by_one": ("prefix + i + 1, out_row);", "prefix + i, out_row);"),
     "table_row_stride": ("P->block_tables[(int64_t)b * P->max_blocks_per_seq + logical_block]",
                          "P->block_tables[(int64_t)b * P->block_size + logical_block]"),
 }

@@ -385,3 +385,67 @@ def test_decode_step_without_rope_is_append_then_attend():
     ref = run_oracle(c.q, kc2, vc2, c.block_tables, c.context_lens, c.scale)
     assert torch.equal(kc, kc2) and torch.equal(vc, vc2)
     assert np.array_equal(out, ref)
+
+
+# ---------------------------------------------------------------------------
+# Chunked prefill
+# ---------------------------------------------------------------------------
+def _prefill_ref_sdpa(c):
+    """torch float64 SDPA per sequence on un-paged K/V with the causal mask offset by the prefix."""
+    T, hq, d = c.q.shape
+    hkv = c.k_cache.shape[1]
+    out = torch.zeros(T, hq, d, dtype=torch.float64)
+    qs = c.query_start.tolist()
+    for b, L in enumerate(c.context_lens.tolist()):
+        C = qs[b + 1] - qs[b]
+        P = L - C
+        K, V = contiguous_kv(c.k_cache, c.v_cache, c.block_tables, c.context_lens, b)
+        K = K.repeat_interleave(hq // hkv, dim=0)
+        V = V.repeat_interleave(hq // hkv, dim=0)
+        qb = f64(c.q[qs[b]:qs[b + 1]]).permute(1, 0, 2)               # [hq, C, d]
+        mask = torch.arange(L)[None, :] <= (P + torch.arange(C))[:, None]
+        o = F.scaled_dot_product_attention(qb, K, V, attn_mask=mask, scale=c.scale)
+        out[qs[b]:qs[b + 1]] = o.permute(1, 0, 2)
+    return out.numpy()
+
+
+def _appended(c):
+    kc, vc = c.k_cache.clone(), c.v_cache.clone()
+    assert oracle.kv_append(c.new_k, c.new_v, c.slot_mapping, kc, vc) == oracle.OK
+    return kc, vc
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_prefill_matches_causal_sdpa(seed):
+    from workloads import make_prefill_case
+    c = make_prefill_case("prefill_tiny", seed=seed)
+    c.k_cache, c.v_cache = _appended(c)
+    out, st = oracle.paged_prefill_attention(c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens,
+                                             c.query_start, c.scale)
+    assert st == oracle.OK
+    np.testing.assert_allclose(out, _prefill_ref_sdpa(c), rtol=0, atol=1e-12)
+
+
+def test_prefill_with_chunks_of_one_is_decode():
+    from workloads import PrefillSpec, make_prefill_case
+    spec = PrefillSpec("ones", "", 8, 2, 128, (1, 1, 1), (0, 60), 5)
+    c = make_prefill_case(spec, seed=2)
+    out, st = oracle.paged_prefill_attention(c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens,
+                                             c.query_start, c.scale)
+    dec, st2 = oracle.paged_decode_attention(c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens, c.scale)
+    assert st == st2 == oracle.OK and np.array_equal(out, dec)
+
+
+def test_prefill_last_chunk_row_is_decode_and_first_row_with_no_prefix_is_its_value():
+    from workloads import make_prefill_case
+    c = make_prefill_case("prefill_tiny", seed=3, prefixes=[0, 21])
+    out, _ = oracle.paged_prefill_attention(c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens,
+                                            c.query_start, c.scale)
+    qs = c.query_start.tolist()
+    last = torch.tensor([qs[1] - 1, qs[2] - 1])
+    dec, _ = oracle.paged_decode_attention(c.q[last].contiguous(), c.k_cache, c.v_cache, c.block_tables,
+                                           c.context_lens, c.scale)
+    assert np.array_equal(out[last.numpy()], dec)
+    # Sequence 0 has no prefix: its first query row sees one token, so out = V_0.
+    v0 = f64(c.v_cache[int(c.block_tables[0, 0]), :, 0]).numpy()       # [hkv, d]
+    assert np.array_equal(out[0], np.repeat(v0, 2, axis=0))

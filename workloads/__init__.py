@@ -363,3 +363,89 @@ def rope_cos_sin(max_position: int, head_dim: int, theta: float = 10000.0) -> to
     inv = theta ** (-2.0 * torch.arange(half, dtype=torch.float64) / head_dim)
     ang = torch.arange(max_position, dtype=torch.float64)[:, None] * inv[None, :]
     return torch.cat([torch.cos(ang), torch.sin(ang)], dim=1).to(torch.float32).contiguous()
+
+
+# ----------------------------------------------------------------------------
+# Chunked prefill: C new tokens per sequence after P cached ones.
+# ----------------------------------------------------------------------------
+@dataclass(frozen=True)
+class PrefillSpec:
+    name: str
+    description: str
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    chunk_lens: tuple          # C_b
+    prefix_range: tuple        # P_b ~ U{lo..hi}
+    max_blocks_per_seq: int
+
+
+PREFILL_SPECS = {
+    "prefill_tiny": PrefillSpec("prefill_tiny", "2 seqs, chunks 5 and 33, 4 q / 2 kv, D 64", 4, 2, 64, (5, 33),
+                                (0, 40), 6),
+    "prefill_qwen3_0.6b": PrefillSpec("prefill_qwen3_0.6b", "Qwen3-0.6B layer: 4 chunks of 512 after 0..2048 cached",
+                                      16, 8, 128, (512, 512, 512, 512), (0, 2048), 160),
+    "prefill_llama3_8b": PrefillSpec("prefill_llama3_8b",
+                                     "LLaMA-3-8B layer: 8 chunks of 512 after 0..3584 cached (32 q / 8 kv)",
+                                     32, 8, 128, (512,) * 8, (0, 3584), 256),
+}
+
+
+@dataclass
+class PrefillCase:
+    spec: PrefillSpec
+    q: torch.Tensor              # [T, Hq, D] bf16
+    k_cache: torch.Tensor        # [NB, Hkv, 16, D]
+    v_cache: torch.Tensor
+    block_tables: torch.Tensor   # [B, W] int32
+    context_lens: torch.Tensor   # [B] int32 = prefix + chunk
+    query_start: torch.Tensor    # [B + 1] int32
+    new_k: torch.Tensor          # [T, Hkv, D]: the chunks' K/V, to append before attending
+    new_v: torch.Tensor
+    slot_mapping: torch.Tensor   # [T] int64
+    scale: float
+
+    def to(self, device) -> "PrefillCase":
+        return PrefillCase(self.spec, *(t.to(device) for t in (
+            self.q, self.k_cache, self.v_cache, self.block_tables, self.context_lens, self.query_start, self.new_k,
+            self.new_v, self.slot_mapping)), self.scale)
+
+
+def make_prefill_case(name: str | PrefillSpec, seed: int = 0, prefixes=None, device="cpu") -> PrefillCase:
+    spec = PREFILL_SPECS[name] if isinstance(name, str) else name
+    g = make_generator(seed)
+    B = len(spec.chunk_lens)
+    lo, hi = spec.prefix_range
+    pre = [int(x) for x in (prefixes if prefixes is not None else torch.randint(lo, hi + 1, (B,), generator=g))]
+    lens = [p + c for p, c in zip(pre, spec.chunk_lens)]
+    if max(lens) > spec.max_blocks_per_seq * BLOCK_SIZE:
+        raise ValueError("sequence longer than the block table")
+    num_blocks = sum(-(-L // BLOCK_SIZE) for L in lens) + 4
+    alloc = BlockAllocator(num_blocks, g)
+    chunk_slots = []
+    for b, (p, L) in enumerate(zip(pre, lens)):
+        s = alloc.add_sequence(b, L)
+        chunk_slots += s[p:]
+    tables = alloc.block_table(list(range(B)), spec.max_blocks_per_seq)
+    T = sum(spec.chunk_lens)
+    qs = [0]
+    for c in spec.chunk_lens:
+        qs.append(qs[-1] + c)
+    Hq, Hkv, D = spec.num_q_heads, spec.num_kv_heads, spec.head_dim
+    return PrefillCase(spec, randn_bf16((T, Hq, D), g), randn_bf16((num_blocks, Hkv, BLOCK_SIZE, D), g),
+                       randn_bf16((num_blocks, Hkv, BLOCK_SIZE, D), g), tables,
+                       torch.tensor(lens, dtype=torch.int32), torch.tensor(qs, dtype=torch.int32),
+                       randn_bf16((T, Hkv, D), g), randn_bf16((T, Hkv, D), g),
+                       torch.tensor(chunk_slots, dtype=torch.int64), 1.0 / math.sqrt(D)).to(device)
+
+
+def prefill_flops(context_lens, query_start, num_q_heads: int, head_dim: int) -> int:
+    """Causal attention flops of a prefill call: 4 * D per (query row, visible key, q head)."""
+    lens = [int(x) for x in context_lens]
+    qs = [int(x) for x in query_start]
+    total = 0
+    for b, L in enumerate(lens):
+        C = qs[b + 1] - qs[b]
+        P = L - C
+        total += C * P + C * (C + 1) // 2
+    return 4 * head_dim * num_q_heads * total
