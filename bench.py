@@ -51,6 +51,13 @@ FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 126 * 2 ** 20
 
 
+def bf16_peak_tflops() -> tuple[float, str]:
+    try:
+        return float(json.loads((ROOT / "MEASURED_PEAKS.json").read_text())["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
 def peaks() -> tuple[float, str]:
     p = ROOT / "MEASURED_PEAKS.json"
     try:
@@ -528,6 +535,41 @@ def run_component(args) -> dict:
         return {"component": "block_manager", "metric": "append slots per second (host, one thread)",
                 "value": round(256 * args.steps / dt, 1), "unit": "slot/s", "steps": args.steps,
                 "us_per_batch_of_256": round(1e6 * dt / args.steps, 2), "kind": "C ABI through ctypes"}
+    if args.component == "prefill":
+        from workloads import make_prefill_case, prefill_flops
+        c = make_prefill_case("prefill_llama3_8b", seed=0).to("cuda")
+        pkv.kv_append(c.new_k, c.new_v, c.slot_mapping, c.k_cache, c.v_cache)
+        out = torch.empty_like(c.q)
+        max_q = max(c.spec.chunk_lens)
+
+        def call():
+            pkv.paged_prefill_attention(c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens, c.query_start,
+                                        max_q, c.scale, out)
+
+        for _ in range(args.warmup):
+            call()
+        stream = torch.cuda.current_stream()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(args.steps):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if pkv.get_and_clear_device_error() != 0:
+            raise RuntimeError("device error during the prefill timing")
+        sec = e0.elapsed_time(e1) / 1e3 / args.steps
+        flops = prefill_flops(c.context_lens.cpu(), c.query_start.cpu(), c.spec.num_q_heads, c.spec.head_dim)
+        tf = flops / sec / 1e12
+        bf16_peak, kind = bf16_peak_tflops()
+        return {"component": "prefill", "metric": "chunked paged prefill attention TFLOP/s (causal flops)",
+                "value": round(tf, 2), "unit": "TFLOP/s", "steps": args.steps, "warmup": args.warmup,
+                "us_per_launch": round(sec * 1e6, 2),
+                "config": {"workload": c.spec.description, "tokens": int(c.q.shape[0]),
+                           "context_lens": c.context_lens.tolist()},
+                "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": bf16_peak, "unit": "TFLOP/s",
+                             "frac": round(tf / bf16_peak, 4), "frac_of": f"{kind} bf16 dense (cuBLAS burst)",
+                             "algorithmic_flops_per_launch": flops, "traffic": None}}
     # copy_blocks: copy-on-write of 4096 distinct block pairs of the Qwen3/LLaMA-3 kv layout.
     dev = torch.device("cuda", 0)
     g = make_generator(7)
@@ -575,7 +617,7 @@ def main(argv=None) -> int:
                     help="seconds the reference arm's warm-up + timed steps should take")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per partition launch from an ncu capture of the current kernel")
-    ap.add_argument("--component", choices=("copy_blocks", "block_manager"), default=None,
+    ap.add_argument("--component", choices=("copy_blocks", "block_manager", "prefill"), default=None,
                     help="measure one component instead of the decode step")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -242,6 +242,37 @@ pkv_status pkv_decode_step(const void* q, const void* k_new, const void* v_new, 
                            pkv_stream_t stream);
 
 /*
+ * Chunked paged prefill attention, on the tensor cores.  "从零实现一个 mini
+ * vLLM--开篇", section 2: prefill runs the prompt at once and keeps every
+ * layer's K and V; section 5 lists chunked prefill.  Sequence b appends C_b new
+ * tokens, C_b = query_start[b+1] - query_start[b], after P_b cached ones;
+ * context_lens[b] = P_b + C_b counts them all and the chunk's K/V must already
+ * be in the cache (pkv_kv_append).  Query row t = query_start[b] + i attends
+ * causally over the first P_b + i + 1 tokens:
+ *
+ *   out[t][h][:] = sum_{j <= P_b + i} softmax_j(scale * <q[t][h], K_j>) V_j
+ *
+ * with K_j / V_j found through block_tables as in paged decode (kv head h / G).
+ * bf16 in and out; S = q K^T and O = P V run as tcgen05 MMAs with fp32
+ * accumulation, P is rounded to bf16 for the second product (the softmax
+ * denominator sums the same rounded values).
+ *
+ *   q, out        device, bf16 [T][num_q_heads][head_dim], T = query_start[num_seqs]
+ *   query_start   device, int32 [num_seqs + 1], non-decreasing, query_start[0] = 0
+ *   max_query_len host: at least every C_b (sizes the grid)
+ * No workspace.  num_seqs == 0 or max_query_len == 0 is a no-op.  Device-side:
+ * C_b > max_query_len or C_b > context_lens[b] sets
+ * PKV_DEVERR_CONTEXT_LEN_TOO_LONG (that sequence is skipped or cut); a bad
+ * block id sets PKV_DEVERR_BLOCK_ID_OUT_OF_RANGE (block 0 is read instead).
+ */
+pkv_status pkv_paged_prefill_attention(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* context_lens, const int32_t* query_start,
+                                       int32_t max_query_len, int32_t num_seqs, int32_t num_q_heads,
+                                       int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks, int32_t block_size,
+                                       float scale, void* out, pkv_stream_t stream);
+
+/*
  * Copy whole KV blocks inside the pool: the copy half of copy-on-write for
  * blocks shared between sequences.  The pages let requests share a prompt's
  * KV blocks ("v0版本介绍", section "为什么需要推理框架") and plan a prefix

@@ -49,6 +49,7 @@ EXPORTS = (
     "pkv_paged_decode_attention_static",
     "pkv_copy_blocks",
     "pkv_decode_step",
+    "pkv_paged_prefill_attention",
     "pkv_bm_create",
     "pkv_bm_destroy",
     "pkv_bm_num_free",
@@ -98,6 +99,8 @@ def load(path: Path | str | None = None) -> ctypes.CDLL:
         lib.pkv_copy_blocks.argtypes = [V, V, V, I32, I32, I32, I64, V]
         lib.pkv_decode_step.argtypes = [V, V, V, V, I64, V, V, V, I32, V, I32, I32, I32, I32, I64, I32,
                                         ctypes.c_float, V, V, SZ, V]
+        lib.pkv_paged_prefill_attention.argtypes = [V, V, V, V, I32, V, V, I32, I32, I32, I32, I32, I64, I32,
+                                                    ctypes.c_float, V, V]
         lib.pkv_bm_create.argtypes = [I64, V, ctypes.POINTER(V)]
         lib.pkv_bm_destroy.argtypes = [V]
         lib.pkv_bm_num_free.argtypes = [V, ctypes.POINTER(I64)]
@@ -110,7 +113,7 @@ def load(path: Path | str | None = None) -> ctypes.CDLL:
         lib.pkv_get_and_clear_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), V]
         for name in ("pkv_kv_append", "pkv_decode_workspace_size", "pkv_decode_default_partitions",
                      "pkv_paged_decode_attention", "pkv_paged_decode_attention_split",
-                     "pkv_paged_decode_attention_static", "pkv_get_and_clear_device_error", "pkv_copy_blocks", "pkv_decode_step",
+                     "pkv_paged_decode_attention_static", "pkv_get_and_clear_device_error", "pkv_copy_blocks", "pkv_decode_step", "pkv_paged_prefill_attention",
                      "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_num_free", "pkv_bm_add_sequence",
                      "pkv_bm_append_slots", "pkv_bm_fork", "pkv_bm_free_sequence", "pkv_bm_block_tables",
                      "pkv_bm_ref_count"):
@@ -377,4 +380,32 @@ def decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cac
                                       k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), W,
                                       context_lens.data_ptr(), B, hq, hkv, d, nb, bs, float(scale), out.data_ptr(),
                                       workspace.data_ptr(), wsize, sh))
+    return out
+
+
+def paged_prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            block_tables: torch.Tensor, context_lens: torch.Tensor, query_start: torch.Tensor,
+                            max_query_len: int, scale: float, out: torch.Tensor,
+                            stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+    """Chunked prefill: q / out [T, Hq, D] bf16, query_start [B + 1] int32; causal over each sequence's
+    context_lens[b] - (chunk length) cached tokens plus the chunk.  Returns ``out``."""
+    _require(q, "q", torch.bfloat16, 3)
+    dev = q.device
+    _require(k_cache, "k_cache", torch.bfloat16, 4, dev)
+    _require(v_cache, "v_cache", torch.bfloat16, 4, dev)
+    _require(block_tables, "block_tables", torch.int32, 2, dev)
+    _require(context_lens, "context_lens", torch.int32, 1, dev)
+    _require(query_start, "query_start", torch.int32, 1, dev)
+    _require(out, "out", torch.bfloat16, 3, dev)
+    T, hq, d = q.shape
+    nb, hkv, bs, _ = k_cache.shape
+    B = context_lens.shape[0]
+    if out.shape != q.shape or query_start.shape[0] != B + 1 or block_tables.shape[0] != B:
+        raise ValueError("shape mismatch")
+    with torch.cuda.device(dev):
+        _check(load().pkv_paged_prefill_attention(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                                  block_tables.data_ptr(), block_tables.shape[1],
+                                                  context_lens.data_ptr(), query_start.data_ptr(), int(max_query_len),
+                                                  B, hq, hkv, d, nb, bs, float(scale), out.data_ptr(),
+                                                  _stream_handle(stream)))
     return out

@@ -24,7 +24,7 @@ INCLUDE = ROOT / "include"
 BUILD = PKG / "_build"
 LIB = PKG / "libpagedkv.so"
 SOURCES = ["capi.cu", "kv_append.cu", "paged_decode.cu", "static_workspace.cu", "copy_blocks.cu",
-           "block_manager.cpp"]
+           "block_manager.cpp", "paged_prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

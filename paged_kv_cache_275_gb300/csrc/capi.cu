@@ -274,6 +274,53 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_dst,
   return ok();
 }
 
+pkv_status pkv_paged_prefill_attention(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* context_lens, const int32_t* query_start,
+                                       int32_t max_query_len, int32_t num_seqs, int32_t num_q_heads,
+                                       int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks, int32_t block_size,
+                                       float scale, void* out, pkv_stream_t stream) {
+  if (pkv_status st = check_decode_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
+      st != PKV_OK)
+    return st;
+  if (block_size != PKV_BLOCK_SIZE)
+    return fail(PKV_ERR_UNSUPPORTED, "block_size must be %d (got %d)", PKV_BLOCK_SIZE, block_size);
+  if (num_blocks <= 0 || num_blocks * num_kv_heads * PKV_BLOCK_SIZE >= (int64_t{1} << 31))
+    return fail(PKV_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * 16 must be in (0, 2^31) (got %lld blocks)",
+                (long long)num_blocks);
+  if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID_ARGUMENT, "scale must be finite");
+  if (max_query_len < 0) return fail(PKV_ERR_INVALID_ARGUMENT, "max_query_len must be >= 0 (got %d)", max_query_len);
+  if (num_seqs == 0 || max_query_len == 0) return ok();
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start || !out)
+    return fail(PKV_ERR_INVALID_ARGUMENT, "null pointer argument");
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out) ||
+      (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u) ||
+      (reinterpret_cast<uintptr_t>(query_start) & 3u))
+    return fail(PKV_ERR_INVALID_ARGUMENT, "q, caches and out must be 16-byte aligned");
+  unsigned* err = nullptr;
+  if (pkv_status st = device_state(&err, nullptr); st != PKV_OK) return st;
+  pkv::PrefillParams p{};
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.context_lens = context_lens;
+  p.query_start = query_start;
+  p.out = out;
+  p.err = err;
+  p.num_blocks = num_blocks;
+  p.num_seqs = num_seqs;
+  p.num_q_heads = num_q_heads;
+  p.num_kv_heads = num_kv_heads;
+  p.max_blocks_per_seq = max_blocks_per_seq;
+  p.scale = scale;
+  const cudaError_t e = pkv::launch_paged_prefill(p, head_dim, num_q_heads / num_kv_heads, max_query_len,
+                                                  reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "prefill kernel launch");
+  g_launches.fetch_add(1);
+  return ok();
+}
+
 pkv_status pkv_decode_default_partitions(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                          int32_t head_dim, int32_t max_blocks_per_seq, int32_t* num_partitions) {
   if (!num_partitions) return fail(PKV_ERR_INVALID_ARGUMENT, "num_partitions is null");

@@ -1,0 +1,559 @@
+// Chunked paged prefill attention on the 5th-generation tensor cores (sm_103a).
+//
+// What is computed ("从零实现一个 mini vLLM--开篇", section 2: prefill runs the
+// prompt at once and keeps every layer's K and V; section 5: chunked prefill;
+// section 5, phases 4-5: K and V are found through the block table): for each
+// sequence b, C_b new tokens follow P_b cached ones (context_lens[b] = P_b + C_b,
+// the chunk already appended); query row i of the chunk attends causally over
+// the first P_b + i + 1 tokens: out = softmax(scale * q K^T) V.
+//
+// How (GB300-first).  One CTA per (128-row query tile, kv head, sequence).  The
+// 128 MMA rows pack 128/G chunk tokens x the G q heads of the group, so every K/V
+// tile serves the whole group.  Keys advance 64 at a time (4 pages of 16).
+//   * warp 4 (one lane): TMA producer.  Each page half (16 tokens x 64 dims) is a
+//     2D tensor-map copy with 128-byte swizzle, gathered through the block table
+//     into a 2-stage K/V ring; mbarrier completion by transaction bytes.
+//   * warp 5 (one lane): MMA issuer.  tcgen05.mma kind::f16 (bf16 in, fp32
+//     accumulate): S = Q K^T into one of two TMEM buffers (M 128, N 64), then
+//     O += P V into TMEM (M 128, N 64 per 64-dim half of V), commits to mbarriers.
+//     The warp also allocates and frees the TMEM columns.
+//   * warps 0-3 (128 threads, one row each, the TMEM lanes they may address):
+//     stage Q, then per key step read S (tcgen05.ld), apply the causal and length
+//     mask, run the online softmax in base 2 (lazy rescale: O is rescaled only
+//     when a row's max grows by more than 2^8), write P as bf16 to shared memory;
+//     finally read O, divide by the row sum and store bf16 rows.
+// Every mbarrier wait is bounded by a time limit; a wait that runs out sets
+// PKV_DEVERR_PIPELINE_TIMEOUT, the warps finish their loops and the TMEM is
+// freed before the CTA exits.
+#include <cuda.h>  // CUtensorMap and its enums (the encoder is fetched at run time)
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+
+#include "pkv_internal.h"
+
+namespace pkv {
+namespace {
+
+constexpr int kRows = 128;    // MMA M: query rows (chunk tokens x group heads)
+constexpr int kKeys = 64;     // keys per step (MMA N of S, MMA K of P.V)
+constexpr int kStages = 2;    // K/V ring depth
+constexpr int kThreads = 192; // warps 0-3 softmax, 4 producer, 5 MMA
+constexpr int kTmemCols = 256;
+constexpr int kColS = 0;      // S buffers at columns [0, 64) and [64, 128)
+constexpr int kColO = 128;    // O at columns [128, 128 + D)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kSlack = 8.0f;
+constexpr unsigned long long kWaitNs = 2000000000ull;
+
+template <int D>
+struct Pf {
+  static constexpr int kHalves = D / 64;           // 128-byte swizzle atoms across a row
+  static constexpr int kQHalf = kRows * 128;       // 16 KB: 128 rows x 64 dims
+  static constexpr int kKVHalf = kKeys * 128;      // 8 KB: 64 keys x 64 dims
+  static constexpr int kTile = kHalves * kKVHalf;  // one K (or V) tile of a step
+  static constexpr int kStageBytes = 2 * kTile;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffKV = kOffQ + kHalves * kQHalf;
+  static constexpr int kOffP = kOffKV + kStages * kStageBytes;
+  static constexpr int kOffBar = kOffP + kRows * kKeys * 2;
+  static constexpr int kRaw = kOffBar + 128 + 1024;  // barriers + TMEM slot, alignment slack
+  // At least 80 KB so that no more than two CTAs share an SM: each holds 256 of
+  // the SM's 512 TMEM columns, and a third CTA's allocation would have to wait.
+  static constexpr int kSmem = kRaw > 80 * 1024 ? kRaw : 80 * 1024;
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t saddr(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+__device__ __forceinline__ void bar_init(uint32_t b, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(b), "r"(n) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(uint32_t b) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(b) : "memory");
+}
+__device__ __forceinline__ void bar_expect_tx(uint32_t b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(b), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool bar_try(uint32_t b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(b), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ unsigned long long now_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait; false if the phase did not complete in time.
+__device__ __forceinline__ bool bar_wait(uint32_t b, uint32_t parity) {
+  if (bar_try(b, parity)) return true;
+  const unsigned long long t0 = now_ns();
+  for (uint32_t it = 1; it < (1u << 30); ++it) {
+    if (bar_try(b, parity)) return true;
+    if ((it & 63u) == 0 && now_ns() - t0 > kWaitNs) return false;
+  }
+  return false;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t b) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(b)
+      : "memory");
+}
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void tc_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor: 128-byte swizzle with 8-row groups 1024 bytes
+// apart.  Every operand here is one swizzle atom (64 elements) wide across, so
+// the only stride the MMA walks is the one between 8-row groups; both offset
+// fields carry it.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr) {
+  uint64_t d = (addr & 0x3FFFFu) >> 4;
+  d |= uint64_t(1024 >> 4) << 16;    // leading byte offset
+  d |= uint64_t(1024 >> 4) << 32;    // stride byte offset: 8 rows x 128 B
+  d |= uint64_t(1) << 46;            // descriptor version
+  d |= uint64_t(2) << 61;            // 128-byte swizzle
+  return d;
+}
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M 128, N 64.
+__host__ __device__ constexpr uint32_t idesc_bf16(bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) | ((64u >> 3) << 17) |
+         ((128u >> 4) << 24);
+}
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
+__device__ __forceinline__ void mma_commit(uint32_t b) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(b) : "memory");
+}
+// 32 lanes x 32 columns of 32-bit values: this thread's row, 32 consecutive columns.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])), "r"(__float_as_uint(v[3])),
+      "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])), "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])),
+      "r"(__float_as_uint(v[8])), "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])),
+      "r"(__float_as_uint(v[11])), "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])),
+      "r"(__float_as_uint(v[14])), "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])),
+      "r"(__float_as_uint(v[17])), "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])),
+      "r"(__float_as_uint(v[20])), "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])),
+      "r"(__float_as_uint(v[23])), "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])),
+      "r"(__float_as_uint(v[26])), "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])),
+      "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+// Byte offset of 16-byte chunk `chunk` (0..7) of row `r` in a 128-byte-swizzled
+// region of 128-byte rows (the layout the TMA writes and the MMA reads).
+__device__ __forceinline__ uint32_t swz(int r, int chunk) {
+  return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((chunk ^ (r & 7)) << 4));
+}
+
+// ---------------------------------------------------------------------------
+// The kernel
+// ---------------------------------------------------------------------------
+template <int D, int G>
+__global__ void __launch_bounds__(kThreads, 2)
+    paged_prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap map_k,
+                         const __grid_constant__ CUtensorMap map_v) {
+  using T = Pf<D>;
+  constexpr int kTokens = kRows / G;  // chunk tokens per tile
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char* smem =
+      smem_raw + ((1024u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 1023u)) & 1023u);
+  const uint32_t s_base = saddr(smem);
+
+  const int tile = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);  // longest tiles first
+  const int kvh = blockIdx.y;
+  const int b = blockIdx.z;
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5;
+  const int lane = tid & 31;
+
+  const int q0 = p.query_start[b];
+  const int C = p.query_start[b + 1] - q0;
+  int L = p.context_lens[b];
+  const int cap = p.max_blocks_per_seq * kBlockTokens;
+  if (C < 0 || L < C || L > cap) {
+    if (tid == 0 && tile == 0) atomicOr(p.err, kErrLenTooLong);
+    return;
+  }
+  if (tile == 0 && C > static_cast<int>(gridDim.x) * kTokens && tid == 0) atomicOr(p.err, kErrLenTooLong);
+  const int i0 = tile * kTokens;  // first chunk token of the tile
+  if (i0 >= C) return;            // uniform for the CTA: nothing allocated yet
+  const int prefix = L - C;
+  const int i_last = min(C, i0 + kTokens) - 1;
+  const int kv_end = prefix + i_last + 1;            // keys the tile's last row sees
+  const int nsteps = (kv_end + kKeys - 1) / kKeys;
+
+  const uint32_t bar = s_base + T::kOffBar;
+  const uint32_t kv_full = bar, kv_empty = bar + 16, s_full = bar + 32, p_full = bar + 48, pv_done = bar + 56,
+                 o_full = bar + 64, q_ready = bar + 72, mma_drained = bar + 80;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::kOffBar + 96);
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      bar_init(kv_full + 8 * s, 1);
+      bar_init(kv_empty + 8 * s, 1);
+      bar_init(s_full + 8 * s, 1);
+    }
+    bar_init(p_full, 128);
+    bar_init(pv_done, 1);
+    bar_init(o_full, 1);
+    bar_init(q_ready, 128);
+    bar_init(mma_drained, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 5) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_before_sync();
+  __syncthreads();
+  tc_after_sync();
+  const uint32_t tmem = *tmem_slot;
+  bool failed = false;
+
+  if (warp == 4) {
+    // ---------------- TMA producer ----------------
+    if (lane == 0) {
+      int issued = 0;
+      for (int j = 0; j < nsteps && !failed; ++j) {
+        const int s = j % kStages;
+        if (j >= kStages && !bar_wait(kv_empty + 8 * s, ((j / kStages) + 1) & 1)) {
+          failed = true;
+          break;
+        }
+        const uint32_t st = s_base + T::kOffKV + s * T::kStageBytes;
+        int pages = 0;
+        for (int pg = 0; pg < kKeys / kBlockTokens; ++pg)
+          if ((j * kKeys + pg * kBlockTokens) < kv_end) ++pages;
+        bar_expect_tx(kv_full + 8 * s, static_cast<uint32_t>(pages * 2 * T::kHalves * kBlockTokens * 128));
+        for (int pg = 0; pg < pages; ++pg) {
+          const int lp = (j * kKeys) / kBlockTokens + pg;
+          int id = __ldg(p.block_tables + static_cast<size_t>(b) * p.max_blocks_per_seq + lp);
+          if (id < 0 || id >= p.num_blocks) {
+            atomicOr(p.err, kErrBlockId);
+            id = 0;
+          }
+          const int row = (id * p.num_kv_heads + kvh) * kBlockTokens;
+          for (int h = 0; h < T::kHalves; ++h) {
+            const uint32_t off = h * T::kKVHalf + pg * (kBlockTokens * 128);
+            tma_load_2d(st + off, &map_k, 64 * h, row, kv_full + 8 * s);
+            tma_load_2d(st + T::kTile + off, &map_v, 64 * h, row, kv_full + 8 * s);
+          }
+        }
+        issued = j + 1;
+      }
+      if (failed) {  // let the copies still in flight land before the CTA exits
+        atomicOr(p.err, kErrTimeout);
+        for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
+          bar_wait(kv_full + 8 * (j % kStages), (j / kStages) & 1);
+      }
+    }
+  } else if (warp == 5) {
+    // ---------------- MMA issuer ----------------
+    constexpr uint32_t kIdS = idesc_bf16(false);
+    constexpr uint32_t kIdPV = idesc_bf16(true);
+    if (!bar_wait(q_ready, 0)) failed = true;
+    tc_after_sync();
+    for (int j = 0; j <= nsteps && !failed; ++j) {
+      if (j < nsteps) {
+        const int s = j % kStages;
+        if (!bar_wait(kv_full + 8 * s, (j / kStages) & 1)) {
+          failed = true;
+          break;
+        }
+        const uint32_t st = s_base + T::kOffKV + s * T::kStageBytes;
+        if (j == nsteps - 1 && kv_end < (j + 1) * kKeys) {
+          // Keys past the tile's end: zero their V rows (stale or NaN data must not meet p = 0).
+          const int first = kv_end - j * kKeys;
+          for (int idx = lane; idx < (kKeys - first) * T::kHalves * 8; idx += 32) {
+            const int r = first + idx / (T::kHalves * 8);
+            const int rem = idx % (T::kHalves * 8);
+            const int h = rem / 8, ch = rem % 8;
+            *reinterpret_cast<uint4*>(smem + T::kOffKV + s * T::kStageBytes + T::kTile + h * T::kKVHalf +
+                                      swz(r, ch)) = make_uint4(0u, 0u, 0u, 0u);
+          }
+          fence_async_smem();
+          __syncwarp();
+        }
+        if (lane == 0) {
+          tc_after_sync();
+          const uint32_t d = tmem + kColS + (j & 1) * kKeys;
+#pragma unroll
+          for (int h = 0; h < T::kHalves; ++h)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16(d, sdesc(s_base + T::kOffQ + h * T::kQHalf + kk * 32), sdesc(st + h * T::kKVHalf + kk * 32),
+                       kIdS, (h | kk) != 0);
+          mma_commit(s_full + 8 * (j & 1));
+        }
+        __syncwarp();
+      }
+      if (j >= 1) {
+        const int jp = j - 1;  // P of step jp is ready once the softmax warps arrive
+        if (!bar_wait(p_full, jp & 1)) {
+          failed = true;
+          break;
+        }
+        if (lane == 0) {
+          tc_after_sync();
+          const uint32_t st = s_base + T::kOffKV + (jp % kStages) * T::kStageBytes + T::kTile;
+#pragma unroll
+          for (int h = 0; h < T::kHalves; ++h)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16(tmem + kColO + 64 * h, sdesc(s_base + T::kOffP + kk * 32),
+                       sdesc(st + h * T::kKVHalf + kk * 16 * 128), kIdPV, (jp | kk) != 0);
+          mma_commit(kv_empty + 8 * (jp % kStages));
+          mma_commit(pv_done);
+          if (jp == nsteps - 1) mma_commit(o_full);
+        }
+        __syncwarp();
+      }
+    }
+    if (failed && lane == 0) atomicOr(p.err, kErrTimeout);
+    // Every MMA this warp issued must have completed before the TMEM is freed.
+    if (lane == 0) {
+      mma_commit(mma_drained);
+      bar_wait(mma_drained, 0);
+    }
+    __syncwarp();
+  } else {
+    // ---------------- softmax / epilogue (warps 0-3, thread = row) ----------------
+    const int r = tid;
+    const int i = i0 + r / G;  // chunk token of this row
+    const int g = r % G;
+    const bool row_ok = i < C;
+    // Stage Q rows (zero rows past the chunk) in the swizzled K-major layout.
+    {
+      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
+                                                        (static_cast<size_t>(q0 + (row_ok ? i : 0)) * p.num_q_heads +
+                                                         kvh * G + g) * D);
+#pragma unroll
+      for (int h = 0; h < T::kHalves; ++h)
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch) {
+          const uint4 v = row_ok ? __ldg(src + h * 8 + ch) : make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(smem + T::kOffQ + h * T::kQHalf + swz(r, ch)) = v;
+        }
+      fence_async_smem();
+      bar_arrive(q_ready);
+    }
+    const float qk = p.scale * kLog2e;
+    const int limit = row_ok ? prefix + i + 1 : 0;  // keys this row may see
+    float m_used = -INFINITY, l = 0.f;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    for (int j = 0; j < nsteps && !failed; ++j) {
+      if (!__all_sync(0xffffffffu, bar_wait(s_full + 8 * (j & 1), (j >> 1) & 1))) {
+        failed = true;
+        break;
+      }
+      tc_after_sync();
+      float s[kKeys];
+      {
+        float a[32], c2[32];
+        tmem_ld32(lane_base + kColS + (j & 1) * kKeys, a);
+        tmem_ld32(lane_base + kColS + (j & 1) * kKeys + 32, c2);
+#pragma unroll
+        for (int x = 0; x < 32; ++x) {
+          s[x] = a[x];
+          s[32 + x] = c2[x];
+        }
+      }
+      float bm = -INFINITY;
+#pragma unroll
+      for (int x = 0; x < kKeys; ++x) {
+        const int key = j * kKeys + x;
+        s[x] = key < limit ? s[x] * qk : -INFINITY;
+        bm = fmaxf(bm, s[x]);
+      }
+      const bool raise = bm > m_used + kSlack;
+      const float m_new = raise ? bm : m_used;
+      const float alpha = raise ? exp2f(m_used - m_new) : 1.f;  // 0 on the first raise
+      float psum = 0.f;
+      uint32_t packed[kKeys / 2];
+#pragma unroll
+      for (int x = 0; x < kKeys; x += 2) {
+        const float p0 = row_ok ? exp2f(s[x] - m_new) : 0.f;
+        const float p1 = row_ok ? exp2f(s[x + 1] - m_new) : 0.f;
+        packed[x / 2] = pack_bf16(p0, p1);
+        // The denominator sums the same bf16 values the MMA multiplies.
+        psum += __uint_as_float(packed[x / 2] << 16) + __uint_as_float(packed[x / 2] & 0xffff0000u);
+      }
+      l = l * alpha + psum;
+      m_used = m_new;
+      // P of the previous step must be consumed (and O updated) before P and O change.
+      if (j >= 1 && !__all_sync(0xffffffffu, bar_wait(pv_done, (j - 1) & 1))) {
+        failed = true;
+        break;
+      }
+      tc_after_sync();
+      if (j >= 1 && __any_sync(0xffffffffu, raise)) {
+#pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float o[32];
+          tmem_ld32(lane_base + kColO + c0, o);
+#pragma unroll
+          for (int x = 0; x < 32; ++x) o[x] *= alpha;
+          tmem_st32(lane_base + kColO + c0, o);
+        }
+      }
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch)
+        *reinterpret_cast<uint4*>(smem + T::kOffP + swz(r, ch)) =
+            make_uint4(packed[4 * ch], packed[4 * ch + 1], packed[4 * ch + 2], packed[4 * ch + 3]);
+      fence_async_smem();
+      tc_before_sync();
+      bar_arrive(p_full);
+    }
+    // Epilogue: O / l, bf16, one 2*D-byte row per thread.
+    if (!failed && __all_sync(0xffffffffu, bar_wait(o_full, 0))) {
+      tc_after_sync();
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
+                                            (static_cast<size_t>(q0 + i) * p.num_q_heads + kvh * G + g) * D);
+#pragma unroll
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        float o[32];
+        tmem_ld32(lane_base + kColO + c0, o);
+        if (row_ok) {
+#pragma unroll
+          for (int x = 0; x < 32; x += 8)
+            dst[(c0 + x) / 8] = make_uint4(pack_bf16(o[x] * inv, o[x + 1] * inv), pack_bf16(o[x + 2] * inv, o[x + 3] * inv),
+                                           pack_bf16(o[x + 4] * inv, o[x + 5] * inv),
+                                           pack_bf16(o[x + 6] * inv, o[x + 7] * inv));
+        }
+      }
+    } else {
+      failed = true;
+    }
+    if (failed && lane == 0) atomicOr(p.err, kErrTimeout);
+  }
+
+  // Everyone done with TMEM (the MMA warp's last commit arrived before o_full).
+  tc_before_sync();
+  __syncthreads();
+  if (warp == 5) {
+    tc_after_sync();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+cudaError_t encoder(EncodeTiled* out) {
+  static std::mutex mu;
+  static EncodeTiled fn = nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q);
+    if (e != cudaSuccess) return e;
+    if (q != cudaDriverEntryPointSuccess || !ptr) return cudaErrorNotSupported;
+    fn = reinterpret_cast<EncodeTiled>(ptr);
+  }
+  *out = fn;
+  return cudaSuccess;
+}
+
+// The cache viewed as [num_blocks * num_kv_heads * 16 rows][head_dim] bf16; box 16 rows x 64 dims.
+cudaError_t cache_map(CUtensorMap* map, const void* cache, int64_t rows, int head_dim) {
+  EncodeTiled enc = nullptr;
+  cudaError_t e = encoder(&enc);
+  if (e != cudaSuccess) return e;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(kBlockTokens)};
+  const cuuint32_t elem[2] = {1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(cache), dims, strides, box, elem,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int D, int G>
+cudaError_t launch_t(const PrefillParams& p, int max_query_len, cudaStream_t stream) {
+  constexpr int kTokens = kRows / G;
+  static std::mutex mu;
+  static uint64_t ready = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    if (!(dev < 64 && ((ready >> dev) & 1u))) {
+      e = cudaFuncSetAttribute(&paged_prefill_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, Pf<D>::kSmem);
+      if (e != cudaSuccess) return e;
+      if (dev < 64) ready |= uint64_t{1} << dev;
+    }
+  }
+  CUtensorMap mk, mv;
+  const int64_t rows = p.num_blocks * p.num_kv_heads * kBlockTokens;
+  if ((e = cache_map(&mk, p.k_cache, rows, D)) != cudaSuccess) return e;
+  if ((e = cache_map(&mv, p.v_cache, rows, D)) != cudaSuccess) return e;
+  const dim3 grid((max_query_len + kTokens - 1) / kTokens, p.num_kv_heads, p.num_seqs);
+  paged_prefill_kernel<D, G><<<grid, kThreads, Pf<D>::kSmem, stream>>>(p, mk, mv);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_paged_prefill(const PrefillParams& p, int head_dim, int group, int max_query_len,
+                                 cudaStream_t stream) {
+  switch (head_dim * 16 + group) {
+    case 64 * 16 + 1: return launch_t<64, 1>(p, max_query_len, stream);
+    case 64 * 16 + 2: return launch_t<64, 2>(p, max_query_len, stream);
+    case 64 * 16 + 4: return launch_t<64, 4>(p, max_query_len, stream);
+    case 64 * 16 + 8: return launch_t<64, 8>(p, max_query_len, stream);
+    case 128 * 16 + 1: return launch_t<128, 1>(p, max_query_len, stream);
+    case 128 * 16 + 2: return launch_t<128, 2>(p, max_query_len, stream);
+    case 128 * 16 + 4: return launch_t<128, 4>(p, max_query_len, stream);
+    case 128 * 16 + 8: return launch_t<128, 8>(p, max_query_len, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace pkv

@@ -70,6 +70,27 @@ struct CopyParams {
 // copy_blocks kernel launch (one CTA per pair and K/V).
 cudaError_t launch_copy_blocks(const CopyParams& p, int num_pairs, cudaStream_t stream);
 
+struct PrefillParams {
+  const void* q;               // bf16 [T][num_q_heads][head_dim]
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;  // prefix + chunk
+  const int32_t* query_start;   // [num_seqs + 1]
+  void* out;                    // bf16 [T][num_q_heads][head_dim]
+  unsigned* err;
+  int64_t num_blocks;
+  int num_seqs;
+  int num_q_heads;
+  int num_kv_heads;
+  int max_blocks_per_seq;
+  float scale;
+};
+
+// Chunked prefill attention (tensor cores); grid covers max_query_len rows per sequence.
+cudaError_t launch_paged_prefill(const PrefillParams& p, int head_dim, int group, int max_query_len,
+                                 cudaStream_t stream);
+
 // Set the per-host-thread message returned by pkv_last_error_message().
 void set_error_message(const char* message);
 

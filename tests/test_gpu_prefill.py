@@ -1,0 +1,94 @@
+"""Chunked paged prefill on the tensor cores against the fp64 oracle (every output element).
+
+Tolerance as for decode: max |gpu - oracle| <= 1e-2, relative RMS <= 5e-3.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_275_gb300 as pkv
+from gpu_util import assert_close, device_errors
+from workloads import BLOCK_SIZE, PrefillSpec, make_prefill_case
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(c):
+    g = c.to("cuda")
+    pkv.kv_append(g.new_k, g.new_v, g.slot_mapping, g.k_cache, g.v_cache)
+    out = torch.full_like(g.q, float("nan"))
+    max_q = int(max(c.spec.chunk_lens))
+    pkv.paged_prefill_attention(g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens, g.query_start, max_q,
+                                g.scale, out)
+    torch.cuda.synchronize()
+    return g, out
+
+
+def _ref(c):
+    kc, vc = c.k_cache.clone(), c.v_cache.clone()
+    assert oracle.kv_append(c.new_k, c.new_v, c.slot_mapping, kc, vc) == oracle.OK
+    ref, st = oracle.paged_prefill_attention(c.q, kc, vc, c.block_tables, c.context_lens, c.query_start, c.scale)
+    assert st == oracle.OK
+    return ref
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_prefill_tiny(seed):
+    c = make_prefill_case("prefill_tiny", seed=seed)
+    _, out = _run(c)
+    assert_close(out, _ref(c), f"prefill_tiny seed {seed}")
+    assert device_errors() == 0
+
+
+@pytest.mark.parametrize("head_dim,hq,hkv", [(128, 8, 8), (128, 16, 8), (128, 32, 8), (128, 32, 4), (64, 4, 4),
+                                             (64, 16, 4)])
+def test_prefill_every_layout_ragged(head_dim, hq, hkv):
+    spec = PrefillSpec("ragged", "", hq, hkv, head_dim, (1, 7, 37, 130, 16), (0, 0), 60)
+    c = make_prefill_case(spec, seed=5, prefixes=[0, 3, 100, 500, 64])
+    _, out = _run(c)
+    assert_close(out, _ref(c), f"D{head_dim} {hq}/{hkv}")
+    assert device_errors() == 0
+
+
+def test_prefill_qwen3_chunks():
+    c = make_prefill_case("prefill_qwen3_0.6b", seed=0)
+    _, out = _run(c)
+    assert_close(out, _ref(c), "prefill_qwen3_0.6b")
+    assert device_errors() == 0
+
+
+def test_prefill_llama3_chunks():
+    c = make_prefill_case("prefill_llama3_8b", seed=0)
+    _, out = _run(c)
+    assert_close(out, _ref(c), "prefill_llama3_8b")
+    assert device_errors() == 0
+
+
+def test_prefill_chunks_of_one_match_decode():
+    spec = PrefillSpec("ones", "", 32, 8, 128, (1,) * 6, (0, 300), 30)
+    c = make_prefill_case(spec, seed=7)
+    g, out = _run(c)
+    dec = torch.empty_like(g.q)
+    pkv.paged_decode_attention(g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens, g.scale, dec)
+    ref = _ref(c)
+    assert_close(out, ref, "chunks of one")
+    assert_close(dec, ref, "decode on the same rows")
+
+
+def test_prefill_poisoned_unused_slots_do_not_leak():
+    c = make_prefill_case("prefill_tiny", seed=8)
+    _, clean = _run(c)
+    lens = c.context_lens.tolist()
+    used = torch.zeros(c.k_cache.shape[0] * BLOCK_SIZE, dtype=torch.bool)
+    for b, L in enumerate(lens):
+        for t in range(L):
+            used[int(c.block_tables[b, t // BLOCK_SIZE]) * BLOCK_SIZE + t % BLOCK_SIZE] = True
+    unused = (~used).view(c.k_cache.shape[0], BLOCK_SIZE)
+    nan = torch.tensor(float("nan"), dtype=torch.bfloat16)
+    c.k_cache.permute(0, 2, 1, 3)[unused] = nan
+    c.v_cache.permute(0, 2, 1, 3)[unused] = nan
+    _, out = _run(c)
+    assert torch.isfinite(out.float()).all()
+    assert torch.equal(out, clean)
+    assert device_errors() == 0
