@@ -57,9 +57,14 @@ struct Pf {
   static constexpr int kStageBytes = 2 * kTile;
   static constexpr int kOffQ = 0;
   static constexpr int kOffKV = kOffQ + kHalves * kQHalf;
+  // At D = 128 a step's K tile (64 keys x 128 dims) is exactly the size of its P
+  // tile (128 rows x 64 keys): once S = Q K^T has retired, P is written over it,
+  // which keeps two CTAs per SM.  At D = 64 P has a buffer of its own.
+  static constexpr bool kPInK = (kTile == kRows * kKeys * 2);
   static constexpr int kOffP = kOffKV + kStages * kStageBytes;
-  static constexpr int kOffBar = kOffP + kRows * kKeys * 2;
-  static constexpr int kRaw = kOffBar + 128 + 1024;  // barriers + TMEM slot, alignment slack
+  static constexpr int kOffBar = kOffP + (kPInK ? 0 : kRows * kKeys * 2);
+  __host__ __device__ static constexpr int p_offset(int stage) { return kPInK ? kOffKV + stage * kStageBytes : kOffP; }
+  static constexpr int kRaw = kOffBar + 256 + 1024;  // barriers + TMEM slot, alignment slack
   // At least 80 KB so that no more than two CTAs share an SM: each holds 256 of
   // the SM's 512 TMEM columns, and a third CTA's allocation would have to wait.
   static constexpr int kSmem = kRaw > 80 * 1024 ? kRaw : 80 * 1024;
@@ -219,15 +224,21 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int kv_end = prefix + i_last + 1;            // keys the tile's last row sees
   const int nsteps = (kv_end + kKeys - 1) / kKeys;
 
+  // Separate K and V rings over the same stage memory: a K slot frees when its
+  // S = Q K^T retires, a V slot when its O += P V retires, so each stream is
+  // fetched about two steps ahead of its use.
   const uint32_t bar = s_base + T::kOffBar;
-  const uint32_t kv_full = bar, kv_empty = bar + 16, s_full = bar + 32, p_full = bar + 48, pv_done = bar + 56,
-                 o_full = bar + 64, q_ready = bar + 72, mma_drained = bar + 80;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::kOffBar + 96);
+  const uint32_t k_full = bar, k_empty = bar + 16, v_full = bar + 32, v_empty = bar + 48, s_full = bar + 64,
+                 p_full = bar + 80, pv_done = bar + 88, o_full = bar + 96, q_ready = bar + 104,
+                 mma_drained = bar + 112;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::kOffBar + 128);
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
-      bar_init(kv_full + 8 * s, 1);
-      bar_init(kv_empty + 8 * s, 1);
+      bar_init(k_full + 8 * s, 1);
+      bar_init(k_empty + 8 * s, 1);
+      bar_init(v_full + 8 * s, 1);
+      bar_init(v_empty + 8 * s, 1);
       bar_init(s_full + 8 * s, 1);
     }
     bar_init(p_full, 128);
@@ -250,42 +261,88 @@ __global__ void __launch_bounds__(kThreads, 2)
   bool failed = false;
 
   if (warp == 4) {
-    // ---------------- TMA producer ----------------
-    if (lane == 0) {
-      int issued = 0;
-      for (int j = 0; j < nsteps && !failed; ++j) {
+    // ---------------- TMA producer (whole warp; lane 0 issues) ----------------
+    // Block ids come from a 32-page window held one per lane, with the next
+    // window already in flight, so no copy waits on a dependent table load.
+    constexpr int kPages = kKeys / kBlockTokens;  // pages per step
+    const int npages = (kv_end + kBlockTokens - 1) / kBlockTokens;
+    const int32_t* table = p.block_tables + static_cast<size_t>(b) * p.max_blocks_per_seq;
+    auto fetch = [&](int page) -> int {
+      if (page >= npages) return 0;
+      const int id = __ldg(table + page);
+      if (id < 0 || id >= p.num_blocks) {
+        atomicOr(p.err, kErrBlockId);
+        return 0;
+      }
+      return id;
+    };
+    int win = 0;
+    int id_cur = fetch(lane), id_next = fetch(32 + lane);
+    int prev_ids[kPages];
+    int issued_k = 0, issued_v = 0;
+    auto issue = [&](int j, const int (&ids)[kPages], uint32_t dst, const CUtensorMap* map, uint32_t full) {
+      int pages = 0;
+#pragma unroll
+      for (int pg = 0; pg < kPages; ++pg)
+        if ((j * kKeys + pg * kBlockTokens) < kv_end) ++pages;
+      if (lane == 0) {
+        bar_expect_tx(full, static_cast<uint32_t>(pages * T::kHalves * kBlockTokens * 128));
+        for (int pg = 0; pg < pages; ++pg) {
+          const int row = (ids[pg] * p.num_kv_heads + kvh) * kBlockTokens;
+          for (int h = 0; h < T::kHalves; ++h)
+            tma_load_2d(dst + h * T::kKVHalf + pg * (kBlockTokens * 128), map, 64 * h, row, full);
+        }
+      }
+    };
+    for (int j = 0; j <= nsteps && !failed; ++j) {
+      if (j < nsteps) {  // K of step j
         const int s = j % kStages;
-        if (j >= kStages && !bar_wait(kv_empty + 8 * s, ((j / kStages) + 1) & 1)) {
+        if (j >= kStages && !__all_sync(0xffffffffu, bar_wait(k_empty + 8 * s, ((j / kStages) + 1) & 1))) {
           failed = true;
           break;
         }
-        const uint32_t st = s_base + T::kOffKV + s * T::kStageBytes;
-        int pages = 0;
-        for (int pg = 0; pg < kKeys / kBlockTokens; ++pg)
-          if ((j * kKeys + pg * kBlockTokens) < kv_end) ++pages;
-        bar_expect_tx(kv_full + 8 * s, static_cast<uint32_t>(pages * 2 * T::kHalves * kBlockTokens * 128));
-        for (int pg = 0; pg < pages; ++pg) {
-          const int lp = (j * kKeys) / kBlockTokens + pg;
-          int id = __ldg(p.block_tables + static_cast<size_t>(b) * p.max_blocks_per_seq + lp);
-          if (id < 0 || id >= p.num_blocks) {
-            atomicOr(p.err, kErrBlockId);
-            id = 0;
+        int ids[kPages];
+#pragma unroll
+        for (int pg = 0; pg < kPages; ++pg) {
+          const int page = j * kPages + pg;
+          if (page / 32 != win) {  // slide the window
+            ++win;
+            id_cur = id_next;
+            id_next = fetch(32 * (win + 1) + lane);
           }
-          const int row = (id * p.num_kv_heads + kvh) * kBlockTokens;
-          for (int h = 0; h < T::kHalves; ++h) {
-            const uint32_t off = h * T::kKVHalf + pg * (kBlockTokens * 128);
-            tma_load_2d(st + off, &map_k, 64 * h, row, kv_full + 8 * s);
-            tma_load_2d(st + T::kTile + off, &map_v, 64 * h, row, kv_full + 8 * s);
-          }
+          ids[pg] = __shfl_sync(0xffffffffu, id_cur, page % 32);
         }
-        issued = j + 1;
-      }
-      if (failed) {  // let the copies still in flight land before the CTA exits
-        atomicOr(p.err, kErrTimeout);
-        for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
-          bar_wait(kv_full + 8 * (j % kStages), (j / kStages) & 1);
+        issue(j, ids, s_base + T::kOffKV + s * T::kStageBytes, &map_k, k_full + 8 * s);
+        issued_k = j + 1;
+        if (j >= 1) {  // V of step j - 1 uses the ids its K used
+          const int jv = j - 1, sv = jv % kStages;
+          if (jv >= kStages && !__all_sync(0xffffffffu, bar_wait(v_empty + 8 * sv, ((jv / kStages) + 1) & 1))) {
+            failed = true;
+            break;
+          }
+          issue(jv, prev_ids, s_base + T::kOffKV + sv * T::kStageBytes + T::kTile, &map_v, v_full + 8 * sv);
+          issued_v = jv + 1;
+        }
+#pragma unroll
+        for (int pg = 0; pg < kPages; ++pg) prev_ids[pg] = ids[pg];
+      } else {  // V of the last step
+        const int jv = j - 1, sv = jv % kStages;
+        if (jv >= kStages && !__all_sync(0xffffffffu, bar_wait(v_empty + 8 * sv, ((jv / kStages) + 1) & 1))) {
+          failed = true;
+          break;
+        }
+        issue(jv, prev_ids, s_base + T::kOffKV + sv * T::kStageBytes + T::kTile, &map_v, v_full + 8 * sv);
+        issued_v = jv + 1;
       }
     }
+    if (failed && lane == 0) {  // let the copies still in flight land before the CTA exits
+      atomicOr(p.err, kErrTimeout);
+      for (int j = issued_k > kStages ? issued_k - kStages : 0; j < issued_k; ++j)
+        bar_wait(k_full + 8 * (j % kStages), (j / kStages) & 1);
+      for (int j = issued_v > kStages ? issued_v - kStages : 0; j < issued_v; ++j)
+        bar_wait(v_full + 8 * (j % kStages), (j / kStages) & 1);
+    }
+    __syncwarp();
   } else if (warp == 5) {
     // ---------------- MMA issuer ----------------
     constexpr uint32_t kIdS = idesc_bf16(false);
@@ -295,53 +352,54 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int j = 0; j <= nsteps && !failed; ++j) {
       if (j < nsteps) {
         const int s = j % kStages;
-        if (!bar_wait(kv_full + 8 * s, (j / kStages) & 1)) {
+        if (!bar_wait(k_full + 8 * s, (j / kStages) & 1)) {
           failed = true;
           break;
         }
-        const uint32_t st = s_base + T::kOffKV + s * T::kStageBytes;
-        if (j == nsteps - 1 && kv_end < (j + 1) * kKeys) {
+        if (lane == 0) {
+          tc_after_sync();
+          const uint32_t kt = s_base + T::kOffKV + s * T::kStageBytes;
+          const uint32_t d = tmem + kColS + (j & 1) * kKeys;
+#pragma unroll
+          for (int h = 0; h < T::kHalves; ++h)
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+              mma_bf16(d, sdesc(s_base + T::kOffQ + h * T::kQHalf + kk * 32), sdesc(kt + h * T::kKVHalf + kk * 32),
+                       kIdS, (h | kk) != 0);
+          if (!T::kPInK) mma_commit(k_empty + 8 * s);  // else the slot holds P until P.V retires
+          mma_commit(s_full + 8 * (j & 1));
+        }
+        __syncwarp();
+      }
+      if (j >= 1) {
+        const int jp = j - 1, s = jp % kStages;  // P of step jp is ready once the softmax warps arrive
+        if (!bar_wait(p_full, jp & 1) || !bar_wait(v_full + 8 * s, (jp / kStages) & 1)) {
+          failed = true;
+          break;
+        }
+        const uint32_t vt_off = T::kOffKV + s * T::kStageBytes + T::kTile;
+        if (jp == nsteps - 1 && kv_end < (jp + 1) * kKeys) {
           // Keys past the tile's end: zero their V rows (stale or NaN data must not meet p = 0).
-          const int first = kv_end - j * kKeys;
+          const int first = kv_end - jp * kKeys;
           for (int idx = lane; idx < (kKeys - first) * T::kHalves * 8; idx += 32) {
             const int r = first + idx / (T::kHalves * 8);
             const int rem = idx % (T::kHalves * 8);
             const int h = rem / 8, ch = rem % 8;
-            *reinterpret_cast<uint4*>(smem + T::kOffKV + s * T::kStageBytes + T::kTile + h * T::kKVHalf +
-                                      swz(r, ch)) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(smem + vt_off + h * T::kKVHalf + swz(r, ch)) = make_uint4(0u, 0u, 0u, 0u);
           }
           fence_async_smem();
           __syncwarp();
         }
         if (lane == 0) {
           tc_after_sync();
-          const uint32_t d = tmem + kColS + (j & 1) * kKeys;
 #pragma unroll
           for (int h = 0; h < T::kHalves; ++h)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_bf16(d, sdesc(s_base + T::kOffQ + h * T::kQHalf + kk * 32), sdesc(st + h * T::kKVHalf + kk * 32),
-                       kIdS, (h | kk) != 0);
-          mma_commit(s_full + 8 * (j & 1));
-        }
-        __syncwarp();
-      }
-      if (j >= 1) {
-        const int jp = j - 1;  // P of step jp is ready once the softmax warps arrive
-        if (!bar_wait(p_full, jp & 1)) {
-          failed = true;
-          break;
-        }
-        if (lane == 0) {
-          tc_after_sync();
-          const uint32_t st = s_base + T::kOffKV + (jp % kStages) * T::kStageBytes + T::kTile;
-#pragma unroll
-          for (int h = 0; h < T::kHalves; ++h)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_bf16(tmem + kColO + 64 * h, sdesc(s_base + T::kOffP + kk * 32),
-                       sdesc(st + h * T::kKVHalf + kk * 16 * 128), kIdPV, (jp | kk) != 0);
-          mma_commit(kv_empty + 8 * (jp % kStages));
+              mma_bf16(tmem + kColO + 64 * h, sdesc(s_base + T::p_offset(s) + kk * 32),
+                       sdesc(s_base + vt_off + h * T::kKVHalf + kk * 16 * 128), kIdPV, (jp | kk) != 0);
+          if (T::kPInK) mma_commit(k_empty + 8 * s);
+          mma_commit(v_empty + 8 * s);
           mma_commit(pv_done);
           if (jp == nsteps - 1) mma_commit(o_full);
         }
@@ -419,13 +477,16 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       l = l * alpha + psum;
       m_used = m_new;
-      // P of the previous step must be consumed (and O updated) before P and O change.
-      if (j >= 1 && !__all_sync(0xffffffffu, bar_wait(pv_done, (j - 1) & 1))) {
+      // O may only be rescaled once the previous P.V has retired; a shared P buffer
+      // (D = 64) may only be rewritten then too.  With P in this step's K slot and
+      // no rescale, the softmax runs alongside the previous P.V.
+      const bool rescale = j >= 1 && __any_sync(0xffffffffu, raise);
+      if ((rescale || (!T::kPInK && j >= 1)) && !__all_sync(0xffffffffu, bar_wait(pv_done, (j - 1) & 1))) {
         failed = true;
         break;
       }
       tc_after_sync();
-      if (j >= 1 && __any_sync(0xffffffffu, raise)) {
+      if (rescale) {
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           float o[32];
@@ -437,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch)
-        *reinterpret_cast<uint4*>(smem + T::kOffP + swz(r, ch)) =
+        *reinterpret_cast<uint4*>(smem + T::p_offset(j % kStages) + swz(r, ch)) =
             make_uint4(packed[4 * ch], packed[4 * ch + 1], packed[4 * ch + 2], packed[4 * ch + 3]);
       fence_async_smem();
       tc_before_sync();
