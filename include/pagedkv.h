@@ -78,6 +78,7 @@ typedef enum pkv_status {
 #define PKV_DEVERR_PIPELINE_TIMEOUT 0x10u     /* attention: a shared-memory pipeline wait gave up (partition skipped) */
 #define PKV_DEVERR_COPY_OUT_OF_RANGE 0x20u    /* copy_blocks: a source or destination block outside the pool (pair skipped) */
 #define PKV_DEVERR_POSITION_OUT_OF_TABLE 0x40u /* decode_step: context_len - 1 >= max_position (last table row used) */
+#define PKV_DEVERR_SMEM_ALIGNMENT 0x80u        /* prefill: dynamic shared memory not 1024-byte aligned (tile skipped) */
 
 /* Largest num_seqs one attention call accepts. */
 #define PKV_MAX_SEQS 4096

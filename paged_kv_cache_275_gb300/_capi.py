@@ -31,6 +31,7 @@ DEVERR_CONTEXT_LEN_TOO_LONG = 0x8
 DEVERR_PIPELINE_TIMEOUT = 0x10
 DEVERR_COPY_OUT_OF_RANGE = 0x20
 DEVERR_POSITION_OUT_OF_TABLE = 0x40
+DEVERR_SMEM_ALIGNMENT = 0x80
 
 PHASE_PARTITION = 1
 PHASE_MERGE = 2

@@ -39,7 +39,8 @@ namespace {
 
 constexpr int kRows = 128;    // MMA M: query rows (chunk tokens x group heads)
 constexpr int kKeys = 64;     // keys per step (MMA N of S, MMA K of P.V)
-constexpr int kStages = 2;    // K/V ring depth
+constexpr int kKStages = 3;   // K ring depth (at D = 128 a K slot also carries its step's P)
+constexpr int kVStages = 2;   // V ring depth
 constexpr int kThreads = 192; // warps 0-3 softmax, 4 producer, 5 MMA
 constexpr int kTmemCols = 256;
 constexpr int kColS = 0;      // S buffers at columns [0, 64) and [64, 128)
@@ -54,17 +55,19 @@ struct Pf {
   static constexpr int kQHalf = kRows * 128;       // 16 KB: 128 rows x 64 dims
   static constexpr int kKVHalf = kKeys * 128;      // 8 KB: 64 keys x 64 dims
   static constexpr int kTile = kHalves * kKVHalf;  // one K (or V) tile of a step
-  static constexpr int kStageBytes = 2 * kTile;
   static constexpr int kOffQ = 0;
-  static constexpr int kOffKV = kOffQ + kHalves * kQHalf;
+  static constexpr int kOffK = kOffQ + kHalves * kQHalf;
+  static constexpr int kOffV = kOffK + kKStages * kTile;
   // At D = 128 a step's K tile (64 keys x 128 dims) is exactly the size of its P
   // tile (128 rows x 64 keys): once S = Q K^T has retired, P is written over it,
   // which keeps two CTAs per SM.  At D = 64 P has a buffer of its own.
   static constexpr bool kPInK = (kTile == kRows * kKeys * 2);
-  static constexpr int kOffP = kOffKV + kStages * kStageBytes;
+  static constexpr int kOffP = kOffV + kVStages * kTile;
   static constexpr int kOffBar = kOffP + (kPInK ? 0 : kRows * kKeys * 2);
-  __host__ __device__ static constexpr int p_offset(int stage) { return kPInK ? kOffKV + stage * kStageBytes : kOffP; }
-  static constexpr int kRaw = kOffBar + 256 + 1024;  // barriers + TMEM slot, alignment slack
+  __host__ __device__ static constexpr int p_offset(int kslot) { return kPInK ? kOffK + kslot * kTile : kOffP; }
+  // The dynamic shared memory is requested 1024-byte aligned (checked at run time),
+  // so no alignment slack: 112.25 KB at D = 128, two CTAs per SM.
+  static constexpr int kRaw = kOffBar + 256;  // barriers + TMEM slot
   // At least 80 KB so that no more than two CTAs share an SM: each holds 256 of
   // the SM's 512 TMEM columns, and a third CTA's allocation would have to wait.
   static constexpr int kSmem = kRaw > 80 * 1024 ? kRaw : 80 * 1024;
@@ -160,6 +163,22 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
+// 32 lanes x 64 columns: this thread's row, 64 consecutive columns.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+// 2^x on the SFU (approximate, flush-to-zero): the softmax weights.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
@@ -196,9 +215,7 @@ __global__ void __launch_bounds__(kThreads, 2)
                          const __grid_constant__ CUtensorMap map_v) {
   using T = Pf<D>;
   constexpr int kTokens = kRows / G;  // chunk tokens per tile
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* smem =
-      smem_raw + ((1024u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 1023u)) & 1023u);
+  extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t s_base = saddr(smem);
 
   const int tile = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);  // longest tiles first
@@ -219,6 +236,10 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (tile == 0 && C > static_cast<int>(gridDim.x) * kTokens && tid == 0) atomicOr(p.err, kErrLenTooLong);
   const int i0 = tile * kTokens;  // first chunk token of the tile
   if (i0 >= C) return;            // uniform for the CTA: nothing allocated yet
+  if (s_base & 1023u) {           // the swizzled operands need 1024-byte alignment
+    if (tid == 0) atomicOr(p.err, kErrSmemAlign);
+    return;
+  }
   const int prefix = L - C;
   const int i_last = min(C, i0 + kTokens) - 1;
   const int kv_end = prefix + i_last + 1;            // keys the tile's last row sees
@@ -228,19 +249,21 @@ __global__ void __launch_bounds__(kThreads, 2)
   // S = Q K^T retires, a V slot when its O += P V retires, so each stream is
   // fetched about two steps ahead of its use.
   const uint32_t bar = s_base + T::kOffBar;
-  const uint32_t k_full = bar, k_empty = bar + 16, v_full = bar + 32, v_empty = bar + 48, s_full = bar + 64,
-                 p_full = bar + 80, pv_done = bar + 88, o_full = bar + 96, q_ready = bar + 104,
-                 mma_drained = bar + 112;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::kOffBar + 128);
+  const uint32_t k_full = bar, k_empty = bar + 24, v_full = bar + 48, v_empty = bar + 64, s_full = bar + 80,
+                 p_full = bar + 96, pv_done = bar + 104, o_full = bar + 112, q_ready = bar + 120,
+                 mma_drained = bar + 128;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::kOffBar + 192);
 
   if (tid == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       bar_init(k_full + 8 * s, 1);
       bar_init(k_empty + 8 * s, 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
       bar_init(v_full + 8 * s, 1);
       bar_init(v_empty + 8 * s, 1);
-      bar_init(s_full + 8 * s, 1);
     }
+    for (int s = 0; s < 2; ++s) bar_init(s_full + 8 * s, 1);
     bar_init(p_full, 128);
     bar_init(pv_done, 1);
     bar_init(o_full, 1);
@@ -296,8 +319,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     };
     for (int j = 0; j <= nsteps && !failed; ++j) {
       if (j < nsteps) {  // K of step j
-        const int s = j % kStages;
-        if (j >= kStages && !__all_sync(0xffffffffu, bar_wait(k_empty + 8 * s, ((j / kStages) + 1) & 1))) {
+        const int s = j % kKStages;
+        if (j >= kKStages && !__all_sync(0xffffffffu, bar_wait(k_empty + 8 * s, ((j / kKStages) + 1) & 1))) {
           failed = true;
           break;
         }
@@ -312,35 +335,35 @@ __global__ void __launch_bounds__(kThreads, 2)
           }
           ids[pg] = __shfl_sync(0xffffffffu, id_cur, page % 32);
         }
-        issue(j, ids, s_base + T::kOffKV + s * T::kStageBytes, &map_k, k_full + 8 * s);
+        issue(j, ids, s_base + T::kOffK + s * T::kTile, &map_k, k_full + 8 * s);
         issued_k = j + 1;
         if (j >= 1) {  // V of step j - 1 uses the ids its K used
-          const int jv = j - 1, sv = jv % kStages;
-          if (jv >= kStages && !__all_sync(0xffffffffu, bar_wait(v_empty + 8 * sv, ((jv / kStages) + 1) & 1))) {
+          const int jv = j - 1, sv = jv % kVStages;
+          if (jv >= kVStages && !__all_sync(0xffffffffu, bar_wait(v_empty + 8 * sv, ((jv / kVStages) + 1) & 1))) {
             failed = true;
             break;
           }
-          issue(jv, prev_ids, s_base + T::kOffKV + sv * T::kStageBytes + T::kTile, &map_v, v_full + 8 * sv);
+          issue(jv, prev_ids, s_base + T::kOffV + sv * T::kTile, &map_v, v_full + 8 * sv);
           issued_v = jv + 1;
         }
 #pragma unroll
         for (int pg = 0; pg < kPages; ++pg) prev_ids[pg] = ids[pg];
       } else {  // V of the last step
-        const int jv = j - 1, sv = jv % kStages;
-        if (jv >= kStages && !__all_sync(0xffffffffu, bar_wait(v_empty + 8 * sv, ((jv / kStages) + 1) & 1))) {
+        const int jv = j - 1, sv = jv % kVStages;
+        if (jv >= kVStages && !__all_sync(0xffffffffu, bar_wait(v_empty + 8 * sv, ((jv / kVStages) + 1) & 1))) {
           failed = true;
           break;
         }
-        issue(jv, prev_ids, s_base + T::kOffKV + sv * T::kStageBytes + T::kTile, &map_v, v_full + 8 * sv);
+        issue(jv, prev_ids, s_base + T::kOffV + sv * T::kTile, &map_v, v_full + 8 * sv);
         issued_v = jv + 1;
       }
     }
     if (failed && lane == 0) {  // let the copies still in flight land before the CTA exits
       atomicOr(p.err, kErrTimeout);
-      for (int j = issued_k > kStages ? issued_k - kStages : 0; j < issued_k; ++j)
-        bar_wait(k_full + 8 * (j % kStages), (j / kStages) & 1);
-      for (int j = issued_v > kStages ? issued_v - kStages : 0; j < issued_v; ++j)
-        bar_wait(v_full + 8 * (j % kStages), (j / kStages) & 1);
+      for (int j = issued_k > kKStages ? issued_k - kKStages : 0; j < issued_k; ++j)
+        bar_wait(k_full + 8 * (j % kKStages), (j / kKStages) & 1);
+      for (int j = issued_v > kVStages ? issued_v - kVStages : 0; j < issued_v; ++j)
+        bar_wait(v_full + 8 * (j % kVStages), (j / kVStages) & 1);
     }
     __syncwarp();
   } else if (warp == 5) {
@@ -351,14 +374,14 @@ __global__ void __launch_bounds__(kThreads, 2)
     tc_after_sync();
     for (int j = 0; j <= nsteps && !failed; ++j) {
       if (j < nsteps) {
-        const int s = j % kStages;
-        if (!bar_wait(k_full + 8 * s, (j / kStages) & 1)) {
+        const int s = j % kKStages;
+        if (!bar_wait(k_full + 8 * s, (j / kKStages) & 1)) {
           failed = true;
           break;
         }
         if (lane == 0) {
           tc_after_sync();
-          const uint32_t kt = s_base + T::kOffKV + s * T::kStageBytes;
+          const uint32_t kt = s_base + T::kOffK + s * T::kTile;
           const uint32_t d = tmem + kColS + (j & 1) * kKeys;
 #pragma unroll
           for (int h = 0; h < T::kHalves; ++h)
@@ -372,12 +395,12 @@ __global__ void __launch_bounds__(kThreads, 2)
         __syncwarp();
       }
       if (j >= 1) {
-        const int jp = j - 1, s = jp % kStages;  // P of step jp is ready once the softmax warps arrive
-        if (!bar_wait(p_full, jp & 1) || !bar_wait(v_full + 8 * s, (jp / kStages) & 1)) {
+        const int jp = j - 1, ks = jp % kKStages, s = jp % kVStages;  // P of step jp ready once softmax arrives
+        if (!bar_wait(p_full, jp & 1) || !bar_wait(v_full + 8 * s, (jp / kVStages) & 1)) {
           failed = true;
           break;
         }
-        const uint32_t vt_off = T::kOffKV + s * T::kStageBytes + T::kTile;
+        const uint32_t vt_off = T::kOffV + s * T::kTile;
         if (jp == nsteps - 1 && kv_end < (jp + 1) * kKeys) {
           // Keys past the tile's end: zero their V rows (stale or NaN data must not meet p = 0).
           const int first = kv_end - jp * kKeys;
@@ -396,9 +419,9 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int h = 0; h < T::kHalves; ++h)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_bf16(tmem + kColO + 64 * h, sdesc(s_base + T::p_offset(s) + kk * 32),
+              mma_bf16(tmem + kColO + 64 * h, sdesc(s_base + T::p_offset(ks) + kk * 32),
                        sdesc(s_base + vt_off + h * T::kKVHalf + kk * 16 * 128), kIdPV, (jp | kk) != 0);
-          if (T::kPInK) mma_commit(k_empty + 8 * s);
+          if (T::kPInK) mma_commit(k_empty + 8 * ks);
           mma_commit(v_empty + 8 * s);
           mma_commit(pv_done);
           if (jp == nsteps - 1) mma_commit(o_full);
@@ -445,37 +468,32 @@ __global__ void __launch_bounds__(kThreads, 2)
       }
       tc_after_sync();
       float s[kKeys];
-      {
-        float a[32], c2[32];
-        tmem_ld32(lane_base + kColS + (j & 1) * kKeys, a);
-        tmem_ld32(lane_base + kColS + (j & 1) * kKeys + 32, c2);
+      tmem_ld64(lane_base + kColS + (j & 1) * kKeys, s);
+      // Causal / length mask, only on steps that some row of the warp does not see whole.
+      if (__any_sync(0xffffffffu, (j + 1) * kKeys > limit)) {
 #pragma unroll
-        for (int x = 0; x < 32; ++x) {
-          s[x] = a[x];
-          s[32 + x] = c2[x];
-        }
+        for (int x = 0; x < kKeys; ++x) s[x] = (j * kKeys + x) < limit ? s[x] : -INFINITY;
       }
-      float bm = -INFINITY;
+      float bm = s[0];
 #pragma unroll
-      for (int x = 0; x < kKeys; ++x) {
-        const int key = j * kKeys + x;
-        s[x] = key < limit ? s[x] * qk : -INFINITY;
-        bm = fmaxf(bm, s[x]);
-      }
-      const bool raise = bm > m_used + kSlack;
+      for (int x = 1; x < kKeys; ++x) bm = fmaxf(bm, s[x]);
+      bm *= qk;  // the scale is positive: the max of the scaled scores
+      const bool raise = row_ok && bm > m_used + kSlack;
       const float m_new = raise ? bm : m_used;
-      const float alpha = raise ? exp2f(m_used - m_new) : 1.f;  // 0 on the first raise
-      float psum = 0.f;
+      const float alpha = raise ? ex2_approx(m_used - m_new) : 1.f;  // 0 on the first raise
+      const float neg_m = row_ok ? -m_new : 0.f;                      // rows past the chunk: all p = 0
+      float2 psum2 = make_float2(0.f, 0.f);
       uint32_t packed[kKeys / 2];
 #pragma unroll
       for (int x = 0; x < kKeys; x += 2) {
-        const float p0 = row_ok ? exp2f(s[x] - m_new) : 0.f;
-        const float p1 = row_ok ? exp2f(s[x + 1] - m_new) : 0.f;
+        const float p0 = ex2_approx(fmaf(s[x], qk, neg_m));
+        const float p1 = ex2_approx(fmaf(s[x + 1], qk, neg_m));
         packed[x / 2] = pack_bf16(p0, p1);
         // The denominator sums the same bf16 values the MMA multiplies.
-        psum += __uint_as_float(packed[x / 2] << 16) + __uint_as_float(packed[x / 2] & 0xffff0000u);
+        psum2 = __fadd2_rn(psum2, make_float2(__uint_as_float(packed[x / 2] << 16),
+                                              __uint_as_float(packed[x / 2] & 0xffff0000u)));
       }
-      l = l * alpha + psum;
+      l = l * alpha + (psum2.x + psum2.y);
       m_used = m_new;
       // O may only be rescaled once the previous P.V has retired; a shared P buffer
       // (D = 64) may only be rewritten then too.  With P in this step's K slot and
@@ -496,9 +514,10 @@ __global__ void __launch_bounds__(kThreads, 2)
           tmem_st32(lane_base + kColO + c0, o);
         }
       }
+      unsigned char* prow = smem + T::p_offset(j % kKStages) + (r >> 3) * 1024 + (r & 7) * 128;
 #pragma unroll
       for (int ch = 0; ch < 8; ++ch)
-        *reinterpret_cast<uint4*>(smem + T::p_offset(j % kStages) + swz(r, ch)) =
+        *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) =
             make_uint4(packed[4 * ch], packed[4 * ch + 1], packed[4 * ch + 2], packed[4 * ch + 3]);
       fence_async_smem();
       tc_before_sync();

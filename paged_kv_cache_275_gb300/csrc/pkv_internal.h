@@ -19,6 +19,7 @@ constexpr unsigned kErrLenTooLong = 0x8u;
 constexpr unsigned kErrTimeout = 0x10u;
 constexpr unsigned kErrCopyRange = 0x20u;
 constexpr unsigned kErrPosition = 0x40u;
+constexpr unsigned kErrSmemAlign = 0x80u;
 
 struct AppendParams {
   const void* k;
