@@ -51,6 +51,33 @@ FALLBACK_HBM_GBS = 6800.0
 L2_BYTES = 126 * 2 ** 20
 
 
+KERNEL_SOURCES = {
+    "paged_decode_partition_kernel": ("paged_kv_cache_275_gb300/csrc/paged_decode.cu",
+                                      "paged_kv_cache_275_gb300/csrc/pkv_internal.h"),
+}
+
+
+def source_hash(kernel: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kernel]:
+        h.update((ROOT / rel).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str) -> float | None:
+    """DRAM bytes per launch from profiles/traffic.txt, if measured on the current kernel source."""
+    path = ROOT / "profiles" / "traffic.txt"
+    if not path.exists():
+        return None
+    want = source_hash(kernel)
+    for line in path.read_text().splitlines():
+        f = line.split()
+        if len(f) >= 4 and not line.startswith("#") and f[0] == kernel and f[1] == workload and f[2] == want:
+            return float(f[3])
+    return None
+
+
 def bf16_peak_tflops() -> tuple[float, str]:
     try:
         return float(json.loads((ROOT / "MEASURED_PEAKS.json").read_text())["bf16_tflops"]), "measured"
@@ -495,7 +522,11 @@ def run_ours(args, dist: Dist) -> dict | None:
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "frac_of": f"{peak_kind} HBM copy bandwidth", "frac_nominal_8TBps": round(
                          achieved / NOMINAL_HBM_GBS, 4),
-                     "traffic": args.traffic, "algorithmic_bytes_per_launch": bytes_attn,
+                     "traffic": args.traffic if args.traffic is not None else recorded_traffic(
+                         "paged_decode_partition_kernel", args.workload),
+                     "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, profiles/traffic.txt "
+                                       f"(kernel source {source_hash('paged_decode_partition_kernel')})",
+                     "algorithmic_bytes_per_launch": bytes_attn,
                      "mean_launch_us": round(part_mean_s * 1e6, 2)},
         "e2e": {"value": round(e2e_value / 1e9, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * e2e_elapsed / K, 4)},
@@ -535,6 +566,64 @@ def run_component(args) -> dict:
         return {"component": "block_manager", "metric": "append slots per second (host, one thread)",
                 "value": round(256 * args.steps / dt, 1), "unit": "slot/s", "steps": args.steps,
                 "us_per_batch_of_256": round(1e6 * dt / args.steps, 2), "kind": "C ABI through ctypes"}
+    if args.component == "trace":
+        # Continuous-batching trace (Qwen3-0.6B shape, 28 layers, up to 256 sequences, 100 decode steps):
+        # every input of every step is generated and staged on the device first; the timed region is
+        # the library calls only (prompt appends of joining sequences, the step's appends, attention).
+        from workloads import TRACE, TraceGenerator, make_generator, randn_bf16, algorithmic_bytes as ab
+        spec = TRACE
+        tg = TraceGenerator(spec, seed=0)
+        gen = make_generator(1, "cuda")
+        H, Hkv, D, NL = spec.num_q_heads, spec.num_kv_heads, spec.head_dim, spec.num_layers
+        kp = [randn_bf16((tg.num_blocks, Hkv, 16, D), gen, "cuda") for _ in range(NL)]
+        vp = [randn_bf16((tg.num_blocks, Hkv, 16, D), gen, "cuda") for _ in range(NL)]
+        steps = []
+        seq_layers = 0
+        bytes_total = 0
+        for st in tg.steps():
+            B = len(st.seq_ids)
+            js = torch.cat([st.join_slots[x] for x in st.joined]).cuda() if st.joined else None
+            nj = 0 if js is None else js.numel()
+            steps.append(dict(bt=st.block_tables.cuda(), cl=st.context_lens.cuda(), slots=st.slot_mapping.cuda(),
+                              js=js, q=randn_bf16((NL, B, H, D), gen, "cuda"),
+                              k=randn_bf16((NL, B, Hkv, D), gen, "cuda"), v=randn_bf16((NL, B, Hkv, D), gen, "cuda"),
+                              pk=randn_bf16((nj, Hkv, D), gen, "cuda") if nj else None,
+                              pv=randn_bf16((nj, Hkv, D), gen, "cuda") if nj else None,
+                              out=torch.empty(B, H, D, dtype=torch.bfloat16, device="cuda")))
+            seq_layers += B * NL
+            bytes_total += NL * (ab(st.context_lens, H, Hkv, D) + append_bytes(B + nj, Hkv, D))
+        W = tg.width
+        ws = torch.empty(pkv.workspace_size(256, H, Hkv, D, W), dtype=torch.uint8, device="cuda")
+
+        def run():
+            for x in steps:
+                for layer in range(NL):
+                    if x["js"] is not None:
+                        pkv.kv_append(x["pk"], x["pv"], x["js"], kp[layer], vp[layer])
+                    pkv.kv_append(x["k"][layer], x["v"][layer], x["slots"], kp[layer], vp[layer])
+                    pkv.paged_decode_attention(x["q"][layer], kp[layer], vp[layer], x["bt"], x["cl"], D ** -0.5,
+                                               x["out"], workspace=ws)
+
+        run()  # warm-up pass (also the parity-tested path)
+        torch.cuda.synchronize()
+        launches0 = pkv.kernel_launch_count()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        e0.record()
+        run()
+        e1.record()
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+        sec = e0.elapsed_time(e1) / 1e3
+        if pkv.get_and_clear_device_error() != 0:
+            raise RuntimeError("device error during the trace")
+        return {"component": "trace", "metric": "continuous-batching trace seq·layer/s", "value": round(
+            seq_layers / sec, 1), "unit": "seq·layer/s", "gbs": round(bytes_total / sec / 1e9, 1),
+                "seconds": round(sec, 4), "host_wall_seconds": round(wall, 4),
+                "gpu_launches": pkv.kernel_launch_count() - launches0,
+                "config": {"workload": f"{spec.name}: {NL} layers, <= {spec.max_seqs} sequences, {spec.steps} "
+                                       f"decode steps, Poisson({spec.join_rate}) joins / finishes",
+                           "seq_layers": seq_layers, "algorithmic_bytes": bytes_total}}
     if args.component == "prefill":
         from workloads import make_prefill_case, prefill_flops
         c = make_prefill_case("prefill_llama3_8b", seed=0).to("cuda")
@@ -617,7 +706,7 @@ def main(argv=None) -> int:
                     help="seconds the reference arm's warm-up + timed steps should take")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per partition launch from an ncu capture of the current kernel")
-    ap.add_argument("--component", choices=("copy_blocks", "block_manager", "prefill"), default=None,
+    ap.add_argument("--component", choices=("copy_blocks", "block_manager", "prefill", "trace"), default=None,
                     help="measure one component instead of the decode step")
     args = ap.parse_args(argv)
     if args.warmup < 3:
