@@ -313,6 +313,7 @@ pkv_status pkv_paged_prefill_attention(const void* q, const void* k_cache, const
   p.num_q_heads = num_q_heads;
   p.num_kv_heads = num_kv_heads;
   p.max_blocks_per_seq = max_blocks_per_seq;
+  p.max_query_len = max_query_len;
   p.scale = scale;
   const cudaError_t e = pkv::launch_paged_prefill(p, head_dim, num_q_heads / num_kv_heads, max_query_len,
                                                   reinterpret_cast<cudaStream_t>(stream));

@@ -233,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (tid == 0 && tile == 0) atomicOr(p.err, kErrLenTooLong);
     return;
   }
-  if (tile == 0 && C > static_cast<int>(gridDim.x) * kTokens && tid == 0) atomicOr(p.err, kErrLenTooLong);
+  if (tile == 0 && C > p.max_query_len && tid == 0) atomicOr(p.err, kErrLenTooLong);  // rows past the grid are lost
   const int i0 = tile * kTokens;  // first chunk token of the tile
   if (i0 >= C) return;            // uniform for the CTA: nothing allocated yet
   if (s_base & 1023u) {           // the swizzled operands need 1024-byte alignment

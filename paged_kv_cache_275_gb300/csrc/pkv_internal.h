@@ -85,6 +85,7 @@ struct PrefillParams {
   int num_q_heads;
   int num_kv_heads;
   int max_blocks_per_seq;
+  int max_query_len;  // host's bound on the chunk lengths (sizes the grid)
   float scale;
 };
 
