@@ -220,10 +220,33 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   const int tile = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);  // longest tiles first
   const int kvh = blockIdx.y;
-  const int b = blockIdx.z;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  // Longest sequences first: CTAs start in blockIdx order (x fastest), so z indexes the
+  // sequences by decreasing context length (ties by index); with x = tiles from the
+  // longest, the launch order approximates longest-processing-time-first and the last
+  // wave holds the shortest tiles.  Ranked in shared memory when num_seqs <= kThreads,
+  // in the V ring (not yet in use) and a spare word of the barrier area: a static
+  // array would push the footprint past two CTAs per SM.
+  int b = blockIdx.z;
+  if (p.num_seqs <= kThreads) {
+    int* s_lens = reinterpret_cast<int*>(smem + T::kOffV);
+    int& s_pick = *reinterpret_cast<int*>(smem + T::kOffBar + 196);
+    if (tid < p.num_seqs) s_lens[tid] = p.context_lens[tid];
+    __syncthreads();
+    if (tid < p.num_seqs) {
+      const int mine = s_lens[tid];
+      int rank = 0;
+      for (int u = 0; u < p.num_seqs; ++u) {
+        const int other = s_lens[u];
+        rank += (other > mine) || (other == mine && u < tid);
+      }
+      if (rank == static_cast<int>(blockIdx.z)) s_pick = tid;
+    }
+    __syncthreads();
+    b = s_pick;
+  }
 
   const int q0 = p.query_start[b];
   const int C = p.query_start[b + 1] - q0;
@@ -474,26 +497,34 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
         for (int x = 0; x < kKeys; ++x) s[x] = (j * kKeys + x) < limit ? s[x] : -INFINITY;
       }
-      float bm = s[0];
+      // Row max as a tree (six dependent steps instead of sixty-three).
+      float mx[kKeys / 2];
 #pragma unroll
-      for (int x = 1; x < kKeys; ++x) bm = fmaxf(bm, s[x]);
-      bm *= qk;  // the scale is positive: the max of the scaled scores
+      for (int x = 0; x < kKeys / 2; ++x) mx[x] = fmaxf(s[2 * x], s[2 * x + 1]);
+#pragma unroll
+      for (int w = kKeys / 4; w >= 1; w /= 2)
+#pragma unroll
+        for (int x = 0; x < w; ++x) mx[x] = fmaxf(mx[x], mx[x + w]);
+      const float bm = mx[0] * qk;  // the scale is positive: the max of the scaled scores
       const bool raise = row_ok && bm > m_used + kSlack;
       const float m_new = raise ? bm : m_used;
       const float alpha = raise ? ex2_approx(m_used - m_new) : 1.f;  // 0 on the first raise
       const float neg_m = row_ok ? -m_new : 0.f;                      // rows past the chunk: all p = 0
-      float2 psum2 = make_float2(0.f, 0.f);
+      float2 acc4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                        make_float2(0.f, 0.f)};
       uint32_t packed[kKeys / 2];
 #pragma unroll
       for (int x = 0; x < kKeys; x += 2) {
         const float p0 = ex2_approx(fmaf(s[x], qk, neg_m));
         const float p1 = ex2_approx(fmaf(s[x + 1], qk, neg_m));
         packed[x / 2] = pack_bf16(p0, p1);
-        // The denominator sums the same bf16 values the MMA multiplies.
-        psum2 = __fadd2_rn(psum2, make_float2(__uint_as_float(packed[x / 2] << 16),
-                                              __uint_as_float(packed[x / 2] & 0xffff0000u)));
+        // The denominator sums the same bf16 values the MMA multiplies (four running sums).
+        acc4[(x / 2) & 3] = __fadd2_rn(acc4[(x / 2) & 3], make_float2(__uint_as_float(packed[x / 2] << 16),
+                                                                      __uint_as_float(packed[x / 2] & 0xffff0000u)));
       }
-      l = l * alpha + (psum2.x + psum2.y);
+      const float2 a01 = __fadd2_rn(acc4[0], acc4[1]), a23 = __fadd2_rn(acc4[2], acc4[3]);
+      const float2 a = __fadd2_rn(a01, a23);
+      l = l * alpha + (a.x + a.y);
       m_used = m_new;
       // O may only be rescaled once the previous P.V has retired; a shared P buffer
       // (D = 64) may only be rewritten then too.  With P in this step's K slot and
