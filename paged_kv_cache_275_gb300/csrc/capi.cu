@@ -14,6 +14,8 @@
 #include <mutex>
 
 #include "pagedkv.h"
+#include "copy_blocks.h"
+#include "paged_prefill.h"
 #include "pkv_internal.h"
 
 // Sticky device error word; one instance per device (module-scope __device__).

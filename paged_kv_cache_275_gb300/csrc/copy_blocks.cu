@@ -8,7 +8,7 @@
 // 16-byte loads and stores, four in flight per thread.
 #include <cuda_runtime.h>
 
-#include "pkv_internal.h"
+#include "copy_blocks.h"
 
 namespace pkv {
 namespace {

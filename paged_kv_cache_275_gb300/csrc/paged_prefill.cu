@@ -32,7 +32,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "pkv_internal.h"
+#include "paged_prefill.h"
 
 namespace pkv {
 namespace {

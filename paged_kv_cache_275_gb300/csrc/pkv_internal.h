@@ -59,40 +59,6 @@ struct DecodeParams {
   int64_t max_position;
 };
 
-struct CopyParams {
-  void* k_cache;
-  void* v_cache;
-  const int64_t* src_dst;  // [num_pairs][2]
-  unsigned* err;
-  int64_t num_blocks;
-  int64_t chunks_per_block;  // 16-byte chunks in one block (all kv heads)
-};
-
-// copy_blocks kernel launch (one CTA per pair and K/V).
-cudaError_t launch_copy_blocks(const CopyParams& p, int num_pairs, cudaStream_t stream);
-
-struct PrefillParams {
-  const void* q;               // bf16 [T][num_q_heads][head_dim]
-  const void* k_cache;
-  const void* v_cache;
-  const int32_t* block_tables;
-  const int32_t* context_lens;  // prefix + chunk
-  const int32_t* query_start;   // [num_seqs + 1]
-  void* out;                    // bf16 [T][num_q_heads][head_dim]
-  unsigned* err;
-  int64_t num_blocks;
-  int num_seqs;
-  int num_q_heads;
-  int num_kv_heads;
-  int max_blocks_per_seq;
-  int max_query_len;  // host's bound on the chunk lengths (sizes the grid)
-  float scale;
-};
-
-// Chunked prefill attention (tensor cores); grid covers max_query_len rows per sequence.
-cudaError_t launch_paged_prefill(const PrefillParams& p, int head_dim, int group, int max_query_len,
-                                 cudaStream_t stream);
-
 // Set the per-host-thread message returned by pkv_last_error_message().
 void set_error_message(const char* message);
 
