@@ -12,15 +12,18 @@
 // tile serves the whole group.  Keys advance 64 at a time (4 pages of 16).
 //   * warp 4 (one lane): TMA producer.  Each page half (16 tokens x 64 dims) is a
 //     2D tensor-map copy with 128-byte swizzle, gathered through the block table
-//     into a 2-stage K/V ring; mbarrier completion by transaction bytes.
+//     into a K ring (3 slots) and a V ring (2 slots); mbarrier completion by
+//     transaction bytes.
 //   * warp 5 (one lane): MMA issuer.  tcgen05.mma kind::f16 (bf16 in, fp32
 //     accumulate): S = Q K^T into one of two TMEM buffers (M 128, N 64), then
-//     O += P V into TMEM (M 128, N 64 per 64-dim half of V), commits to mbarriers.
+//     O += P V into TMEM (M 128, N 64 per 64-dim half of V) with P read from TMEM,
+//     commits to mbarriers.  A K slot frees as soon as its S retires.
 //     The warp also allocates and frees the TMEM columns.
 //   * warps 0-3 (128 threads, one row each, the TMEM lanes they may address):
 //     stage Q, then per key step read S (tcgen05.ld), apply the causal and length
 //     mask, run the online softmax in base 2 (lazy rescale: O is rescaled only
-//     when a row's max grows by more than 2^8), write P as bf16 to shared memory;
+//     when a row's max grows by more than 2^8), write P as bf16 pairs into TMEM over
+//     the S values just read;
 //     finally read O, divide by the row sum and store bf16 rows.
 // Every mbarrier wait is bounded by a time limit; a wait that runs out sets
 // PKV_DEVERR_PIPELINE_TIMEOUT, the warps finish their loops and the TMEM is
@@ -39,11 +42,11 @@ namespace {
 
 constexpr int kRows = 128;    // MMA M: query rows (chunk tokens x group heads)
 constexpr int kKeys = 64;     // keys per step (MMA N of S, MMA K of P.V)
-constexpr int kKStages = 3;   // K ring depth (at D = 128 a K slot also carries its step's P)
+constexpr int kKStages = 3;   // K ring depth
 constexpr int kVStages = 2;   // V ring depth
 constexpr int kThreads = 192; // warps 0-3 softmax, 4 producer, 5 MMA
 constexpr int kTmemCols = 256;
-constexpr int kColS = 0;      // S buffers at columns [0, 64) and [64, 128)
+constexpr int kColS = 0;      // S buffers at columns [0, 64) and [64, 128); P (bf16 pairs) over the first 32 of each
 constexpr int kColO = 128;    // O at columns [128, 128 + D)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kSlack = 8.0f;
@@ -58,13 +61,7 @@ struct Pf {
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kHalves * kQHalf;
   static constexpr int kOffV = kOffK + kKStages * kTile;
-  // At D = 128 a step's K tile (64 keys x 128 dims) is exactly the size of its P
-  // tile (128 rows x 64 keys): once S = Q K^T has retired, P is written over it,
-  // which keeps two CTAs per SM.  At D = 64 P has a buffer of its own.
-  static constexpr bool kPInK = (kTile == kRows * kKeys * 2);
-  static constexpr int kOffP = kOffV + kVStages * kTile;
-  static constexpr int kOffBar = kOffP + (kPInK ? 0 : kRows * kKeys * 2);
-  __host__ __device__ static constexpr int p_offset(int kslot) { return kPInK ? kOffK + kslot * kTile : kOffP; }
+  static constexpr int kOffBar = kOffV + kVStages * kTile;
   // The dynamic shared memory is requested 1024-byte aligned (checked at run time),
   // so no alignment slack: 112.25 KB at D = 128, two CTAs per SM.
   static constexpr int kRaw = kOffBar + 256;  // barriers + TMEM slot
@@ -145,6 +142,14 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b
       "l"(a), "l"(b), "r"(idesc), "r"(acc)
       : "memory");
 }
+// Same, with A read from tensor memory (128 lanes = rows, K along the columns as bf16 pairs).
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      : "memory");
+}
 __device__ __forceinline__ void mma_commit(uint32_t b) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(b) : "memory");
 }
@@ -195,6 +200,17 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) 
       "r"(__float_as_uint(v[29])), "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
       : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// 32 lanes x 32 columns of raw 32-bit values; the caller waits (tcgen05.wait::st).
+__device__ __forceinline__ void tmem_st32_raw(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]),
+      "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]),
+      "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
 }
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -272,9 +288,13 @@ __global__ void __launch_bounds__(kThreads, 2)
   // S = Q K^T retires, a V slot when its O += P V retires, so each stream is
   // fetched about two steps ahead of its use.
   const uint32_t bar = s_base + T::kOffBar;
-  const uint32_t k_full = bar, k_empty = bar + 24, v_full = bar + 48, v_empty = bar + 64, s_full = bar + 80,
-                 p_full = bar + 96, pv_done = bar + 104, o_full = bar + 112, q_ready = bar + 120,
-                 mma_drained = bar + 128;
+  constexpr uint32_t kBarBytes = 8 * (2 * kKStages + 2 * kVStages + 2 + 2 + 4);
+  static_assert(kBarBytes <= 192, "the barriers must end below the TMEM slot at +192");
+  // P ready is one barrier per S buffer, so that a softmax running a step ahead
+  // of the MMA warp's wait can never complete two phases of one barrier unobserved.
+  const uint32_t k_full = bar, k_empty = k_full + 8 * kKStages, v_full = k_empty + 8 * kKStages,
+                 v_empty = v_full + 8 * kVStages, s_full = v_empty + 8 * kVStages, p_full = s_full + 16,
+                 pv_done = p_full + 16, o_full = pv_done + 8, q_ready = o_full + 8, mma_drained = q_ready + 8;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::kOffBar + 192);
 
   if (tid == 0) {
@@ -288,6 +308,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     for (int s = 0; s < 2; ++s) bar_init(s_full + 8 * s, 1);
     bar_init(p_full, 128);
+    bar_init(p_full + 8, 128);
     bar_init(pv_done, 1);
     bar_init(o_full, 1);
     bar_init(q_ready, 128);
@@ -412,14 +433,14 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int kk = 0; kk < 4; ++kk)
               mma_bf16(d, sdesc(s_base + T::kOffQ + h * T::kQHalf + kk * 32), sdesc(kt + h * T::kKVHalf + kk * 32),
                        kIdS, (h | kk) != 0);
-          if (!T::kPInK) mma_commit(k_empty + 8 * s);  // else the slot holds P until P.V retires
+          mma_commit(k_empty + 8 * s);  // the K slot is free once S has retired
           mma_commit(s_full + 8 * (j & 1));
         }
         __syncwarp();
       }
       if (j >= 1) {
-        const int jp = j - 1, ks = jp % kKStages, s = jp % kVStages;  // P of step jp ready once softmax arrives
-        if (!bar_wait(p_full, jp & 1) || !bar_wait(v_full + 8 * s, (jp / kVStages) & 1)) {
+        const int jp = j - 1, s = jp % kVStages;  // P of step jp ready once softmax arrives
+        if (!bar_wait(p_full + 8 * (jp & 1), (jp >> 1) & 1) || !bar_wait(v_full + 8 * s, (jp / kVStages) & 1)) {
           failed = true;
           break;
         }
@@ -442,9 +463,8 @@ __global__ void __launch_bounds__(kThreads, 2)
           for (int h = 0; h < T::kHalves; ++h)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_bf16(tmem + kColO + 64 * h, sdesc(s_base + T::p_offset(ks) + kk * 32),
-                       sdesc(s_base + vt_off + h * T::kKVHalf + kk * 16 * 128), kIdPV, (jp | kk) != 0);
-          if (T::kPInK) mma_commit(k_empty + 8 * ks);
+              mma_bf16_ts(tmem + kColO + 64 * h, tmem + kColS + (jp & 1) * kKeys + kk * 8,
+                          sdesc(s_base + vt_off + h * T::kKVHalf + kk * 16 * 128), kIdPV, (jp | kk) != 0);
           mma_commit(v_empty + 8 * s);
           mma_commit(pv_done);
           if (jp == nsteps - 1) mma_commit(o_full);
@@ -526,11 +546,10 @@ __global__ void __launch_bounds__(kThreads, 2)
       const float2 a = __fadd2_rn(a01, a23);
       l = l * alpha + (a.x + a.y);
       m_used = m_new;
-      // O may only be rescaled once the previous P.V has retired; a shared P buffer
-      // (D = 64) may only be rewritten then too.  With P in this step's K slot and
-      // no rescale, the softmax runs alongside the previous P.V.
+      // O may only be rescaled once the previous P.V has retired; without a
+      // rescale the softmax runs alongside the previous P.V.
       const bool rescale = j >= 1 && __any_sync(0xffffffffu, raise);
-      if ((rescale || (!T::kPInK && j >= 1)) && !__all_sync(0xffffffffu, bar_wait(pv_done, (j - 1) & 1))) {
+      if (rescale && !__all_sync(0xffffffffu, bar_wait(pv_done, (j - 1) & 1))) {
         failed = true;
         break;
       }
@@ -545,14 +564,13 @@ __global__ void __launch_bounds__(kThreads, 2)
           tmem_st32(lane_base + kColO + c0, o);
         }
       }
-      unsigned char* prow = smem + T::p_offset(j % kKStages) + (r >> 3) * 1024 + (r & 7) * 128;
-#pragma unroll
-      for (int ch = 0; ch < 8; ++ch)
-        *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) =
-            make_uint4(packed[4 * ch], packed[4 * ch + 1], packed[4 * ch + 2], packed[4 * ch + 3]);
-      fence_async_smem();
+      // P over the first 32 columns of this step's S buffer, already read: the
+      // tensor-memory A operand of O += P V.  (Step j-2's P.V, the last reader of
+      // this buffer, retired before S of step j did.)
+      tmem_st32_raw(lane_base + kColS + (j & 1) * kKeys, packed);
+      asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_before_sync();
-      bar_arrive(p_full);
+      bar_arrive(p_full + 8 * (j & 1));
     }
     // Epilogue: O / l, bf16, one 2*D-byte row per thread.
     if (!failed && __all_sync(0xffffffffu, bar_wait(o_full, 0))) {
