@@ -7,24 +7,29 @@
 // the chunk already appended); query row i of the chunk attends causally over
 // the first P_b + i + 1 tokens: out = softmax(scale * q K^T) V.
 //
-// How (GB300-first).  One CTA per (128-row query tile, kv head, sequence).  The
-// 128 MMA rows pack 128/G chunk tokens x the G q heads of the group, so every K/V
-// tile serves the whole group.  Keys advance 64 at a time (4 pages of 16).
-//   * warp 4 (one lane): TMA producer.  Each page half (16 tokens x 64 dims) is a
-//     2D tensor-map copy with 128-byte swizzle, gathered through the block table
-//     into a K ring (3 slots) and a V ring (2 slots); mbarrier completion by
-//     transaction bytes.
-//   * warp 5 (one lane): MMA issuer.  tcgen05.mma kind::f16 (bf16 in, fp32
-//     accumulate): S = Q K^T into one of two TMEM buffers (M 128, N 64), then
-//     O += P V into TMEM (M 128, N 64 per 64-dim half of V) with P read from TMEM,
-//     commits to mbarriers.  A K slot frees as soon as its S retires.
-//     The warp also allocates and frees the TMEM columns.
-//   * warps 0-3 (128 threads, one row each, the TMEM lanes they may address):
-//     stage Q, then per key step read S (tcgen05.ld), apply the causal and length
-//     mask, run the online softmax in base 2 (lazy rescale: O is rescaled only
-//     when a row's max grows by more than 2^8), write P as bf16 pairs into TMEM over
-//     the S values just read;
-//     finally read O, divide by the row sum and store bf16 rows.
+// How (GB300-first).  One CTA per SM, per (pair of 128-row query tiles, kv head,
+// sequence).  The 128 MMA rows of a tile pack 128/G chunk tokens x the G q heads
+// of the group; the CTA's two tiles cover consecutive tokens and share every K/V
+// tile.  Keys advance 128 at a time (8 pages of 16), so S = Q K^T is an N = 128
+// MMA and O += P V an N = D one: one thread issues a tcgen05.mma no faster than
+// about one per hundred cycles whatever its N, so the MMAs are made wide and each
+// tile has its own issuing warp.
+//   * warp 8: TMA producer.  Each page half (16 tokens x 64 dims) is a 2D
+//     tensor-map copy with 128-byte swizzle, gathered through the block table into
+//     a K ring (3 slots) and a V ring (2 slots), one copy per lane; mbarrier
+//     completion by transaction bytes.  It also zeroes the rows of the last V
+//     tile past the end of the keys.
+//   * warps 9 + t (one lane): MMA issuer of tile t.  tcgen05.mma kind::f16 (bf16
+//     in, fp32 accumulate): S = Q_t K^T into the tile's TMEM S buffer (M 128,
+//     N 128), then, once the softmax has written P over S, O_t += P V (M 128,
+//     N = D, P read from TMEM); commits to mbarriers.  Warp 9 also allocates and
+//     frees the 512 TMEM columns.
+//   * warps 0-7 (one row each; warps 4t..4t+3 serve tile t, each warp the TMEM
+//     lanes 32 (warp % 4) .. + 31): stage Q, then per key step read S
+//     (tcgen05.ld), apply the causal and length mask, run the online softmax in
+//     base 2 (lazy rescale: O is rescaled only when a row's max grows by more than
+//     2^8), write P as bf16 pairs into TMEM over the S values just read; finally
+//     read O, divide by the row sum and store bf16 rows.
 // Every mbarrier wait is bounded by a time limit; a wait that runs out sets
 // PKV_DEVERR_PIPELINE_TIMEOUT, the warps finish their loops and the TMEM is
 // freed before the CTA exits.
@@ -40,14 +45,24 @@
 namespace pkv {
 namespace {
 
-constexpr int kRows = 128;    // MMA M: query rows (chunk tokens x group heads)
-constexpr int kKeys = 64;     // keys per step (MMA N of S, MMA K of P.V)
-constexpr int kKStages = 3;   // K ring depth
-constexpr int kVStages = 2;   // V ring depth
-constexpr int kThreads = 192; // warps 0-3 softmax, 4 producer, 5 MMA
-constexpr int kTmemCols = 256;
-constexpr int kColS = 0;      // S buffers at columns [0, 64) and [64, 128); P (bf16 pairs) over the first 32 of each
-constexpr int kColO = 128;    // O at columns [128, 128 + D)
+constexpr int kRows = 128;    // MMA M: query rows of one tile (chunk tokens x group heads)
+constexpr int kTiles = 2;     // query tiles per CTA; every K/V tile feeds both
+constexpr int kKeys = 128;    // keys per step (MMA N of S, MMA K of P.V)
+#ifndef PKV_PF_KSTAGES
+#define PKV_PF_KSTAGES 3
+#endif
+#ifndef PKV_PF_VSTAGES
+#define PKV_PF_VSTAGES 2
+#endif
+constexpr int kKStages = PKV_PF_KSTAGES;  // K ring depth
+constexpr int kVStages = PKV_PF_VSTAGES;  // V ring depth
+constexpr int kProducerWarp = 4 * kTiles;  // warps 0-7 softmax (four per tile)
+constexpr int kMmaWarp0 = kProducerWarp + 1;  // one MMA-issuing warp per tile
+constexpr int kThreads = 32 * (kMmaWarp0 + kTiles);
+constexpr int kTmemCols = 512;  // per tile t: S at [256 t, 256 t + 128), O at [256 t + 128, 256 t + 128 + D)
+__host__ __device__ constexpr int col_s(int t) { return 256 * t; }  // P (bf16 pairs) over the first 64 of S
+__host__ __device__ constexpr int col_o(int t) { return 256 * t + 128; }
+constexpr int kTmemSlotOffset = 384;  // in the 512-byte barrier area: barriers below, TMEM slot and sequence pick here
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kSlack = 8.0f;
 constexpr unsigned long long kWaitNs = 2000000000ull;
@@ -56,18 +71,19 @@ template <int D>
 struct Pf {
   static constexpr int kHalves = D / 64;           // 128-byte swizzle atoms across a row
   static constexpr int kQHalf = kRows * 128;       // 16 KB: 128 rows x 64 dims
-  static constexpr int kKVHalf = kKeys * 128;      // 8 KB: 64 keys x 64 dims
+  static constexpr int kQTile = kHalves * kQHalf;  // one tile's Q
+  static constexpr int kKVHalf = kKeys * 128;      // 16 KB: 128 keys x 64 dims
   static constexpr int kTile = kHalves * kKVHalf;  // one K (or V) tile of a step
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kHalves * kQHalf;
+  static constexpr int kOffK = kOffQ + kTiles * kQTile;
   static constexpr int kOffV = kOffK + kKStages * kTile;
   static constexpr int kOffBar = kOffV + kVStages * kTile;
   // The dynamic shared memory is requested 1024-byte aligned (checked at run time),
-  // so no alignment slack: 112.25 KB at D = 128, two CTAs per SM.
-  static constexpr int kRaw = kOffBar + 256;  // barriers + TMEM slot
-  // At least 80 KB so that no more than two CTAs share an SM: each holds 256 of
-  // the SM's 512 TMEM columns, and a third CTA's allocation would have to wait.
-  static constexpr int kSmem = kRaw > 80 * 1024 ? kRaw : 80 * 1024;
+  // so no alignment slack: 224.5 KB at D = 128.
+  static constexpr int kRaw = kOffBar + 512;  // barriers, TMEM slot, sequence pick
+  // At least 120 KB so that one CTA holds the SM: it owns all 512 TMEM columns,
+  // and a second CTA's allocation would have to wait.
+  static constexpr int kSmem = kRaw > 120 * 1024 ? kRaw : 120 * 1024;
 };
 
 // ---------------------------------------------------------------------------
@@ -119,20 +135,20 @@ __device__ __forceinline__ void tc_before_sync() { asm volatile("tcgen05.fence::
 __device__ __forceinline__ void tc_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
 // Shared-memory matrix descriptor: 128-byte swizzle with 8-row groups 1024 bytes
-// apart.  Every operand here is one swizzle atom (64 elements) wide across, so
-// the only stride the MMA walks is the one between 8-row groups; both offset
-// fields carry it.
-__device__ __forceinline__ uint64_t sdesc(uint32_t addr) {
+// apart (the stride byte offset).  K-major operands are one swizzle atom (64
+// elements) wide across the 16-element K of an MMA; an MN-major operand (V, read
+// as N = D) may span two atoms along N, `lbo` bytes apart.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo = 1024) {
   uint64_t d = (addr & 0x3FFFFu) >> 4;
-  d |= uint64_t(1024 >> 4) << 16;    // leading byte offset
+  d |= uint64_t(lbo >> 4) << 16;     // leading byte offset (MN-major: next 64-wide atom along N)
   d |= uint64_t(1024 >> 4) << 32;    // stride byte offset: 8 rows x 128 B
   d |= uint64_t(1) << 46;            // descriptor version
   d |= uint64_t(2) << 61;            // 128-byte swizzle
   return d;
 }
-// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M 128, N 64.
-__host__ __device__ constexpr uint32_t idesc_bf16(bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) | ((64u >> 3) << 17) |
+// Instruction descriptor, kind::f16: bf16 A and B, fp32 D, M 128, N n.
+__host__ __device__ constexpr uint32_t idesc_bf16(int n, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) | ((static_cast<uint32_t>(n) >> 3) << 17) |
          ((128u >> 4) << 24);
 }
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
@@ -226,11 +242,12 @@ __device__ __forceinline__ uint32_t swz(int r, int chunk) {
 // The kernel
 // ---------------------------------------------------------------------------
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     paged_prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap map_k,
                          const __grid_constant__ CUtensorMap map_v) {
   using T = Pf<D>;
-  constexpr int kTokens = kRows / G;  // chunk tokens per tile
+  constexpr int kTokens = kRows / G;            // chunk tokens per 128-row tile
+  constexpr int kCtaTokens = kTiles * kTokens;  // chunk tokens per CTA
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t s_base = saddr(smem);
 
@@ -243,12 +260,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   // sequences by decreasing context length (ties by index); with x = tiles from the
   // longest, the launch order approximates longest-processing-time-first and the last
   // wave holds the shortest tiles.  Ranked in shared memory when num_seqs <= kThreads,
-  // in the V ring (not yet in use) and a spare word of the barrier area: a static
-  // array would push the footprint past two CTAs per SM.
+  // in the V ring (not yet in use) and a spare word of the barrier area.
   int b = blockIdx.z;
   if (p.num_seqs <= kThreads) {
     int* s_lens = reinterpret_cast<int*>(smem + T::kOffV);
-    int& s_pick = *reinterpret_cast<int*>(smem + T::kOffBar + 196);
+    int& s_pick = *reinterpret_cast<int*>(smem + T::kOffBar + kTmemSlotOffset + 4);
     if (tid < p.num_seqs) s_lens[tid] = p.context_lens[tid];
     __syncthreads();
     if (tid < p.num_seqs) {
@@ -273,49 +289,57 @@ __global__ void __launch_bounds__(kThreads, 2)
     return;
   }
   if (tile == 0 && C > p.max_query_len && tid == 0) atomicOr(p.err, kErrLenTooLong);  // rows past the grid are lost
-  const int i0 = tile * kTokens;  // first chunk token of the tile
-  if (i0 >= C) return;            // uniform for the CTA: nothing allocated yet
-  if (s_base & 1023u) {           // the swizzled operands need 1024-byte alignment
+  const int i0 = tile * kCtaTokens;  // first chunk token of the CTA
+  if (i0 >= C) return;               // uniform for the CTA: nothing allocated yet
+  if (s_base & 1023u) {              // the swizzled operands need 1024-byte alignment
     if (tid == 0) atomicOr(p.err, kErrSmemAlign);
     return;
   }
   const int prefix = L - C;
-  const int i_last = min(C, i0 + kTokens) - 1;
-  const int kv_end = prefix + i_last + 1;            // keys the tile's last row sees
+  const int i_last = min(C, i0 + kCtaTokens) - 1;
+  const int n_tiles = (i0 + kTokens < C) ? 2 : 1;  // the second tile only if it holds chunk rows
+  const int kv_end = prefix + i_last + 1;          // keys the CTA's last row sees
   const int nsteps = (kv_end + kKeys - 1) / kKeys;
+  const bool tail = kv_end < nsteps * kKeys;       // the last step has keys past the end
 
-  // Separate K and V rings over the same stage memory: a K slot frees when its
-  // S = Q K^T retires, a V slot when its O += P V retires, so each stream is
-  // fetched about two steps ahead of its use.
+  // Barriers.  K and V rings: a slot frees when every tile's MMA that reads it has
+  // retired.  Per tile: S ready, P ready, O final, Q staged, MMAs drained.  Each
+  // tile has one S buffer (P is written over it), so S of step j + 1 is issued
+  // after P.V of step j by the same thread: the S-ready arrival of a step also
+  // proves the previous P.V retired, and no barrier can run two phases ahead
+  // of its waiter.
   const uint32_t bar = s_base + T::kOffBar;
-  constexpr uint32_t kBarBytes = 8 * (2 * kKStages + 2 * kVStages + 2 + 2 + 4);
-  static_assert(kBarBytes <= 192, "the barriers must end below the TMEM slot at +192");
-  // P ready is one barrier per S buffer, so that a softmax running a step ahead
-  // of the MMA warp's wait can never complete two phases of one barrier unobserved.
+  constexpr uint32_t kBarBytes = 8 * (2 * kKStages + 2 * kVStages + 1 + 5 * kTiles);
+  static_assert(kBarBytes <= kTmemSlotOffset, "the barriers must end below the TMEM slot");
   const uint32_t k_full = bar, k_empty = k_full + 8 * kKStages, v_full = k_empty + 8 * kKStages,
-                 v_empty = v_full + 8 * kVStages, s_full = v_empty + 8 * kVStages, p_full = s_full + 16,
-                 pv_done = p_full + 16, o_full = pv_done + 8, q_ready = o_full + 8, mma_drained = q_ready + 8;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::kOffBar + 192);
+                 v_empty = v_full + 8 * kVStages, v_tail = v_empty + 8 * kVStages,
+                 s_full = v_tail + 8,                 // [tile]
+      p_full = s_full + 8 * kTiles,                   // [tile]
+      o_full = p_full + 8 * kTiles,                   // [tile]
+      q_ready = o_full + 8 * kTiles,                  // [tile]
+      mma_drained = q_ready + 8 * kTiles;             // [tile]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::kOffBar + kTmemSlotOffset);
 
   if (tid == 0) {
     for (int s = 0; s < kKStages; ++s) {
       bar_init(k_full + 8 * s, 1);
-      bar_init(k_empty + 8 * s, 1);
+      bar_init(k_empty + 8 * s, n_tiles);
     }
     for (int s = 0; s < kVStages; ++s) {
       bar_init(v_full + 8 * s, 1);
-      bar_init(v_empty + 8 * s, 1);
+      bar_init(v_empty + 8 * s, n_tiles);
     }
-    for (int s = 0; s < 2; ++s) bar_init(s_full + 8 * s, 1);
-    bar_init(p_full, 128);
-    bar_init(p_full + 8, 128);
-    bar_init(pv_done, 1);
-    bar_init(o_full, 1);
-    bar_init(q_ready, 128);
-    bar_init(mma_drained, 1);
+    bar_init(v_tail, 1);
+    for (int t = 0; t < kTiles; ++t) {
+      bar_init(s_full + 8 * t, 1);
+      bar_init(p_full + 8 * t, 128);
+      bar_init(o_full + 8 * t, 1);
+      bar_init(q_ready + 8 * t, 128);
+      bar_init(mma_drained + 8 * t, 1);
+    }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 5) {
+  if (warp == kMmaWarp0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tmem_slot)),
                  "r"(kTmemCols)
                  : "memory");
@@ -327,11 +351,12 @@ __global__ void __launch_bounds__(kThreads, 2)
   const uint32_t tmem = *tmem_slot;
   bool failed = false;
 
-  if (warp == 4) {
-    // ---------------- TMA producer (whole warp; lane 0 issues) ----------------
+  if (warp == kProducerWarp) {
+    // ---------------- TMA producer (whole warp) ----------------
     // Block ids come from a 32-page window held one per lane, with the next
     // window already in flight, so no copy waits on a dependent table load.
     constexpr int kPages = kKeys / kBlockTokens;  // pages per step
+    static_assert(32 % kPages == 0 && kPages * T::kHalves <= 32, "a step's pages sit in one window, one copy per lane");
     const int npages = (kv_end + kBlockTokens - 1) / kBlockTokens;
     const int32_t* table = p.block_tables + static_cast<size_t>(b) * p.max_blocks_per_seq;
     auto fetch = [&](int page) -> int {
@@ -345,61 +370,67 @@ __global__ void __launch_bounds__(kThreads, 2)
     };
     int win = 0;
     int id_cur = fetch(lane), id_next = fetch(32 + lane);
-    int prev_ids[kPages];
+    int prev_id = 0;  // this lane's page id of the previous step (for its V)
     int issued_k = 0, issued_v = 0;
-    auto issue = [&](int j, const int (&ids)[kPages], uint32_t dst, const CUtensorMap* map, uint32_t full) {
-      int pages = 0;
-#pragma unroll
-      for (int pg = 0; pg < kPages; ++pg)
-        if ((j * kKeys + pg * kBlockTokens) < kv_end) ++pages;
-      if (lane == 0) {
-        bar_expect_tx(full, static_cast<uint32_t>(pages * T::kHalves * kBlockTokens * 128));
-        for (int pg = 0; pg < pages; ++pg) {
-          const int row = (ids[pg] * p.num_kv_heads + kvh) * kBlockTokens;
-          for (int h = 0; h < T::kHalves; ++h)
-            tma_load_2d(dst + h * T::kKVHalf + pg * (kBlockTokens * 128), map, 64 * h, row, full);
-        }
-      }
+    // One copy per lane (page lane / halves, half lane % halves): a thread's tensor
+    // copies issue one after another, slowly, while copies from different lanes go
+    // out together.
+    const int my_pg = lane / T::kHalves, my_h = lane % T::kHalves;
+    auto issue = [&](int j, int my_id, uint32_t dst, const CUtensorMap* map, uint32_t full) {
+      const int pages = min(kPages, npages - j * kPages);
+      if (lane == 0) bar_expect_tx(full, static_cast<uint32_t>(pages * T::kHalves * kBlockTokens * 128));
+      __syncwarp();
+      if (my_pg < pages)
+        tma_load_2d(dst + my_h * T::kKVHalf + my_pg * (kBlockTokens * 128), map, 64 * my_h,
+                    (my_id * p.num_kv_heads + kvh) * kBlockTokens, full);
     };
     for (int j = 0; j <= nsteps && !failed; ++j) {
+      int my_id = 0;
       if (j < nsteps) {  // K of step j
         const int s = j % kKStages;
         if (j >= kKStages && !__all_sync(0xffffffffu, bar_wait(k_empty + 8 * s, ((j / kKStages) + 1) & 1))) {
           failed = true;
           break;
         }
-        int ids[kPages];
-#pragma unroll
-        for (int pg = 0; pg < kPages; ++pg) {
-          const int page = j * kPages + pg;
-          if (page / 32 != win) {  // slide the window
-            ++win;
-            id_cur = id_next;
-            id_next = fetch(32 * (win + 1) + lane);
-          }
-          ids[pg] = __shfl_sync(0xffffffffu, id_cur, page % 32);
+        const int first_page = j * kPages;
+        if (first_page / 32 != win) {  // slide the window
+          ++win;
+          id_cur = id_next;
+          id_next = fetch(32 * (win + 1) + lane);
         }
-        issue(j, ids, s_base + T::kOffK + s * T::kTile, &map_k, k_full + 8 * s);
+        my_id = __shfl_sync(0xffffffffu, id_cur, (first_page % 32) + min(my_pg, kPages - 1));
+        issue(j, my_id, s_base + T::kOffK + s * T::kTile, &map_k, k_full + 8 * s);
         issued_k = j + 1;
-        if (j >= 1) {  // V of step j - 1 uses the ids its K used
-          const int jv = j - 1, sv = jv % kVStages;
-          if (jv >= kVStages && !__all_sync(0xffffffffu, bar_wait(v_empty + 8 * sv, ((jv / kVStages) + 1) & 1))) {
-            failed = true;
-            break;
-          }
-          issue(jv, prev_ids, s_base + T::kOffV + sv * T::kTile, &map_v, v_full + 8 * sv);
-          issued_v = jv + 1;
-        }
-#pragma unroll
-        for (int pg = 0; pg < kPages; ++pg) prev_ids[pg] = ids[pg];
-      } else {  // V of the last step
+      }
+      if (j >= 1) {  // V of step j - 1 uses the ids its K used
         const int jv = j - 1, sv = jv % kVStages;
         if (jv >= kVStages && !__all_sync(0xffffffffu, bar_wait(v_empty + 8 * sv, ((jv / kVStages) + 1) & 1))) {
           failed = true;
           break;
         }
-        issue(jv, prev_ids, s_base + T::kOffV + sv * T::kTile, &map_v, v_full + 8 * sv);
+        issue(jv, prev_id, s_base + T::kOffV + sv * T::kTile, &map_v, v_full + 8 * sv);
         issued_v = jv + 1;
+      }
+      prev_id = my_id;
+    }
+    if (!failed && tail) {
+      // Keys past the CTA's end in the last V tile (a page's tail, or pages not
+      // copied): zero their rows once the copy has landed, so that stale or NaN
+      // data never meets p = 0, then release the tile to the MMA warps.
+      const int jv = nsteps - 1, sv = jv % kVStages;
+      if (__all_sync(0xffffffffu, bar_wait(v_full + 8 * sv, (jv / kVStages) & 1))) {
+        unsigned char* vt = smem + T::kOffV + sv * T::kTile;
+        const int first = kv_end - jv * kKeys;
+        for (int idx = lane; idx < (kKeys - first) * T::kHalves * 8; idx += 32) {
+          const int r = first + idx / (T::kHalves * 8);
+          const int rem = idx % (T::kHalves * 8);
+          *reinterpret_cast<uint4*>(vt + (rem / 8) * T::kKVHalf + swz(r, rem % 8)) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) bar_arrive(v_tail);
+      } else {
+        failed = true;
       }
     }
     if (failed && lane == 0) {  // let the copies still in flight land before the CTA exits
@@ -410,79 +441,66 @@ __global__ void __launch_bounds__(kThreads, 2)
         bar_wait(v_full + 8 * (j % kVStages), (j / kVStages) & 1);
     }
     __syncwarp();
-  } else if (warp == 5) {
-    // ---------------- MMA issuer ----------------
-    constexpr uint32_t kIdS = idesc_bf16(false);
-    constexpr uint32_t kIdPV = idesc_bf16(true);
-    if (!bar_wait(q_ready, 0)) failed = true;
-    tc_after_sync();
-    for (int j = 0; j <= nsteps && !failed; ++j) {
-      if (j < nsteps) {
-        const int s = j % kKStages;
-        if (!bar_wait(k_full + 8 * s, (j / kKStages) & 1)) {
+  } else if (warp >= kMmaWarp0) {
+    // ---------------- MMA issuers: warp kMmaWarp0 + t serves tile t ----------------
+    // Step j: S = Q_t K_j^T (N = 128 keys), wait for P, then O_t += P V_j (N = D).
+    const int t = warp - kMmaWarp0;
+    if (t < n_tiles) {
+      constexpr uint32_t kIdS = idesc_bf16(kKeys, false);
+      constexpr uint32_t kIdPV = idesc_bf16(D, true);
+      const uint32_t d_s = tmem + col_s(t), d_o = tmem + col_o(t);
+      const uint32_t qt = s_base + T::kOffQ + t * T::kQTile;
+      if (!bar_wait(q_ready + 8 * t, 0)) failed = true;
+      tc_after_sync();
+      for (int j = 0; j < nsteps && !failed; ++j) {
+        const int sk = j % kKStages, sv = j % kVStages;
+        if (!bar_wait(k_full + 8 * sk, (j / kKStages) & 1)) {
           failed = true;
           break;
         }
         if (lane == 0) {
           tc_after_sync();
-          const uint32_t kt = s_base + T::kOffK + s * T::kTile;
-          const uint32_t d = tmem + kColS + (j & 1) * kKeys;
+          const uint32_t kt = s_base + T::kOffK + sk * T::kTile;
 #pragma unroll
           for (int h = 0; h < T::kHalves; ++h)
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)
-              mma_bf16(d, sdesc(s_base + T::kOffQ + h * T::kQHalf + kk * 32), sdesc(kt + h * T::kKVHalf + kk * 32),
-                       kIdS, (h | kk) != 0);
-          mma_commit(k_empty + 8 * s);  // the K slot is free once S has retired
-          mma_commit(s_full + 8 * (j & 1));
+              mma_bf16(d_s, sdesc(qt + h * T::kQHalf + kk * 32), sdesc(kt + h * T::kKVHalf + kk * 32), kIdS,
+                       (h | kk) != 0);
+          mma_commit(s_full + 8 * t);
+          mma_commit(k_empty + 8 * sk);  // the K slot frees once every tile's S has retired
         }
         __syncwarp();
-      }
-      if (j >= 1) {
-        const int jp = j - 1, s = jp % kVStages;  // P of step jp ready once softmax arrives
-        if (!bar_wait(p_full + 8 * (jp & 1), (jp >> 1) & 1) || !bar_wait(v_full + 8 * s, (jp / kVStages) & 1)) {
+        const bool last = j == nsteps - 1;
+        if (!bar_wait(p_full + 8 * t, j & 1) ||
+            !(last && tail ? bar_wait(v_tail, 0) : bar_wait(v_full + 8 * sv, (j / kVStages) & 1))) {
           failed = true;
           break;
         }
-        const uint32_t vt_off = T::kOffV + s * T::kTile;
-        if (jp == nsteps - 1 && kv_end < (jp + 1) * kKeys) {
-          // Keys past the tile's end: zero their V rows (stale or NaN data must not meet p = 0).
-          const int first = kv_end - jp * kKeys;
-          for (int idx = lane; idx < (kKeys - first) * T::kHalves * 8; idx += 32) {
-            const int r = first + idx / (T::kHalves * 8);
-            const int rem = idx % (T::kHalves * 8);
-            const int h = rem / 8, ch = rem % 8;
-            *reinterpret_cast<uint4*>(smem + vt_off + h * T::kKVHalf + swz(r, ch)) = make_uint4(0u, 0u, 0u, 0u);
-          }
-          fence_async_smem();
-          __syncwarp();
-        }
         if (lane == 0) {
           tc_after_sync();
+          const uint32_t vt = s_base + T::kOffV + sv * T::kTile;
 #pragma unroll
-          for (int h = 0; h < T::kHalves; ++h)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_bf16_ts(tmem + kColO + 64 * h, tmem + kColS + (jp & 1) * kKeys + kk * 8,
-                          sdesc(s_base + vt_off + h * T::kKVHalf + kk * 16 * 128), kIdPV, (jp | kk) != 0);
-          mma_commit(v_empty + 8 * s);
-          mma_commit(pv_done);
-          if (jp == nsteps - 1) mma_commit(o_full);
+          for (int kk = 0; kk < kKeys / 16; ++kk)
+            mma_bf16_ts(d_o, d_s + kk * 8, sdesc(vt + kk * 16 * 128, T::kKVHalf), kIdPV, (j | kk) != 0);
+          mma_commit(v_empty + 8 * sv);
+          if (last) mma_commit(o_full + 8 * t);
         }
         __syncwarp();
       }
+      if (failed && lane == 0) atomicOr(p.err, kErrTimeout);
+      // Every MMA this warp issued must have completed before the TMEM is freed.
+      if (lane == 0) {
+        mma_commit(mma_drained + 8 * t);
+        bar_wait(mma_drained + 8 * t, 0);
+      }
+      __syncwarp();
     }
-    if (failed && lane == 0) atomicOr(p.err, kErrTimeout);
-    // Every MMA this warp issued must have completed before the TMEM is freed.
-    if (lane == 0) {
-      mma_commit(mma_drained);
-      bar_wait(mma_drained, 0);
-    }
-    __syncwarp();
-  } else {
-    // ---------------- softmax / epilogue (warps 0-3, thread = row) ----------------
-    const int r = tid;
-    const int i = i0 + r / G;  // chunk token of this row
+  } else if ((warp >> 2) < n_tiles) {
+    // ---------------- softmax / epilogue (warps 0-7, thread = row of tile warp / 4) ----------------
+    const int t = warp >> 2;
+    const int r = tid & (kRows - 1);
+    const int i = i0 + t * kTokens + r / G;  // chunk token of this row
     const int g = r % G;
     const bool row_ok = i < C;
     // Stage Q rows (zero rows past the chunk) in the swizzled K-major layout.
@@ -490,34 +508,39 @@ __global__ void __launch_bounds__(kThreads, 2)
       const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
                                                         (static_cast<size_t>(q0 + (row_ok ? i : 0)) * p.num_q_heads +
                                                          kvh * G + g) * D);
+      unsigned char* qt = smem + T::kOffQ + t * T::kQTile;
 #pragma unroll
       for (int h = 0; h < T::kHalves; ++h)
 #pragma unroll
         for (int ch = 0; ch < 8; ++ch) {
           const uint4 v = row_ok ? __ldg(src + h * 8 + ch) : make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4*>(smem + T::kOffQ + h * T::kQHalf + swz(r, ch)) = v;
+          *reinterpret_cast<uint4*>(qt + h * T::kQHalf + swz(r, ch)) = v;
         }
       fence_async_smem();
-      bar_arrive(q_ready);
+      bar_arrive(q_ready + 8 * t);
     }
     const float qk = p.scale * kLog2e;
     const int limit = row_ok ? prefix + i + 1 : 0;  // keys this row may see
     float m_used = -INFINITY, l = 0.f;
-    const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    // A warp reaches the TMEM lanes 32 * (warp % 4) .. + 31: rows r of either tile.
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+    const uint32_t s_cols = lane_base + col_s(t), o_cols = lane_base + col_o(t);
     for (int j = 0; j < nsteps && !failed; ++j) {
-      if (!__all_sync(0xffffffffu, bar_wait(s_full + 8 * (j & 1), (j >> 1) & 1))) {
+      // S of step j has landed, and with it the tile's P.V of step j - 1 (same issuer, issued before).
+      if (!__all_sync(0xffffffffu, bar_wait(s_full + 8 * t, j & 1))) {
         failed = true;
         break;
       }
       tc_after_sync();
       float s[kKeys];
-      tmem_ld64(lane_base + kColS + (j & 1) * kKeys, s);
+      tmem_ld64(s_cols, *reinterpret_cast<float(*)[64]>(&s[0]));
+      tmem_ld64(s_cols + 64, *reinterpret_cast<float(*)[64]>(&s[64]));
       // Causal / length mask, only on steps that some row of the warp does not see whole.
       if (__any_sync(0xffffffffu, (j + 1) * kKeys > limit)) {
 #pragma unroll
         for (int x = 0; x < kKeys; ++x) s[x] = (j * kKeys + x) < limit ? s[x] : -INFINITY;
       }
-      // Row max as a tree (six dependent steps instead of sixty-three).
+      // Row max as a tree.
       float mx[kKeys / 2];
 #pragma unroll
       for (int x = 0; x < kKeys / 2; ++x) mx[x] = fmaxf(s[2 * x], s[2 * x + 1]);
@@ -546,34 +569,27 @@ __global__ void __launch_bounds__(kThreads, 2)
       const float2 a = __fadd2_rn(a01, a23);
       l = l * alpha + (a.x + a.y);
       m_used = m_new;
-      // O may only be rescaled once the previous P.V has retired; without a
-      // rescale the softmax runs alongside the previous P.V.
-      const bool rescale = j >= 1 && __any_sync(0xffffffffu, raise);
-      if (rescale && !__all_sync(0xffffffffu, bar_wait(pv_done, (j - 1) & 1))) {
-        failed = true;
-        break;
-      }
-      tc_after_sync();
-      if (rescale) {
+      // O is rescaled in place (its previous P.V has retired: see the wait above).
+      if (j >= 1 && __any_sync(0xffffffffu, raise)) {
 #pragma unroll
         for (int c0 = 0; c0 < D; c0 += 32) {
           float o[32];
-          tmem_ld32(lane_base + kColO + c0, o);
+          tmem_ld32(o_cols + c0, o);
 #pragma unroll
           for (int x = 0; x < 32; ++x) o[x] *= alpha;
-          tmem_st32(lane_base + kColO + c0, o);
+          tmem_st32(o_cols + c0, o);
         }
       }
-      // P over the first 32 columns of this step's S buffer, already read: the
-      // tensor-memory A operand of O += P V.  (Step j-2's P.V, the last reader of
-      // this buffer, retired before S of step j did.)
-      tmem_st32_raw(lane_base + kColS + (j & 1) * kKeys, packed);
+      // P over the first kKeys / 2 columns of the S buffer, already read: the
+      // tensor-memory A operand of O += P V.
+      tmem_st32_raw(s_cols, *reinterpret_cast<const uint32_t(*)[32]>(&packed[0]));
+      tmem_st32_raw(s_cols + 32, *reinterpret_cast<const uint32_t(*)[32]>(&packed[32]));
       asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       tc_before_sync();
-      bar_arrive(p_full + 8 * (j & 1));
+      bar_arrive(p_full + 8 * t);
     }
     // Epilogue: O / l, bf16, one 2*D-byte row per thread.
-    if (!failed && __all_sync(0xffffffffu, bar_wait(o_full, 0))) {
+    if (!failed && __all_sync(0xffffffffu, bar_wait(o_full + 8 * t, 0))) {
       tc_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
       uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
@@ -581,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         float o[32];
-        tmem_ld32(lane_base + kColO + c0, o);
+        tmem_ld32(o_cols + c0, o);
         if (row_ok) {
 #pragma unroll
           for (int x = 0; x < 32; x += 8)
@@ -596,10 +612,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (failed && lane == 0) atomicOr(p.err, kErrTimeout);
   }
 
-  // Everyone done with TMEM (the MMA warp's last commit arrived before o_full).
+  // Everyone done with TMEM (each MMA warp drained its own MMAs).
   tc_before_sync();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp0) {
     tc_after_sync();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
@@ -645,7 +661,7 @@ cudaError_t cache_map(CUtensorMap* map, const void* cache, int64_t rows, int hea
 
 template <int D, int G>
 cudaError_t launch_t(const PrefillParams& p, int max_query_len, cudaStream_t stream) {
-  constexpr int kTokens = kRows / G;
+  constexpr int kCtaTokens = kTiles * kRows / G;
   static std::mutex mu;
   static uint64_t ready = 0;
   int dev = 0;
@@ -663,7 +679,7 @@ cudaError_t launch_t(const PrefillParams& p, int max_query_len, cudaStream_t str
   const int64_t rows = p.num_blocks * p.num_kv_heads * kBlockTokens;
   if ((e = cache_map(&mk, p.k_cache, rows, D)) != cudaSuccess) return e;
   if ((e = cache_map(&mv, p.v_cache, rows, D)) != cudaSuccess) return e;
-  const dim3 grid((max_query_len + kTokens - 1) / kTokens, p.num_kv_heads, p.num_seqs);
+  const dim3 grid((max_query_len + kCtaTokens - 1) / kCtaTokens, p.num_kv_heads, p.num_seqs);
   paged_prefill_kernel<D, G><<<grid, kThreads, Pf<D>::kSmem, stream>>>(p, mk, mv);
   return cudaGetLastError();
 }
