@@ -11,18 +11,18 @@
 // sequence).  The 128 MMA rows of a tile pack 128/G chunk tokens x the G q heads
 // of the group; the CTA's two tiles cover consecutive tokens and share every K/V
 // tile.  Keys advance 128 at a time (8 pages of 16), so S = Q K^T is an N = 128
-// MMA and O += P V an N = D one: one thread issues a tcgen05.mma no faster than
-// about one per hundred cycles whatever its N, so the MMAs are made wide and each
-// tile has its own issuing warp.
+// MMA and O += P V an N = D one: at N = 64 an MMA is bound by reading its
+// operands from shared memory, at N = 128 by the math.
 //   * warp 8: TMA producer.  Each page half (16 tokens x 64 dims) is a 2D
 //     tensor-map copy with 128-byte swizzle, gathered through the block table into
 //     a K ring (3 slots) and a V ring (2 slots), one copy per lane; mbarrier
 //     completion by transaction bytes.  It also zeroes the rows of the last V
 //     tile past the end of the keys.
-//   * warps 9 + t (one lane): MMA issuer of tile t.  tcgen05.mma kind::f16 (bf16
-//     in, fp32 accumulate): S = Q_t K^T into the tile's TMEM S buffer (M 128,
-//     N 128), then, once the softmax has written P over S, O_t += P V (M 128,
-//     N = D, P read from TMEM); commits to mbarriers.  Warp 9 also allocates and
+//   * warp 9 (one lane): MMA issuer.  tcgen05.mma kind::f16 (bf16 in, fp32
+//     accumulate): S = Q_t K^T into tile t's TMEM S buffer (M 128, N 128); once
+//     the softmax has written P over S, O_t += P V (M 128, N = D, P read from
+//     TMEM) and at once S of the next step.  The two tiles alternate, so one
+//     tile's softmax overlaps the other's MMAs.  The warp also allocates and
 //     frees the 512 TMEM columns.
 //   * warps 0-7 (one row each; warps 4t..4t+3 serve tile t, each warp the TMEM
 //     lanes 32 (warp % 4) .. + 31): stage Q, then per key step read S
@@ -57,8 +57,8 @@ constexpr int kKeys = 128;    // keys per step (MMA N of S, MMA K of P.V)
 constexpr int kKStages = PKV_PF_KSTAGES;  // K ring depth
 constexpr int kVStages = PKV_PF_VSTAGES;  // V ring depth
 constexpr int kProducerWarp = 4 * kTiles;  // warps 0-7 softmax (four per tile)
-constexpr int kMmaWarp0 = kProducerWarp + 1;  // one MMA-issuing warp per tile
-constexpr int kThreads = 32 * (kMmaWarp0 + kTiles);
+constexpr int kMmaWarp = kProducerWarp + 1;
+constexpr int kThreads = 32 * (kMmaWarp + 1);
 constexpr int kTmemCols = 512;  // per tile t: S at [256 t, 256 t + 128), O at [256 t + 128, 256 t + 128 + D)
 __host__ __device__ constexpr int col_s(int t) { return 256 * t; }  // P (bf16 pairs) over the first 64 of S
 __host__ __device__ constexpr int col_o(int t) { return 256 * t + 128; }
@@ -151,19 +151,22 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int n, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) | ((static_cast<uint32_t>(n) >> 3) << 17) |
          ((128u >> 4) << 24);
 }
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+// The instruction descriptor is an immediate operand.
+template <uint32_t kIdesc>
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(acc)
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %3, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %4, p;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(acc), "n"(kIdesc)
       : "memory");
 }
 // Same, with A read from tensor memory (128 lanes = rows, K along the columns as bf16 pairs).
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t acc) {
+template <uint32_t kIdesc>
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t acc) {
   asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %3, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(acc), "n"(kIdesc)
       : "memory");
 }
 __device__ __forceinline__ void mma_commit(uint32_t b) {
@@ -323,11 +326,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kKStages; ++s) {
       bar_init(k_full + 8 * s, 1);
-      bar_init(k_empty + 8 * s, n_tiles);
+      bar_init(k_empty + 8 * s, 1);
     }
     for (int s = 0; s < kVStages; ++s) {
       bar_init(v_full + 8 * s, 1);
-      bar_init(v_empty + 8 * s, n_tiles);
+      bar_init(v_empty + 8 * s, 1);
     }
     bar_init(v_tail, 1);
     for (int t = 0; t < kTiles; ++t) {
@@ -339,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == kMmaWarp0) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(saddr(tmem_slot)),
                  "r"(kTmemCols)
                  : "memory");
@@ -441,61 +444,84 @@ __global__ void __launch_bounds__(kThreads, 1)
         bar_wait(v_full + 8 * (j % kVStages), (j / kVStages) & 1);
     }
     __syncwarp();
-  } else if (warp >= kMmaWarp0) {
-    // ---------------- MMA issuers: warp kMmaWarp0 + t serves tile t ----------------
-    // Step j: S = Q_t K_j^T (N = 128 keys), wait for P, then O_t += P V_j (N = D).
-    const int t = warp - kMmaWarp0;
-    if (t < n_tiles) {
-      constexpr uint32_t kIdS = idesc_bf16(kKeys, false);
-      constexpr uint32_t kIdPV = idesc_bf16(D, true);
-      const uint32_t d_s = tmem + col_s(t), d_o = tmem + col_o(t);
+  } else if (warp == kMmaWarp) {
+    // ---------------- MMA issuer (one lane) ----------------
+    // Ping-pong over the two tiles: S of both for step 0, then per step j and tile
+    // t: O_t += P_t V_j as soon as P_t is ready, followed at once by S_t of step
+    // j + 1.  The tensor pipe runs one tile's MMAs while the other tile's softmax
+    // runs.  S = Q K^T is N = 128 keys, P V is N = D.
+    constexpr uint32_t kIdS = idesc_bf16(kKeys, false);
+    constexpr uint32_t kIdPV = idesc_bf16(D, true);
+    auto issue_s = [&](int t, int j) {  // lane 0
+      const uint32_t kt = s_base + T::kOffK + (j % kKStages) * T::kTile;
       const uint32_t qt = s_base + T::kOffQ + t * T::kQTile;
+#pragma unroll
+      for (int h = 0; h < T::kHalves; ++h)
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_bf16<kIdS>(tmem + col_s(t), sdesc(qt + h * T::kQHalf + kk * 32), sdesc(kt + h * T::kKVHalf + kk * 32),
+                         (h | kk) != 0);
+      mma_commit(s_full + 8 * t);
+    };
+    for (int t = 0; t < n_tiles; ++t)
       if (!bar_wait(q_ready + 8 * t, 0)) failed = true;
-      tc_after_sync();
-      for (int j = 0; j < nsteps && !failed; ++j) {
-        const int sk = j % kKStages, sv = j % kVStages;
-        if (!bar_wait(k_full + 8 * sk, (j / kKStages) & 1)) {
-          failed = true;
-          break;
-        }
-        if (lane == 0) {
-          tc_after_sync();
-          const uint32_t kt = s_base + T::kOffK + sk * T::kTile;
-#pragma unroll
-          for (int h = 0; h < T::kHalves; ++h)
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-              mma_bf16(d_s, sdesc(qt + h * T::kQHalf + kk * 32), sdesc(kt + h * T::kKVHalf + kk * 32), kIdS,
-                       (h | kk) != 0);
-          mma_commit(s_full + 8 * t);
-          mma_commit(k_empty + 8 * sk);  // the K slot frees once every tile's S has retired
-        }
-        __syncwarp();
-        const bool last = j == nsteps - 1;
-        if (!bar_wait(p_full + 8 * t, j & 1) ||
-            !(last && tail ? bar_wait(v_tail, 0) : bar_wait(v_full + 8 * sv, (j / kVStages) & 1))) {
-          failed = true;
-          break;
-        }
-        if (lane == 0) {
-          tc_after_sync();
-          const uint32_t vt = s_base + T::kOffV + sv * T::kTile;
-#pragma unroll
-          for (int kk = 0; kk < kKeys / 16; ++kk)
-            mma_bf16_ts(d_o, d_s + kk * 8, sdesc(vt + kk * 16 * 128, T::kKVHalf), kIdPV, (j | kk) != 0);
-          mma_commit(v_empty + 8 * sv);
-          if (last) mma_commit(o_full + 8 * t);
-        }
-        __syncwarp();
-      }
-      if (failed && lane == 0) atomicOr(p.err, kErrTimeout);
-      // Every MMA this warp issued must have completed before the TMEM is freed.
+    if (!failed && !bar_wait(k_full, 0)) failed = true;
+    if (!failed) {
       if (lane == 0) {
-        mma_commit(mma_drained + 8 * t);
-        bar_wait(mma_drained + 8 * t, 0);
+        tc_after_sync();
+        for (int t = 0; t < n_tiles; ++t) issue_s(t, 0);
+        mma_commit(k_empty);
       }
       __syncwarp();
     }
+    for (int j = 0; j < nsteps && !failed; ++j) {
+      const int sv = j % kVStages;
+      const bool last = j == nsteps - 1;
+      if (!(last && tail ? bar_wait(v_tail, 0) : bar_wait(v_full + 8 * sv, (j / kVStages) & 1))) {
+        failed = true;
+        break;
+      }
+      const uint32_t vt = s_base + T::kOffV + sv * T::kTile;
+      for (int t = 0; t < n_tiles && !failed; ++t) {
+        if (!bar_wait(p_full + 8 * t, j & 1)) {
+          failed = true;
+          break;
+        }
+        if (lane == 0) {
+          tc_after_sync();
+          const uint32_t d_s = tmem + col_s(t);
+#pragma unroll
+          for (int kk = 0; kk < kKeys / 16; ++kk)
+            mma_bf16_ts<kIdPV>(tmem + col_o(t), d_s + kk * 8, sdesc(vt + kk * 16 * 128, T::kKVHalf), (j | kk) != 0);
+          if (last) mma_commit(o_full + 8 * t);
+        }
+        __syncwarp();
+        if (!last) {
+          if (t == 0 && !bar_wait(k_full + 8 * ((j + 1) % kKStages), ((j + 1) / kKStages) & 1)) {
+            failed = true;
+            break;
+          }
+          if (lane == 0) {
+            tc_after_sync();
+            issue_s(t, j + 1);  // overwrites P only after the P.V above (same issuer, in order)
+          }
+          __syncwarp();
+        }
+      }
+      if (failed) break;
+      if (lane == 0) {
+        mma_commit(v_empty + 8 * sv);
+        if (!last) mma_commit(k_empty + 8 * ((j + 1) % kKStages));  // both tiles' S of step j + 1 are in
+      }
+      __syncwarp();
+    }
+    if (failed && lane == 0) atomicOr(p.err, kErrTimeout);
+    // Every MMA this warp issued must have completed before the TMEM is freed.
+    if (lane == 0) {
+      mma_commit(mma_drained);
+      bar_wait(mma_drained, 0);
+    }
+    __syncwarp();
   } else if ((warp >> 2) < n_tiles) {
     // ---------------- softmax / epilogue (warps 0-7, thread = row of tile warp / 4) ----------------
     const int t = warp >> 2;
@@ -612,10 +638,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (failed && lane == 0) atomicOr(p.err, kErrTimeout);
   }
 
-  // Everyone done with TMEM (each MMA warp drained its own MMAs).
+  // Everyone done with TMEM (the MMA warp drained its MMAs).
   tc_before_sync();
   __syncthreads();
-  if (warp == kMmaWarp0) {
+  if (warp == kMmaWarp) {
     tc_after_sync();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
