@@ -197,6 +197,12 @@ __device__ __forceinline__ void tmem_ld64(uint32_t taddr, float (&v)[64]) {
 #pragma unroll
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
 // 2^x on the SFU (approximate, flush-to-zero): the softmax weights.
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
@@ -566,15 +572,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int x = 0; x < kKeys; ++x) s[x] = (j * kKeys + x) < limit ? s[x] : -INFINITY;
       }
-      // Row max as a tree.
-      float mx[kKeys / 2];
+      // Row max: eight chains of three-input maxima, then their maximum.
+      static_assert(kKeys % 8 == 0 && kKeys >= 24, "row max layout");
+      float mc[8];
 #pragma unroll
-      for (int x = 0; x < kKeys / 2; ++x) mx[x] = fmaxf(s[2 * x], s[2 * x + 1]);
+      for (int k = 0; k < 8; ++k) mc[k] = fmax3(s[k], s[k + 8], s[k + 16]);
+      constexpr int kPairsEnd = 24 + ((kKeys - 24) / 16) * 16;
 #pragma unroll
-      for (int w = kKeys / 4; w >= 1; w /= 2)
+      for (int x = 24; x < kPairsEnd; x += 16)
 #pragma unroll
-        for (int x = 0; x < w; ++x) mx[x] = fmaxf(mx[x], mx[x + w]);
-      const float bm = mx[0] * qk;  // the scale is positive: the max of the scaled scores
+        for (int k = 0; k < 8; ++k) mc[k] = fmax3(mc[k], s[x + k], s[x + 8 + k]);
+      if constexpr (kPairsEnd < kKeys) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mc[k] = fmaxf(mc[k], s[kPairsEnd + k]);
+      }
+      const float row_max = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
+      const float bm = row_max * qk;  // the scale is positive: the max of the scaled scores
       const bool raise = row_ok && bm > m_used + kSlack;
       const float m_new = raise ? bm : m_used;
       const float alpha = raise ? ex2_approx(m_used - m_new) : 1.f;  // 0 on the first raise
@@ -582,14 +595,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       float2 acc4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                         make_float2(0.f, 0.f)};
       uint32_t packed[kKeys / 2];
+      const float2 qk2 = make_float2(qk, qk), neg_m2 = make_float2(neg_m, neg_m);
 #pragma unroll
       for (int x = 0; x < kKeys; x += 2) {
-        const float p0 = ex2_approx(fmaf(s[x], qk, neg_m));
-        const float p1 = ex2_approx(fmaf(s[x + 1], qk, neg_m));
+        // Paired fp32 arithmetic (one FFMA2 / FADD2 per two keys); the denominator
+        // sums the fp32 weights, within 2^-9 relative of the bf16 ones P carries.
+        const float2 e = __ffma2_rn(make_float2(s[x], s[x + 1]), qk2, neg_m2);
+        const float p0 = ex2_approx(e.x), p1 = ex2_approx(e.y);
         packed[x / 2] = pack_bf16(p0, p1);
-        // The denominator sums the same bf16 values the MMA multiplies (four running sums).
-        acc4[(x / 2) & 3] = __fadd2_rn(acc4[(x / 2) & 3], make_float2(__uint_as_float(packed[x / 2] << 16),
-                                                                      __uint_as_float(packed[x / 2] & 0xffff0000u)));
+        acc4[(x / 2) & 3] = __fadd2_rn(acc4[(x / 2) & 3], make_float2(p0, p1));
       }
       const float2 a01 = __fadd2_rn(acc4[0], acc4[1]), a23 = __fadd2_rn(acc4[2], acc4[3]);
       const float2 a = __fadd2_rn(a01, a23);
