@@ -17,6 +17,8 @@ constexpr int kThreads = 256;
 constexpr int kUnroll = 4;
 
 __global__ void __launch_bounds__(kThreads) copy_blocks_kernel(const CopyParams p) {
+  pdl_trigger();
+  pdl_wait();
   const int pair = blockIdx.x >> 1;
   const int64_t src = p.src_dst[2 * pair];
   const int64_t dst = p.src_dst[2 * pair + 1];
@@ -42,8 +44,7 @@ __global__ void __launch_bounds__(kThreads) copy_blocks_kernel(const CopyParams 
 }  // namespace
 
 cudaError_t launch_copy_blocks(const CopyParams& p, int num_pairs, cudaStream_t stream) {
-  copy_blocks_kernel<<<static_cast<unsigned>(num_pairs) * 2u, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(copy_blocks_kernel, dim3(static_cast<unsigned>(num_pairs) * 2u), dim3(kThreads), 0, stream, p);
 }
 
 }  // namespace pkv

@@ -25,6 +25,8 @@ __device__ __forceinline__ uint4 load_stream(const uint4* p) {
 }
 
 __global__ void __launch_bounds__(256) kv_append_kernel(const AppendParams p) {
+  pdl_trigger();
+  pdl_wait();
   const int chunks_per_row = p.head_dim / 8;                    // 16-byte chunks per (token, head) row
   const int chunks_per_token = p.num_kv_heads * chunks_per_row;
   const int64_t total = p.num_tokens * chunks_per_token;
@@ -63,8 +65,7 @@ cudaError_t launch_kv_append(const AppendParams& p, int num_sms, cudaStream_t st
   const int64_t cap = static_cast<int64_t>(num_sms) * 8;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  kv_append_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(kv_append_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, stream, p);
 }
 
 }  // namespace pkv

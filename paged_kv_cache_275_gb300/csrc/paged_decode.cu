@@ -385,6 +385,8 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  pdl_trigger();
+  pdl_wait();
 
   // --- CTA prologue: clamp lengths, block prefix over sequences -------------
   if (tid == 0) s_prefix[0] = 0;
@@ -695,6 +697,8 @@ __global__ void __launch_bounds__(G * 32) paged_decode_merge_kernel(const Decode
   const int kvh = blockIdx.x - b * hkv;
   const int g = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  pdl_trigger();
+  pdl_wait();
   const int* prefix = p.ws_prefix;
   const int nblk = prefix[b + 1] - prefix[b];
   __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
@@ -801,15 +805,13 @@ struct Instance {
     if (e != cudaSuccess) return e;
     if ((e = prepare(dev)) != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>((p.num_partitions + NW - 1) / NW);
-    paged_decode_partition_kernel<D, G, NW, S>
-        <<<grid, NW * 32, partition_smem_bytes<D, G>(p.num_seqs), stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(paged_decode_partition_kernel<D, G, NW, S>, dim3(grid), dim3(NW * 32),
+                      partition_smem_bytes<D, G>(p.num_seqs), stream, p);
   }
 
   static cudaError_t merge(const DecodeParams& p, cudaStream_t stream) {
     const unsigned grid = static_cast<unsigned>(p.num_seqs) * static_cast<unsigned>(p.num_kv_heads);
-    paged_decode_merge_kernel<D, G><<<grid, G * 32, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(paged_decode_merge_kernel<D, G>, dim3(grid), dim3(G * 32), 0, stream, p);
   }
 };
 

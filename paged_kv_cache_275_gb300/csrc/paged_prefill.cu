@@ -259,6 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kCtaTokens = kTiles * kTokens;  // chunk tokens per CTA
   extern __shared__ __align__(1024) unsigned char smem[];
   const uint32_t s_base = saddr(smem);
+  pdl_trigger();
+  pdl_wait();
 
   const int tile = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);  // longest tiles first
   const int kvh = blockIdx.y;
@@ -720,8 +722,7 @@ cudaError_t launch_t(const PrefillParams& p, int max_query_len, cudaStream_t str
   if ((e = cache_map(&mk, p.k_cache, rows, D)) != cudaSuccess) return e;
   if ((e = cache_map(&mv, p.v_cache, rows, D)) != cudaSuccess) return e;
   const dim3 grid((max_query_len + kCtaTokens - 1) / kCtaTokens, p.num_kv_heads, p.num_seqs);
-  paged_prefill_kernel<D, G><<<grid, kThreads, Pf<D>::kSmem, stream>>>(p, mk, mv);
-  return cudaGetLastError();
+  return launch_pdl(paged_prefill_kernel<D, G>, grid, dim3(kThreads), Pf<D>::kSmem, stream, p, mk, mv);
 }
 
 }  // namespace

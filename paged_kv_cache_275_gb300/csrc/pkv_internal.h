@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include <cuda_runtime.h>
 
@@ -58,6 +59,34 @@ struct DecodeParams {
   const float* cos_sin;  // fp32 [max_position][head_dim] (cos | sin) or null: no RoPE
   int64_t max_position;
 };
+
+// Programmatic dependent launch.  Every kernel of this library is launched with
+// programmatic stream serialization: it may start (and run its prologue) while
+// the previous kernel in the stream drains, and it executes pdl_wait() before
+// its first access to global memory, which returns once that kernel has
+// completed and its writes are visible.  Each kernel also calls pdl_trigger()
+// on entry so that the next one can be scheduled early.  Launched after
+// anything else (a copy, another library's kernel) the launch is an ordinary
+// stream-ordered one.
+template <typename... Params, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem_bytes, cudaStream_t stream,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+#endif
 
 // Set the per-host-thread message returned by pkv_last_error_message().
 void set_error_message(const char* message);
