@@ -76,6 +76,20 @@ def test_prefill_chunks_of_one_match_decode():
     assert_close(dec, ref, "decode on the same rows")
 
 
+@pytest.mark.parametrize("num_seqs", [320, 321])
+def test_prefill_many_sequences_either_side_of_the_ranking_limit(num_seqs):
+    """Up to 320 sequences each CTA ranks them by length to pick its own; beyond that the grid takes
+    them in index order.  Both orders must give the oracle's result."""
+    import random
+    rng = random.Random(num_seqs)
+    chunks = tuple(rng.randint(1, 24) for _ in range(num_seqs))
+    spec = PrefillSpec("many", "", 8, 2, 64, chunks, (0, 100), 9)
+    c = make_prefill_case(spec, seed=num_seqs)
+    _, out = _run(c)
+    assert_close(out, _ref(c), f"{num_seqs} sequences")
+    assert device_errors() == 0
+
+
 def test_prefill_poisoned_unused_slots_do_not_leak():
     c = make_prefill_case("prefill_tiny", seed=8)
     _, clean = _run(c)
