@@ -54,6 +54,9 @@ L2_BYTES = 126 * 2 ** 20
 KERNEL_SOURCES = {
     "paged_decode_partition_kernel": ("paged_kv_cache_275_gb300/csrc/paged_decode.cu",
                                       "paged_kv_cache_275_gb300/csrc/pkv_internal.h"),
+    "paged_prefill_kernel": ("paged_kv_cache_275_gb300/csrc/paged_prefill.cu",
+                             "paged_kv_cache_275_gb300/csrc/paged_prefill.h",
+                             "paged_kv_cache_275_gb300/csrc/pkv_internal.h"),
 }
 
 
@@ -76,6 +79,17 @@ def recorded_traffic(kernel: str, workload: str) -> float | None:
         if len(f) >= 4 and not line.startswith("#") and f[0] == kernel and f[1] == workload and f[2] == want:
             return float(f[3])
     return None
+
+
+def prefill_compulsory_bytes(c) -> int:
+    """Bytes a prefill launch must move at least: q and out, plus every cached K/V row its queries see
+    (each (sequence, kv head) row read once) and the block-table entries."""
+    lens = c.context_lens.cpu().tolist()
+    hkv, d = c.spec.num_kv_heads, c.spec.head_dim
+    qo = 2 * c.q.numel() * c.q.element_size()
+    kv = sum(2 * L * hkv * d * 2 for L in lens)
+    tables = sum(4 * ((L + 15) // 16) for L in lens)
+    return int(qo + kv + tables)
 
 
 def bf16_peak_tflops() -> tuple[float, str]:
@@ -658,7 +672,11 @@ def run_component(args) -> dict:
                            "context_lens": c.context_lens.tolist()},
                 "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": bf16_peak, "unit": "TFLOP/s",
                              "frac": round(tf / bf16_peak, 4), "frac_of": f"{kind} bf16 dense (cuBLAS burst)",
-                             "algorithmic_flops_per_launch": flops, "traffic": None}}
+                             "algorithmic_flops_per_launch": flops,
+                             "traffic": recorded_traffic("paged_prefill_kernel", "prefill_llama3_8b"),
+                             "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, profiles/traffic.txt "
+                                               f"(kernel source {source_hash('paged_prefill_kernel')})",
+                             "compulsory_bytes_per_launch": prefill_compulsory_bytes(c)}}
     # copy_blocks: copy-on-write of 4096 distinct block pairs of the Qwen3/LLaMA-3 kv layout.
     dev = torch.device("cuda", 0)
     g = make_generator(7)
