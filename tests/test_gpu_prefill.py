@@ -90,6 +90,15 @@ def test_prefill_many_sequences_either_side_of_the_ranking_limit(num_seqs):
     assert device_errors() == 0
 
 
+def test_prefill_long_prefix():
+    """A 20000-token prefix: about 160 key steps and 1250 pages, so the block-id window slides ~40 times."""
+    spec = PrefillSpec("long", "", 8, 2, 128, (16, 3, 200), (0, 0), 1270)
+    c = make_prefill_case(spec, seed=12, prefixes=[20000, 5000, 300])
+    _, out = _run(c)
+    assert_close(out, _ref(c), "long prefix")
+    assert device_errors() == 0
+
+
 def test_prefill_poisoned_unused_slots_do_not_leak():
     c = make_prefill_case("prefill_tiny", seed=8)
     _, clean = _run(c)
