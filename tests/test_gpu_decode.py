@@ -94,6 +94,30 @@ def test_every_length_through_three_blocks():
     assert device_errors() == 0
 
 
+@pytest.mark.parametrize("seed", range(8))
+def test_random_shapes(seed):
+    """Seeded random layouts, batch sizes, length mixes (empty to a few thousand tokens) and
+    partition counts (the default, one, and a random count that may exceed the work)."""
+    import random
+    rng = random.Random(3000 + seed)
+    d = rng.choice([64, 128])
+    hkv = rng.choice([1, 2, 4, 8])
+    g = rng.choice([1, 2, 4, 8])
+    b = rng.randint(1, 40)
+    lens = tuple(rng.choice([0, rng.randint(1, 48), rng.randint(48, 3000)]) for _ in range(b))
+    width = max(1, max(-(-L // BLOCK_SIZE) for L in lens)) + rng.randint(0, 3)
+    spec = DecodeSpec(name="random", description="", num_seqs=b, num_q_heads=hkv * g, num_kv_heads=hkv,
+                      head_dim=d, max_blocks_per_seq=width, length_kind="fixed", lengths=lens,
+                      pool_slack=rng.choice([0.0, 0.3]))
+    c = make_decode_case(spec, seed=4000 + seed)
+    c.slot_mapping[c.context_lens == 0] = -1
+    ref, _, _ = oracle_step(c)
+    for parts in (0, 1, rng.randint(2, 3000)):
+        _, out = _run(c, parts)
+        assert_close(out, ref, f"seed {seed}: D{d} {hkv * g}/{hkv} B{b} parts {parts}")
+    assert device_errors() == 0
+
+
 # ---------------------------------------------------------------------------
 # Invariants and special cases
 # ---------------------------------------------------------------------------

@@ -99,6 +99,26 @@ def test_prefill_long_prefix():
     assert device_errors() == 0
 
 
+@pytest.mark.parametrize("seed", range(8))
+def test_prefill_random_shapes(seed):
+    """Seeded random layouts: head dim, group size, sequence count, chunk and prefix lengths (chunks from
+    one token to several CTAs, prefixes from none to a few thousand tokens)."""
+    import random
+    rng = random.Random(1000 + seed)
+    d = rng.choice([64, 128])
+    hkv = rng.choice([1, 2, 4, 8])
+    g = rng.choice([1, 2, 4, 8])
+    b = rng.randint(1, 12)
+    chunks = tuple(rng.choice([1, rng.randint(1, 40), rng.randint(40, 300)]) for _ in range(b))
+    prefixes = [rng.choice([0, rng.randint(0, 64), rng.randint(64, 3000)]) for _ in range(b)]
+    width = max(-(-(p_ + c_) // BLOCK_SIZE) for p_, c_ in zip(prefixes, chunks)) + rng.randint(0, 3)
+    spec = PrefillSpec("random", "", hkv * g, hkv, d, chunks, (0, 0), width)
+    c = make_prefill_case(spec, seed=2000 + seed, prefixes=prefixes)
+    _, out = _run(c)
+    assert_close(out, _ref(c), f"seed {seed}: D{d} {hkv * g}/{hkv} chunks {chunks} prefixes {prefixes}")
+    assert device_errors() == 0
+
+
 def test_prefill_poisoned_unused_slots_do_not_leak():
     c = make_prefill_case("prefill_tiny", seed=8)
     _, clean = _run(c)
