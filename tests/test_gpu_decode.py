@@ -241,6 +241,23 @@ def test_bad_block_id_and_lengths_are_flagged():
     assert device_errors() == 0
 
 
+def test_largest_batch():
+    """num_seqs = PKV_MAX_SEQS (4096) short sequences, empty ones among them: every CTA ranks and
+    prefixes the whole batch in shared memory."""
+    import random
+    rng = random.Random(77)
+    lens = tuple(rng.choice([0, rng.randint(1, 40)]) for _ in range(pkv.MAX_SEQS))
+    spec = DecodeSpec(name="max_batch", description="", num_seqs=pkv.MAX_SEQS, num_q_heads=8, num_kv_heads=2,
+                      head_dim=64, max_blocks_per_seq=3, length_kind="fixed", lengths=lens, pool_slack=0.1)
+    c = make_decode_case(spec, seed=78)
+    c.slot_mapping[c.context_lens == 0] = -1
+    ref, _, _ = oracle_step(c)
+    for parts in (0, 1000):
+        _, out = _run(c, parts)
+        assert_close(out, ref, f"4096 sequences parts {parts}")
+    assert device_errors() == 0
+
+
 def test_host_errors_raise_before_launch():
     c = make_decode_case("tiny", seed=15).to("cuda")
     before = pkv.kernel_launch_count()
