@@ -272,11 +272,21 @@ def cpu_baseline(case_cpu, target_s: float = 10.0, max_s: float = 30.0) -> dict:
         if el >= target_s or el + times[-1] > max_s:
             break
     total = sum(times)
+    # One thread as well, on a bounded sample of the same step (the first n sequences, ~3 s).
+    lens = case_cpu.context_lens.tolist()
+    probe = make_decode_case(case_cpu.spec.name, seed=0, lengths=lens[:8])
+    per_seq = oracle_step_seconds(probe, 1) / 8
+    n = max(1, min(len(lens), int(3.0 / max(per_seq, 1e-9))))
+    one = make_decode_case(case_cpu.spec.name, seed=0, lengths=lens[:n])
+    t1 = oracle_step_seconds(one, 1)
     return {"value": round(b * len(times) / total / 1e9, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
             "sample": f"the full {case_cpu.spec.name} step (append + attention, all {case_cpu.spec.num_seqs} "
                       f"sequences x {case_cpu.spec.num_q_heads} q heads) repeated {len(times)} times, fp64, "
                       f"{threads} threads, {total:.1f} s",
-            "seconds_per_step": round(total / len(times), 4)}
+            "seconds_per_step": round(total / len(times), 4),
+            "single_thread": {"value": round(step_bytes(one) / t1 / 1e9, 4), "unit": UNIT, "cores": 1,
+                              "sample": f"the first {n} sequences of the same step (all q heads), one thread, "
+                                        f"{t1:.1f} s"}}
 
 
 def run_reference(args, dist: Dist) -> dict | None:
