@@ -7,8 +7,9 @@
 // the chunk already appended); query row i of the chunk attends causally over
 // the first P_b + i + 1 tokens: out = softmax(scale * q K^T) V.
 //
-// How (GB300-first).  One CTA per SM, per (pair of 128-row query tiles, kv head,
-// sequence).  The 128 MMA rows of a tile pack 128/G chunk tokens x the G q heads
+// How (GB300-first).  One CTA per (pair of 128-row query tiles, kv head, sequence),
+// each holding a whole SM (all 512 TMEM columns), launched longest first.  The 128
+// MMA rows of a tile pack 128/G chunk tokens x the G q heads
 // of the group; the CTA's two tiles cover consecutive tokens and share every K/V
 // tile.  Keys advance 128 at a time (8 pages of 16), so S = Q K^T is an N = 128
 // MMA and O += P V an N = D one: at N = 64 an MMA is bound by reading its
