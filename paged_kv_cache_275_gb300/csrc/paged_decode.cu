@@ -107,28 +107,35 @@ struct Geo {
   }
 };
 
-// Launch shape per head_dim (warps per CTA, ring stages per warp); overridable at build time.
-#ifndef PKV_D128_WARPS
-#define PKV_D128_WARPS 4
-#endif
-#ifndef PKV_D128_STAGES
-#define PKV_D128_STAGES 3
-#endif
+// Launch shape per (head_dim, group): warps per CTA and ring stages per warp.  At
+// D = 128 a group of up to two q heads does little arithmetic per byte, and eight
+// warps with two stages each keep more copies moving (measured on the Qwen3-shape
+// trace: 6.20 against 5.76 TB/s); from four q heads on, four warps with three
+// stages are faster (LLaMA-3 shape: 201.6 against 209.6 us).  The macros override
+// the D = 128 shape for every group, for sweeps.
 #ifndef PKV_D64_WARPS
 #define PKV_D64_WARPS 4
 #endif
 #ifndef PKV_D64_STAGES
 #define PKV_D64_STAGES 4
 #endif
-template <int D>
+template <int D, int G>
 struct Shape;
-template <>
-struct Shape<128> {
+template <int G>
+struct Shape<128, G> {
+#ifdef PKV_D128_WARPS
   static constexpr int kWarps = PKV_D128_WARPS;
+#else
+  static constexpr int kWarps = G <= 2 ? 8 : 4;
+#endif
+#ifdef PKV_D128_STAGES
   static constexpr int kStages = PKV_D128_STAGES;
+#else
+  static constexpr int kStages = G <= 2 ? 2 : 3;
+#endif
 };
-template <>
-struct Shape<64> {
+template <int G>
+struct Shape<64, G> {
   static constexpr int kWarps = PKV_D64_WARPS;
   static constexpr int kStages = PKV_D64_STAGES;
 };
@@ -136,7 +143,7 @@ struct Shape<64> {
 template <int D, int G>
 constexpr size_t static_smem_bytes() {
   using T = Geo<D, G>;
-  constexpr int NW = Shape<D>::kWarps, S = Shape<D>::kStages;
+  constexpr int NW = Shape<D, G>::kWarps, S = Shape<D, G>::kStages;
   return size_t(NW) * S * T::kStageBytes + size_t(NW) * T::kPTileBytes + size_t(NW) * S * 8;
 }
 template <int D, int G>
@@ -760,8 +767,8 @@ __global__ void __launch_bounds__(G * 32) paged_decode_merge_kernel(const Decode
 // ---------------------------------------------------------------------------
 template <int D, int G>
 struct Instance {
-  static constexpr int NW = Shape<D>::kWarps;
-  static constexpr int S = Shape<D>::kStages;
+  static constexpr int NW = Shape<D, G>::kWarps;
+  static constexpr int S = Shape<D, G>::kStages;
   static void* partition_fn() { return reinterpret_cast<void*>(&paged_decode_partition_kernel<D, G, NW, S>); }
 
   static cudaError_t prepare(int dev) {
@@ -836,7 +843,10 @@ int piece_floats(int head_dim, int group) { return group * head_dim + ((2 * grou
 
 size_t workspace_header_bytes(int num_seqs) { return (static_cast<size_t>(num_seqs + 1) * 4 + 255) & ~size_t(255); }
 
-int partition_warps_per_cta(int head_dim, int) { return head_dim == 64 ? Shape<64>::kWarps : Shape<128>::kWarps; }
+int partition_warps_per_cta(int head_dim, int group) {
+  if (head_dim == 64) return Shape<64, 1>::kWarps;
+  return group <= 2 ? Shape<128, 2>::kWarps : Shape<128, 4>::kWarps;
+}
 
 cudaError_t resident_partition_warps(int head_dim, int group, int num_seqs, int* warps) {
   return dispatch(head_dim, group, [&](auto inst) { return decltype(inst)::resident_warps(num_seqs, warps); });
