@@ -108,11 +108,13 @@ struct Geo {
 };
 
 // Launch shape per (head_dim, group): warps per CTA and ring stages per warp.  At
-// D = 128 a group of up to two q heads does little arithmetic per byte, and eight
-// warps with two stages each keep more copies moving (measured on the Qwen3-shape
-// trace: 6.20 against 5.76 TB/s); from four q heads on, four warps with three
-// stages are faster (LLaMA-3 shape: 201.6 against 209.6 us).  The macros override
-// the D = 128 shape for every group, for sweeps.
+// D = 128, four q heads per kv head run best with four warps of three stages
+// (LLaMA-3 shape: 201.6 against 209.6 us with eight warps of two); every other group
+// size with eight warps of two stages: one or two heads do little arithmetic per
+// byte and more warps keep more copies moving (Qwen3-shape trace: 6.20 against
+// 5.76 TB/s), and eight heads need the registers of two passes and the larger q
+// rows of a stage (339 against 531 us on a 1.27 GB batch).  The macros override the
+// D = 128 shape for every group, for sweeps.
 #ifndef PKV_D64_WARPS
 #define PKV_D64_WARPS 4
 #endif
@@ -126,12 +128,12 @@ struct Shape<128, G> {
 #ifdef PKV_D128_WARPS
   static constexpr int kWarps = PKV_D128_WARPS;
 #else
-  static constexpr int kWarps = G <= 2 ? 8 : 4;
+  static constexpr int kWarps = G == 4 ? 4 : 8;
 #endif
 #ifdef PKV_D128_STAGES
   static constexpr int kStages = PKV_D128_STAGES;
 #else
-  static constexpr int kStages = G <= 2 ? 2 : 3;
+  static constexpr int kStages = G == 4 ? 3 : 2;
 #endif
 };
 template <int G>
@@ -377,7 +379,13 @@ __device__ __forceinline__ void advance(Cursor& cur, const int* s_prefix, int nu
 template <int D, int G, int NW, int S>
 __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const DecodeParams p) {
   using T = Geo<D, G>;
-  static_assert(T::valid(), "unsupported (head_dim, group) geometry");
+  // Heads are processed in sub-groups of at most four: a group of eight runs the
+  // four-head block routine twice per staged K/V tile (its state would not fit the
+  // registers in one pass), still reading every tile from HBM once.
+  constexpr int GS = G > 4 ? 4 : G;
+  constexpr int SUB = G / GS;
+  using TS = Geo<D, GS>;
+  static_assert(TS::valid() && G % GS == 0, "unsupported (head_dim, group) geometry");
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int s_wsum[32];
 
@@ -520,16 +528,16 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
     next_id = ids[S];
   }
 
-  const int c = lane & (T::kLanesPerToken - 1);
-  const int half = lane / T::kLanesPerToken;
-  const int mask = T::mask_of(c);
-  const int mg = mask % G;
+  const int c = lane & (TS::kLanesPerToken - 1);
+  const int half = lane / TS::kLanesPerToken;
+  const int mask = TS::mask_of(c);
+  const int mg = mask % GS;
   const float qscale = p.qscale;
 
-  float2 q[G][4];
-  float2 acc[G][4];
-  float m_ref[G];
-  float m_mine[T::kFinal], l_mine[T::kFinal];
+  float2 q[SUB][GS][4];  // q[sb][gp]: head sb * GS + (gp ^ mg), swizzled per lane
+  float2 acc[SUB][GS][4];  // acc[sb][g]: head sb * GS + g
+  float m_ref[SUB][GS];
+  float m_mine[SUB][TS::kFinal], l_mine[SUB][TS::kFinal];
   bool pair_from_start = false;
   bool first_pair = true;
 
@@ -559,23 +567,27 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
         cs_row = p.cos_sin + pos * D;
       }
 #pragma unroll
-      for (int gp = 0; gp < G; ++gp) {
-        uint4 w = lds128(sq + (gp ^ mg) * (D * 2) + c * 16);
-        if (cs_row != nullptr)
-          w = rope_chunk<D>(w, lds128(sq + (gp ^ mg) * (D * 2) + ((c * 16 + D) % (D * 2))), cs_row, c);
-        const float2 s2 = make_float2(qscale, qscale);
-        q[gp][0] = __fmul2_rn(bf16x2_to_float2(w.x), s2);
-        q[gp][1] = __fmul2_rn(bf16x2_to_float2(w.y), s2);
-        q[gp][2] = __fmul2_rn(bf16x2_to_float2(w.z), s2);
-        q[gp][3] = __fmul2_rn(bf16x2_to_float2(w.w), s2);
+      for (int sb = 0; sb < SUB; ++sb) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[gp][e] = make_float2(0.f, 0.f);
-        m_ref[gp] = -INFINITY;
-      }
+        for (int gp = 0; gp < GS; ++gp) {
+          const int head = sb * GS + (gp ^ mg);
+          uint4 w = lds128(sq + head * (D * 2) + c * 16);
+          if (cs_row != nullptr)
+            w = rope_chunk<D>(w, lds128(sq + head * (D * 2) + ((c * 16 + D) % (D * 2))), cs_row, c);
+          const float2 s2 = make_float2(qscale, qscale);
+          q[sb][gp][0] = __fmul2_rn(bf16x2_to_float2(w.x), s2);
+          q[sb][gp][1] = __fmul2_rn(bf16x2_to_float2(w.y), s2);
+          q[sb][gp][2] = __fmul2_rn(bf16x2_to_float2(w.z), s2);
+          q[sb][gp][3] = __fmul2_rn(bf16x2_to_float2(w.w), s2);
 #pragma unroll
-      for (int k = 0; k < T::kFinal; ++k) {
-        m_mine[k] = -INFINITY;
-        l_mine[k] = 0.f;
+          for (int e = 0; e < 4; ++e) acc[sb][gp][e] = make_float2(0.f, 0.f);
+          m_ref[sb][gp] = -INFINITY;
+        }
+#pragma unroll
+        for (int k = 0; k < TS::kFinal; ++k) {
+          m_mine[sb][k] = -INFINITY;
+          l_mine[sb][k] = 0.f;
+        }
       }
       pair_from_start = (cc.blk == 0);
     }
@@ -607,12 +619,16 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
       }
       __syncwarp();
     }
-    if (valid >= kBlockTokens)
-      process_block<D, G, false>(st_ptr, st_ptr + T::kTileBytes, ptile, q, acc, m_ref, m_mine, l_mine, c, half,
-                                 mask, kBlockTokens);
-    else
-      process_block<D, G, true>(st_ptr, st_ptr + T::kTileBytes, ptile, q, acc, m_ref, m_mine, l_mine, c, half,
-                                mask, valid);
+#pragma unroll
+    for (int sb = 0; sb < SUB; ++sb) {
+      if (sb > 0) __syncwarp();  // the p tile is rewritten for the next sub-group
+      if (valid >= kBlockTokens)
+        process_block<D, GS, false>(st_ptr, st_ptr + T::kTileBytes, ptile, q[sb], acc[sb], m_ref[sb], m_mine[sb],
+                                    l_mine[sb], c, half, mask, kBlockTokens);
+      else
+        process_block<D, GS, true>(st_ptr, st_ptr + T::kTileBytes, ptile, q[sb], acc[sb], m_ref[sb], m_mine[sb],
+                                   l_mine[sb], c, half, mask, valid);
+    }
     __syncwarp();
 
     // Refill the stage just consumed with block i + S.
@@ -629,22 +645,28 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
     if (last_of_pair || i == n - 1) {
       // Combine the token-parity lanes, then finish the pair or park its partial state.
 #pragma unroll
-      for (int off = T::kLanesPerToken; off < 32; off <<= 1)
+      for (int off = TS::kLanesPerToken; off < 32; off <<= 1)
 #pragma unroll
-        for (int g = 0; g < G; ++g)
+        for (int sb = 0; sb < SUB; ++sb)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            acc[g][e].x += __shfl_xor_sync(kFull, acc[g][e].x, off);
-            acc[g][e].y += __shfl_xor_sync(kFull, acc[g][e].y, off);
-          }
+          for (int g = 0; g < GS; ++g)
 #pragma unroll
-      for (int k = 0; k < T::kFinal; ++k)
+            for (int e = 0; e < 4; ++e) {
+              acc[sb][g][e].x += __shfl_xor_sync(kFull, acc[sb][g][e].x, off);
+              acc[sb][g][e].y += __shfl_xor_sync(kFull, acc[sb][g][e].y, off);
+            }
 #pragma unroll
-        for (int bit = 1; bit < 32; bit <<= 1)
-          if (T::sum_bits() & bit) l_mine[k] += __shfl_xor_sync(kFull, l_mine[k], bit);
-      float l_all[G];
+      for (int sb = 0; sb < SUB; ++sb)
 #pragma unroll
-      for (int g = 0; g < G; ++g) l_all[g] = __shfl_sync(kFull, l_mine[g % T::kFinal], T::src_lane(g));
+        for (int k = 0; k < TS::kFinal; ++k)
+#pragma unroll
+          for (int bit = 1; bit < 32; bit <<= 1)
+            if (TS::sum_bits() & bit) l_mine[sb][k] += __shfl_xor_sync(kFull, l_mine[sb][k], bit);
+      float l_all[SUB][GS];
+#pragma unroll
+      for (int sb = 0; sb < SUB; ++sb)
+#pragma unroll
+        for (int g = 0; g < GS; ++g) l_all[sb][g] = __shfl_sync(kFull, l_mine[sb][g % TS::kFinal], TS::src_lane(g));
 
       if (pair_from_start && last_of_pair) {
         if (half == 0) {
@@ -652,32 +674,38 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
                                                  (static_cast<size_t>(cc.b) * p.num_q_heads + cc.kvh * G) * D) +
                         c;
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            const float inv = 1.0f / l_all[g];
-            uint4 o;
-            o.x = float2_to_bf16x2(acc[g][0].x * inv, acc[g][0].y * inv);
-            o.y = float2_to_bf16x2(acc[g][1].x * inv, acc[g][1].y * inv);
-            o.z = float2_to_bf16x2(acc[g][2].x * inv, acc[g][2].y * inv);
-            o.w = float2_to_bf16x2(acc[g][3].x * inv, acc[g][3].y * inv);
-            orow[g * (D / 8)] = o;
-          }
+          for (int sb = 0; sb < SUB; ++sb)
+#pragma unroll
+            for (int g = 0; g < GS; ++g) {
+              const float inv = 1.0f / l_all[sb][g];
+              uint4 o;
+              o.x = float2_to_bf16x2(acc[sb][g][0].x * inv, acc[sb][g][0].y * inv);
+              o.y = float2_to_bf16x2(acc[sb][g][1].x * inv, acc[sb][g][1].y * inv);
+              o.z = float2_to_bf16x2(acc[sb][g][2].x * inv, acc[sb][g][2].y * inv);
+              o.w = float2_to_bf16x2(acc[sb][g][3].x * inv, acc[sb][g][3].y * inv);
+              orow[(sb * GS + g) * (D / 8)] = o;
+            }
         }
       } else {
         float* piece = p.ws_pieces + (static_cast<size_t>(gw) * 2 + (first_pair ? 0 : 1)) * T::kPieceFloats;
         if (half == 0) {
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            float4* dst = reinterpret_cast<float4*>(piece + g * D + c * 8);
-            dst[0] = make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
-            dst[1] = make_float4(acc[g][2].x, acc[g][2].y, acc[g][3].x, acc[g][3].y);
-          }
+          for (int sb = 0; sb < SUB; ++sb)
+#pragma unroll
+            for (int g = 0; g < GS; ++g) {
+              float4* dst = reinterpret_cast<float4*>(piece + (sb * GS + g) * D + c * 8);
+              dst[0] = make_float4(acc[sb][g][0].x, acc[sb][g][0].y, acc[sb][g][1].x, acc[sb][g][1].y);
+              dst[1] = make_float4(acc[sb][g][2].x, acc[sb][g][2].y, acc[sb][g][3].x, acc[sb][g][3].y);
+            }
         }
         if (lane == 0) {
 #pragma unroll
-          for (int g = 0; g < G; ++g) {
-            piece[G * D + g] = m_ref[g];
-            piece[G * D + G + g] = l_all[g];
-          }
+          for (int sb = 0; sb < SUB; ++sb)
+#pragma unroll
+            for (int g = 0; g < GS; ++g) {
+              piece[G * D + sb * GS + g] = m_ref[sb][g];
+              piece[G * D + G + sb * GS + g] = l_all[sb][g];
+            }
         }
       }
       first_pair = false;
@@ -845,7 +873,7 @@ size_t workspace_header_bytes(int num_seqs) { return (static_cast<size_t>(num_se
 
 int partition_warps_per_cta(int head_dim, int group) {
   if (head_dim == 64) return Shape<64, 1>::kWarps;
-  return group <= 2 ? Shape<128, 2>::kWarps : Shape<128, 4>::kWarps;
+  return group == 4 ? Shape<128, 4>::kWarps : Shape<128, 8>::kWarps;
 }
 
 cudaError_t resident_partition_warps(int head_dim, int group, int num_seqs, int* warps) {

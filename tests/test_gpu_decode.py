@@ -54,6 +54,16 @@ def test_llama3_layer_full():
     assert device_errors() == 0
 
 
+def test_llama3_70b_layer_full():
+    """Groups of eight q heads (64 q / 8 kv), which run in two four-head passes per K/V tile."""
+    c = make_decode_case("llama3_70b", seed=0)
+    ref, _, _ = oracle_step(c)
+    for parts in (0, 97):
+        _, out = _run(c, parts)
+        assert_close(out, ref, f"llama3_70b parts {parts}")
+    assert device_errors() == 0
+
+
 def test_long_context_skew_full():
     """Log-uniform lengths 16..65536 plus one 131072-token sequence (8192 blocks)."""
     c = make_decode_case("long_skew", seed=0)

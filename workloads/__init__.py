@@ -64,6 +64,10 @@ SPECS = {
         name="llama3_8b", description="LLaMA-3-8B layer: 32 q / 8 kv heads, D 128, B 128, L~U{512..4096}",
         num_seqs=128, num_q_heads=32, num_kv_heads=8, head_dim=128, max_blocks_per_seq=256,
         length_kind="uniform", length_range=(512, 4096)),
+    "llama3_70b": DecodeSpec(
+        name="llama3_70b", description="LLaMA-3-70B layer: 64 q / 8 kv heads, D 128, B 128, L~U{512..4096}",
+        num_seqs=128, num_q_heads=64, num_kv_heads=8, head_dim=128, max_blocks_per_seq=256,
+        length_kind="uniform", length_range=(512, 4096)),
     "long_skew": DecodeSpec(
         name="long_skew",
         description="long-context skew: 32 q / 8 kv heads, D 128, B 64, L log-uniform 16..65536, one seq 131072",
