@@ -12,9 +12,11 @@ bf16 N(0, 1) data from a seeded generator.
 Reported (one JSON line on rank 0):
   value       algorithmic GB/s of the step (attention + append bytes) with the
               inputs resident in HBM, device-timed with CUDA events;
-  e2e         the same metric through the public API with this step's inputs
-              copied from pinned host memory and the output read back, inside
-              the timed region;
+  e2e         the same metric through the public API with every step's inputs
+              copied from pinned host memory and its output read back, inside
+              the timed region; the copies run on their own streams, double-
+              buffered, overlapping the neighbouring steps' kernels (the serial
+              form, copies and kernels one after another, is reported beside it);
   roofline    the partition kernel (dominant): algorithmic bytes per launch /
               its mean duration (CUDA events on the launching stream) against
               the measured HBM copy bandwidth;
@@ -476,6 +478,9 @@ def run_ours(args, dist: Dist) -> dict | None:
 
     # End to end through the public API: this step's inputs staged in one pinned host buffer and sent
     # with one copy, the kernels reading views of its device twin, the output read back to pinned memory.
+    # Measured twice: serially on the compute stream, and pipelined, with two device slots for the
+    # inputs and the output so that step i+1's inputs go in (and step i-1's output comes back) on their
+    # own copy streams while step i computes.  Every step makes both copies in either form.
     names = ("q", "new_k", "new_v", "slot_mapping", "block_tables", "context_lens")
     offsets, total = {}, 0
     for name in names:
@@ -518,14 +523,69 @@ def run_ours(args, dist: Dist) -> dict | None:
         e1.record(stream)
     stream.synchronize()
     dist.barrier()
-    e2e_elapsed = e0.elapsed_time(e1) / 1e3
+    serial_elapsed = e0.elapsed_time(e1) / 1e3
     if not torch.equal(out_host, out.cpu()):
         raise RuntimeError("e2e output read-back mismatch")
+
+    # Pipelined: slot s = i % 2 holds step i's inputs and output on the device.
+    h2d_stream, d2h_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    slots_in = [stage_dev, torch.empty_like(stage_dev)]
+    slots_view = [e2e, {name: view(slots_in[1], name) for name in names}]
+    slots_out = [out, torch.empty_like(out)]
+    hosts_out = [out_host, torch.empty_like(out_host).pin_memory()]
+    ev_in = [torch.cuda.Event() for _ in range(2)]    # slot's inputs are on the device
+    ev_done = [torch.cuda.Event() for _ in range(2)]  # slot's kernels finished (inputs free, output ready)
+    ev_out = [torch.cuda.Event() for _ in range(2)]   # slot's output is back on the host (output free)
+
+    def pipelined_step(i):
+        sl = i % 2
+        v = slots_view[sl]
+        h2d_stream.wait_event(ev_done[sl])
+        with torch.cuda.stream(h2d_stream):
+            slots_in[sl].copy_(stage_host, non_blocking=True)
+        ev_in[sl].record(h2d_stream)
+        stream.wait_event(ev_in[sl])
+        stream.wait_event(ev_out[sl])
+        pkv.kv_append(v["new_k"], v["new_v"], v["slot_mapping"], g.k_cache, g.v_cache, stream=stream)
+        pkv.paged_decode_attention(v["q"], g.k_cache, g.v_cache, v["block_tables"], v["context_lens"], g.scale,
+                                   slots_out[sl], num_partitions=parts, workspace=ws, stream=stream)
+        ev_done[sl].record(stream)
+        d2h_stream.wait_event(ev_done[sl])
+        with torch.cuda.stream(d2h_stream):
+            hosts_out[sl].copy_(slots_out[sl], non_blocking=True)
+        ev_out[sl].record(d2h_stream)
+
+    def pipelined(n, e_start=None, e_end=None):
+        if e_start is not None:
+            e_start.record(stream)
+        h2d_stream.wait_stream(stream)
+        d2h_stream.wait_stream(stream)
+        for i in range(n):
+            pipelined_step(i)
+        stream.wait_stream(d2h_stream)
+        if e_end is not None:
+            e_end.record(stream)
+
+    for h in hosts_out:
+        h.zero_()
+    pipelined(max(W, 2))
+    stream.synchronize()
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    pipelined(K, p0, p1)
+    stream.synchronize()
+    dist.barrier()
+    e2e_elapsed = p0.elapsed_time(p1) / 1e3
+    for h, o in zip(hosts_out[:min(K, 2)], slots_out):
+        if not torch.equal(h, o.cpu()):
+            raise RuntimeError("pipelined e2e output read-back mismatch")
     fused = fused_step_timing(pkv, g, spec, out, ws, stream, K, W, bytes_step)
     rows = sampler.stop() if sampler else []
 
     value, slowest = aggregate(bytes_step * K, elapsed, dist)
     e2e_value, _ = aggregate(bytes_step * K, e2e_elapsed, dist)
+    serial_value, _ = aggregate(bytes_step * K, serial_elapsed, dist)
     seqs, _ = aggregate(B * K, elapsed, dist)
     if dist.rank != 0:
         return None
@@ -561,7 +621,11 @@ def run_ours(args, dist: Dist) -> dict | None:
                      "algorithmic_bytes_per_launch": bytes_attn,
                      "mean_launch_us": round(part_mean_s * 1e6, 2)},
         "e2e": {"value": round(e2e_value / 1e9, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * e2e_elapsed / K, 4)},
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * e2e_elapsed / K, 4),
+                "copies": "pipelined: two device slots; step i+1's inputs in and step i-1's output out on "
+                          "two copy streams while step i computes",
+                "serial": {"value": round(serial_value / 1e9, 2), "ms_per_step": round(1e3 * serial_elapsed / K, 4),
+                           "copies": "in, kernels, out, one after another on the compute stream"}},
         "gpu_launches": launches,
         "clocks": clocks,
         "parity": parity,
