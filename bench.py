@@ -59,6 +59,8 @@ KERNEL_SOURCES = {
     "paged_prefill_kernel": ("paged_kv_cache_275_gb300/csrc/paged_prefill.cu",
                              "paged_kv_cache_275_gb300/csrc/paged_prefill.h",
                              "paged_kv_cache_275_gb300/csrc/pkv_internal.h"),
+    "kv_append_kernel": ("paged_kv_cache_275_gb300/csrc/kv_append.cu",
+                         "paged_kv_cache_275_gb300/csrc/pkv_internal.h"),
 }
 
 
@@ -638,6 +640,91 @@ def run_ours(args, dist: Dist) -> dict | None:
 # ---------------------------------------------------------------------------
 # Component measurements (not the headline step): block copy, block manager
 # ---------------------------------------------------------------------------
+def append_component(args, pkv, peak: float, peak_kind: str) -> dict:
+    """kv_append at prompt size: 16 prompts of 4096 tokens (65536 tokens, LLaMA-3 kv layout: 8 kv heads,
+    D 128) written into randomly permuted blocks of a 1.2 GB pool; plus the decode size (one token for
+    each of 128 sequences), which launch latency bounds."""
+    from workloads import make_generator, randn_bf16
+    dev = torch.device("cuda", 0)
+    hkv, d, nb = 8, 128, 18432
+    n_seq, per_seq = 16, 4096
+    n = n_seq * per_seq
+    kc = torch.zeros((nb, hkv, 16, d), dtype=torch.bfloat16, device=dev)
+    vc = torch.zeros_like(kc)
+    blocks = torch.randperm(nb, generator=make_generator(11))[:n // 16]
+    tok = torch.arange(n)
+    slots = (blocks[tok // 16] * 16 + tok % 16).to(torch.int64).to(dev)
+    k = randn_bf16((n, hkv, d), make_generator(12, "cuda"), "cuda")
+    v = randn_bf16((n, hkv, d), make_generator(13, "cuda"), "cuda")
+    pkv.kv_append(k, v, slots, kc, vc)
+    torch.cuda.synchronize()
+    b_idx, off = slots // 16, slots % 16
+    if (pkv.get_and_clear_device_error() != 0 or not torch.equal(kc[b_idx, :, off].view(torch.int16), k.view(torch.int16))
+            or not torch.equal(vc[b_idx, :, off].view(torch.int16), v.view(torch.int16))):
+        raise RuntimeError("kv_append parity failed before timing")
+    stream = torch.cuda.current_stream()
+
+    def timed(kk, vv, ss, steps):
+        for _ in range(args.warmup):
+            pkv.kv_append(kk, vv, ss, kc, vc)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for _ in range(steps):
+            pkv.kv_append(kk, vv, ss, kc, vc)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / 1e3 / steps
+
+    steps = min(args.steps, 500)
+    sec = timed(k, v, slots, steps)
+    moved = 2 * (2 * n * hkv * d * 2) + 8 * n    # K and V rows read and written, and the slot ids
+    gbs = moved / sec / 1e9
+    # Decode size, replayed from a CUDA graph of 64 calls: one Python call takes longer than the kernel.
+    dec_slots = slots[::per_seq // 8][:128].contiguous()
+    dk, dv = k[:128].contiguous(), v[:128].contiguous()
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            pkv.kv_append(dk, dv, dec_slots, kc, vc, stream=side)
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for _ in range(64):
+            pkv.kv_append(dk, dv, dec_slots, kc, vc, stream=side)
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(1, steps // 64)
+    e0.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    dec_sec = e0.elapsed_time(e1) / 1e3 / (64 * reps)
+    if pkv.get_and_clear_device_error() != 0:
+        raise RuntimeError("device error during the kv_append timing")
+    return {"component": "kv_append", "metric": "kv_append HBM GB/s (K/V rows read + written, slot ids)",
+            "value": round(gbs, 1), "unit": "GB/s", "steps": steps, "warmup": args.warmup,
+            "us_per_launch": round(sec * 1e6, 2),
+            "config": {"workload": "16 prompts x 4096 tokens, 8 kv heads, D 128, into permuted blocks of an "
+                                   "18432-block (1.2 GB) pool", "tokens": n,
+                       "l2": "536 MB moved per launch, over 4x the L2; no flush"},
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                         "frac": round(gbs / peak, 4), "frac_of": f"{peak_kind} HBM copy bandwidth",
+                         "algorithmic_bytes_per_launch": moved,
+                         "traffic": recorded_traffic("kv_append_kernel", "append_16x4096"),
+                         "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, profiles/traffic.txt "
+                                           f"(kernel source {source_hash('kv_append_kernel')})"},
+            "decode_size": {"tokens": 128, "us_per_launch": round(dec_sec * 1e6, 2),
+                            "bytes_per_launch": 2 * (2 * 128 * hkv * d * 2) + 8 * 128,
+                            "timing": "CUDA graph of 64 calls, replayed",
+                            "note": "one token per sequence: launch latency, not bandwidth"}}
+
+
 def run_component(args) -> dict:
     import numpy as np
 
@@ -759,6 +846,8 @@ def run_component(args) -> dict:
                              "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, profiles/traffic.txt "
                                                f"(kernel source {source_hash('paged_prefill_kernel')})",
                              "compulsory_bytes_per_launch": prefill_compulsory_bytes(c)}}
+    if args.component == "kv_append":
+        return append_component(args, pkv, peak, peak_kind)
     # copy_blocks: copy-on-write of 4096 distinct block pairs of the Qwen3/LLaMA-3 kv layout.
     dev = torch.device("cuda", 0)
     g = make_generator(7)
@@ -806,7 +895,7 @@ def main(argv=None) -> int:
                     help="seconds the reference arm's warm-up + timed steps should take")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per partition launch from an ncu capture of the current kernel")
-    ap.add_argument("--component", choices=("copy_blocks", "block_manager", "prefill", "trace"), default=None,
+    ap.add_argument("--component", choices=("copy_blocks", "block_manager", "prefill", "trace", "kv_append"), default=None,
                     help="measure one component instead of the decode step")
     args = ap.parse_args(argv)
     if args.warmup < 3:
