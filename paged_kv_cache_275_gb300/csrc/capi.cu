@@ -100,12 +100,12 @@ constexpr int32_t kMaxPartitions = 1 << 20;
 
 pkv_status default_partitions(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim, int32_t group,
                               int32_t max_blocks_per_seq, int32_t* out) {
-  int warps = 0;
-  const cudaError_t e = pkv::resident_partition_warps(head_dim, group, num_seqs, &warps);
+  int pieces = 0;
+  const cudaError_t e = pkv::resident_partition_pieces(head_dim, group, num_seqs, &pieces);
   if (e != cudaSuccess) return cuda_fail(e, "occupancy query");
   // Never more pieces than the block stream can have items.
   const int64_t bound = static_cast<int64_t>(num_seqs) * num_kv_heads * max_blocks_per_seq;
-  int64_t n = warps;
+  int64_t n = pieces;
   if (n > bound) n = bound;
   if (n > kMaxPartitions) n = kMaxPartitions;
   if (n < 1) n = 1;

@@ -39,6 +39,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "pagedkv.h"
 #include "pkv_internal.h"
 
 namespace pkv {
@@ -107,14 +108,14 @@ struct Geo {
   }
 };
 
-// Launch shape per (head_dim, group): warps per CTA and ring stages per warp.  At
+// Launch shape per (head_dim, group): warps per CTA and stages per ring.  At
 // D = 128, four q heads per kv head run best with four warps of three stages
-// (LLaMA-3 shape: 201.6 against 209.6 us with eight warps of two); every other group
-// size with eight warps of two stages: one or two heads do little arithmetic per
-// byte and more warps keep more copies moving (Qwen3-shape trace: 6.20 against
-// 5.76 TB/s), and eight heads need the registers of two passes and the larger q
-// rows of a stage (339 against 531 us on a 1.27 GB batch).  The macros override the
-// D = 128 shape for every group, for sweeps.
+// (LLaMA-3 shape: 201.6 against 209.6 us with eight warps of two); one or two heads
+// with eight warps of two stages, since they do little arithmetic per byte and more
+// warps keep more copies moving (Qwen3-shape trace: 6.20 against 5.76 TB/s); eight
+// heads, two warps to a ring, with twelve warps of three stages (LLaMA-3-70B shape:
+// 323 us, against 328-330 with 12 x 2 or 16 x 2 and 404 with 8 x 2).  The macros
+// override the D = 128 shape for every group, for sweeps.
 #ifndef PKV_D64_WARPS
 #define PKV_D64_WARPS 4
 #endif
@@ -128,12 +129,12 @@ struct Shape<128, G> {
 #ifdef PKV_D128_WARPS
   static constexpr int kWarps = PKV_D128_WARPS;
 #else
-  static constexpr int kWarps = G == 4 ? 4 : 8;
+  static constexpr int kWarps = G == 4 ? 4 : G == 8 ? 12 : 8;
 #endif
 #ifdef PKV_D128_STAGES
   static constexpr int kStages = PKV_D128_STAGES;
 #else
-  static constexpr int kStages = G == 4 ? 3 : 2;
+  static constexpr int kStages = G >= 4 ? 3 : 2;
 #endif
 };
 template <int G>
@@ -142,16 +143,38 @@ struct Shape<64, G> {
   static constexpr int kStages = PKV_D64_STAGES;
 };
 
+// Heads of a group are processed four at a time: a group of eight runs two warps
+// over each staged K/V tile, one per four heads, so each warp keeps the registers of
+// a four-head group and every tile is still read from HBM once.
+template <int G>
+struct Split {
+  static constexpr int kHeads = G > 4 ? 4 : G;  // q heads per warp
+  static constexpr int kWarps = G / kHeads;     // warps sharing one ring
+};
+// Shared memory of one CTA: a ring per warp group, a p tile per warp, a barrier per stage.
+template <int D, int G, int NW, int S>
+constexpr size_t ring_smem_bytes() {
+  constexpr int kRings = NW / Split<G>::kWarps;
+  return size_t(kRings) * S * Geo<D, G>::kStageBytes + size_t(NW) * Geo<D, Split<G>::kHeads>::kPTileBytes +
+         size_t(kRings) * S * 8;
+}
 template <int D, int G>
 constexpr size_t static_smem_bytes() {
-  using T = Geo<D, G>;
-  constexpr int NW = Shape<D, G>::kWarps, S = Shape<D, G>::kStages;
-  return size_t(NW) * S * T::kStageBytes + size_t(NW) * T::kPTileBytes + size_t(NW) * S * 8;
+  return ring_smem_bytes<D, G, Shape<D, G>::kWarps, Shape<D, G>::kStages>();
 }
 template <int D, int G>
 size_t partition_smem_bytes(int num_seqs) {
   return (static_smem_bytes<D, G>() + size_t(2 * num_seqs + 1) * 4 + 15) & ~size_t(15);
 }
+// Every instance fits the 227 KB a CTA may opt in to, with the largest batch's lengths and prefix.
+template <int D, int G>
+constexpr bool fits_largest_batch() {
+  return static_smem_bytes<D, G>() + size_t(2 * PKV_MAX_SEQS + 1) * 4 + 16 <= 227u * 1024u;
+}
+static_assert(fits_largest_batch<64, 1>() && fits_largest_batch<64, 2>() && fits_largest_batch<64, 4>() &&
+                  fits_largest_batch<64, 8>() && fits_largest_batch<128, 1>() && fits_largest_batch<128, 2>() &&
+                  fits_largest_batch<128, 4>() && fits_largest_batch<128, 8>(),
+              "partition kernel shared memory");
 
 // ---------------------------------------------------------------------------
 // PTX wrappers (mbarrier, bulk copy, timers).
@@ -194,6 +217,21 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 // Wait for phase `parity` of an mbarrier, giving up after `limit_ns`.
+// Named barrier over the `count` threads of one ring's warps (id 1 + ring; 0 is __syncthreads).
+__device__ __forceinline__ void ring_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// The same barrier, returning whether `v` holds on every participating thread.
+__device__ __forceinline__ bool ring_all(bool v, int id, int count) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred pv, pa;\n\tsetp.ne.s32 pv, %1, 0;\n\tbar.red.and.pred pa, %2, %3, pv;\n\t"
+      "selp.s32 %0, 1, 0, pa;\n\t}"
+      : "=r"(r)
+      : "r"(v ? 1 : 0), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
@@ -379,27 +417,31 @@ __device__ __forceinline__ void advance(Cursor& cur, const int* s_prefix, int nu
 template <int D, int G, int NW, int S>
 __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const DecodeParams p) {
   using T = Geo<D, G>;
-  // Heads are processed in sub-groups of at most four: a group of eight runs the
-  // four-head block routine twice per staged K/V tile (its state would not fit the
-  // registers in one pass), still reading every tile from HBM once.
-  constexpr int GS = G > 4 ? 4 : G;
-  constexpr int SUB = G / GS;
+  // SP warps share each ring, warp `sub` of a ring taking heads sub * GS .. + GS - 1.
+  constexpr int GS = Split<G>::kHeads;
+  constexpr int SP = Split<G>::kWarps;
+  constexpr int NR = NW / SP;  // rings (pieces in flight) per CTA
   using TS = Geo<D, GS>;
-  static_assert(TS::valid() && G % GS == 0, "unsupported (head_dim, group) geometry");
+  static_assert(TS::valid() && G % GS == 0 && NW % SP == 0, "unsupported (head_dim, group) geometry");
+  static_assert(SP == 1 || NR <= 15, "one named barrier per ring");
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int s_wsum[32];
 
   const int B = p.num_seqs;
   const int hkv = p.num_kv_heads;
   unsigned char* stages = smem;
-  float2* ptiles = reinterpret_cast<float2*>(stages + size_t(NW) * S * T::kStageBytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(ptiles) + NW * T::kPTileBytes);
-  int* s_prefix = reinterpret_cast<int*>(bars + NW * S);
+  float2* ptiles = reinterpret_cast<float2*>(stages + size_t(NR) * S * T::kStageBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(ptiles) + NW * TS::kPTileBytes);
+  int* s_prefix = reinterpret_cast<int*>(bars + NR * S);
   int* s_len = s_prefix + (B + 1);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
+  const int rg = warp / SP;   // this warp's ring
+  const int sub = warp % SP;  // its four-head sub-group
+  const int ring_bar = 1 + rg;
+  const bool producer = lane == 0 && sub == 0;
   pdl_trigger();
   pdl_wait();
 
@@ -447,20 +489,21 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
   if (blockIdx.x == 0)
     for (int i = tid; i <= B; i += NW * 32) p.ws_prefix[i] = s_prefix[i];
 
-  // --- per-warp ring ----------------------------------------------------------
-  unsigned char* ring_ptr = stages + size_t(warp) * S * T::kStageBytes;
+  // --- per-ring stages ----------------------------------------------------------
+  unsigned char* ring_ptr = stages + size_t(rg) * S * T::kStageBytes;
   const uint32_t ring = smem_addr(ring_ptr);
-  const uint32_t bar0 = smem_addr(bars + warp * S);
-  float2* ptile = ptiles + warp * (T::kPTileBytes / 8);
-  if (lane == 0) {
+  const uint32_t bar0 = smem_addr(bars + rg * S);
+  float2* ptile = ptiles + warp * (TS::kPTileBytes / 8);
+  if (producer) {
 #pragma unroll
     for (int s = 0; s < S; ++s) mbar_init(bar0 + 8 * s, 1);
     fence_mbar_init();
   }
-  __syncwarp();
+  if constexpr (SP > 1) __syncthreads();  // every warp of the CTA is still here
+  else __syncwarp();
 
   const long long total = static_cast<long long>(hkv) * s_prefix[B];
-  const int gw = blockIdx.x * NW + warp;
+  const int gw = blockIdx.x * NR + rg;  // the piece: the same for the warps of a ring
   if (gw >= p.num_partitions || total == 0) return;
   const long long begin = gw * total / p.num_partitions;
   const long long end = (gw + 1) * total / p.num_partitions;
@@ -510,7 +553,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
 
   // Prologue: fetch the first S + 1 block ids together, fill the ring.
   int next_id = 0;
-  if (lane == 0) {
+  if (producer) {
     int ids[S + 1];
     Cursor cur = pc;
 #pragma unroll
@@ -534,10 +577,11 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
   const int mg = mask % GS;
   const float qscale = p.qscale;
 
-  float2 q[SUB][GS][4];  // q[sb][gp]: head sb * GS + (gp ^ mg), swizzled per lane
-  float2 acc[SUB][GS][4];  // acc[sb][g]: head sb * GS + g
-  float m_ref[SUB][GS];
-  float m_mine[SUB][TS::kFinal], l_mine[SUB][TS::kFinal];
+  const int h0 = sub * GS;  // first q head of this warp within the group
+  float2 q[GS][4];          // q[gp]: head h0 + (gp ^ mg), swizzled per lane
+  float2 acc[GS][4];        // acc[g]: head h0 + g
+  float m_ref[GS];
+  float m_mine[TS::kFinal], l_mine[TS::kFinal];
   bool pair_from_start = false;
   bool first_pair = true;
 
@@ -546,7 +590,10 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
   for (int i = 0; i < n; ++i) {
     const unsigned char* st_ptr = ring_ptr + stage * T::kStageBytes;
     const bool landed = mbar_wait(bar0 + 8 * stage, phase, kWaitTimeoutNs);
-    if (!__all_sync(kFull, landed)) {
+    bool all_landed;
+    if constexpr (SP > 1) all_landed = ring_all(landed, ring_bar, SP * 32);  // the ring's warps decide together
+    else all_landed = __all_sync(kFull, landed);
+    if (!all_landed) {
       // Give up on this piece: flag it, let the copies already in flight land, leave.
       if (lane == 0) atomicOr(p.err, kErrTimeout);
       for (int x = i; x < n && x < i + S; ++x) mbar_wait(bar0 + 8 * (x % S), (x / S) & 1, kDrainTimeoutNs);
@@ -567,27 +614,24 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
         cs_row = p.cos_sin + pos * D;
       }
 #pragma unroll
-      for (int sb = 0; sb < SUB; ++sb) {
+      for (int gp = 0; gp < GS; ++gp) {
+        const int head = h0 + (gp ^ mg);
+        uint4 w = lds128(sq + head * (D * 2) + c * 16);
+        if (cs_row != nullptr)
+          w = rope_chunk<D>(w, lds128(sq + head * (D * 2) + ((c * 16 + D) % (D * 2))), cs_row, c);
+        const float2 s2 = make_float2(qscale, qscale);
+        q[gp][0] = __fmul2_rn(bf16x2_to_float2(w.x), s2);
+        q[gp][1] = __fmul2_rn(bf16x2_to_float2(w.y), s2);
+        q[gp][2] = __fmul2_rn(bf16x2_to_float2(w.z), s2);
+        q[gp][3] = __fmul2_rn(bf16x2_to_float2(w.w), s2);
 #pragma unroll
-        for (int gp = 0; gp < GS; ++gp) {
-          const int head = sb * GS + (gp ^ mg);
-          uint4 w = lds128(sq + head * (D * 2) + c * 16);
-          if (cs_row != nullptr)
-            w = rope_chunk<D>(w, lds128(sq + head * (D * 2) + ((c * 16 + D) % (D * 2))), cs_row, c);
-          const float2 s2 = make_float2(qscale, qscale);
-          q[sb][gp][0] = __fmul2_rn(bf16x2_to_float2(w.x), s2);
-          q[sb][gp][1] = __fmul2_rn(bf16x2_to_float2(w.y), s2);
-          q[sb][gp][2] = __fmul2_rn(bf16x2_to_float2(w.z), s2);
-          q[sb][gp][3] = __fmul2_rn(bf16x2_to_float2(w.w), s2);
+        for (int e = 0; e < 4; ++e) acc[gp][e] = make_float2(0.f, 0.f);
+        m_ref[gp] = -INFINITY;
+      }
 #pragma unroll
-          for (int e = 0; e < 4; ++e) acc[sb][gp][e] = make_float2(0.f, 0.f);
-          m_ref[sb][gp] = -INFINITY;
-        }
-#pragma unroll
-        for (int k = 0; k < TS::kFinal; ++k) {
-          m_mine[sb][k] = -INFINITY;
-          l_mine[sb][k] = 0.f;
-        }
+      for (int k = 0; k < TS::kFinal; ++k) {
+        m_mine[k] = -INFINITY;
+        l_mine[k] = 0.f;
       }
       pair_from_start = (cc.blk == 0);
     }
@@ -596,7 +640,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
       // Fused step: this block holds position len - 1, the step's new token.  Put its
       // (rotated) K row and its V row into the staged tiles and append them to the cache.
       const int row = (seq_len - 1) % kBlockTokens;
-      if (half == 0) {
+      if (half == 0 && sub == 0) {
         const size_t src = (static_cast<size_t>(cc.b) * hkv + cc.kvh) * D;
         const uint4* kn = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.k_new) + src);
         const uint4* vn = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.v_new) + src);
@@ -617,22 +661,20 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
           reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(const_cast<void*>(p.v_cache)) + dst)[c] = vw;
         }
       }
-      __syncwarp();
+      if constexpr (SP > 1) ring_sync(ring_bar, SP * 32);  // the row is in the stage for every warp
+      else __syncwarp();
     }
-#pragma unroll
-    for (int sb = 0; sb < SUB; ++sb) {
-      if (sb > 0) __syncwarp();  // the p tile is rewritten for the next sub-group
-      if (valid >= kBlockTokens)
-        process_block<D, GS, false>(st_ptr, st_ptr + T::kTileBytes, ptile, q[sb], acc[sb], m_ref[sb], m_mine[sb],
-                                    l_mine[sb], c, half, mask, kBlockTokens);
-      else
-        process_block<D, GS, true>(st_ptr, st_ptr + T::kTileBytes, ptile, q[sb], acc[sb], m_ref[sb], m_mine[sb],
-                                   l_mine[sb], c, half, mask, valid);
-    }
-    __syncwarp();
+    if (valid >= kBlockTokens)
+      process_block<D, GS, false>(st_ptr, st_ptr + T::kTileBytes, ptile, q, acc, m_ref, m_mine, l_mine, c, half,
+                                  mask, kBlockTokens);
+    else
+      process_block<D, GS, true>(st_ptr, st_ptr + T::kTileBytes, ptile, q, acc, m_ref, m_mine, l_mine, c, half,
+                                 mask, valid);
+    if constexpr (SP > 1) ring_sync(ring_bar, SP * 32);  // every warp of the ring is done with the stage
+    else __syncwarp();
 
     // Refill the stage just consumed with block i + S.
-    if (lane == 0 && i + S < n) {
+    if (producer && i + S < n) {
       fence_proxy_async_smem();
       issue(stage, pc, next_id, pc.blk == 0);
       if (i + S + 1 < n) {
@@ -647,26 +689,20 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
 #pragma unroll
       for (int off = TS::kLanesPerToken; off < 32; off <<= 1)
 #pragma unroll
-        for (int sb = 0; sb < SUB; ++sb)
+        for (int g = 0; g < GS; ++g)
 #pragma unroll
-          for (int g = 0; g < GS; ++g)
+          for (int e = 0; e < 4; ++e) {
+            acc[g][e].x += __shfl_xor_sync(kFull, acc[g][e].x, off);
+            acc[g][e].y += __shfl_xor_sync(kFull, acc[g][e].y, off);
+          }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              acc[sb][g][e].x += __shfl_xor_sync(kFull, acc[sb][g][e].x, off);
-              acc[sb][g][e].y += __shfl_xor_sync(kFull, acc[sb][g][e].y, off);
-            }
+      for (int k = 0; k < TS::kFinal; ++k)
 #pragma unroll
-      for (int sb = 0; sb < SUB; ++sb)
+        for (int bit = 1; bit < 32; bit <<= 1)
+          if (TS::sum_bits() & bit) l_mine[k] += __shfl_xor_sync(kFull, l_mine[k], bit);
+      float l_all[GS];
 #pragma unroll
-        for (int k = 0; k < TS::kFinal; ++k)
-#pragma unroll
-          for (int bit = 1; bit < 32; bit <<= 1)
-            if (TS::sum_bits() & bit) l_mine[sb][k] += __shfl_xor_sync(kFull, l_mine[sb][k], bit);
-      float l_all[SUB][GS];
-#pragma unroll
-      for (int sb = 0; sb < SUB; ++sb)
-#pragma unroll
-        for (int g = 0; g < GS; ++g) l_all[sb][g] = __shfl_sync(kFull, l_mine[sb][g % TS::kFinal], TS::src_lane(g));
+      for (int g = 0; g < GS; ++g) l_all[g] = __shfl_sync(kFull, l_mine[g % TS::kFinal], TS::src_lane(g));
 
       if (pair_from_start && last_of_pair) {
         if (half == 0) {
@@ -674,38 +710,32 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
                                                  (static_cast<size_t>(cc.b) * p.num_q_heads + cc.kvh * G) * D) +
                         c;
 #pragma unroll
-          for (int sb = 0; sb < SUB; ++sb)
-#pragma unroll
-            for (int g = 0; g < GS; ++g) {
-              const float inv = 1.0f / l_all[sb][g];
-              uint4 o;
-              o.x = float2_to_bf16x2(acc[sb][g][0].x * inv, acc[sb][g][0].y * inv);
-              o.y = float2_to_bf16x2(acc[sb][g][1].x * inv, acc[sb][g][1].y * inv);
-              o.z = float2_to_bf16x2(acc[sb][g][2].x * inv, acc[sb][g][2].y * inv);
-              o.w = float2_to_bf16x2(acc[sb][g][3].x * inv, acc[sb][g][3].y * inv);
-              orow[(sb * GS + g) * (D / 8)] = o;
-            }
+          for (int g = 0; g < GS; ++g) {
+            const float inv = 1.0f / l_all[g];
+            uint4 o;
+            o.x = float2_to_bf16x2(acc[g][0].x * inv, acc[g][0].y * inv);
+            o.y = float2_to_bf16x2(acc[g][1].x * inv, acc[g][1].y * inv);
+            o.z = float2_to_bf16x2(acc[g][2].x * inv, acc[g][2].y * inv);
+            o.w = float2_to_bf16x2(acc[g][3].x * inv, acc[g][3].y * inv);
+            orow[(h0 + g) * (D / 8)] = o;
+          }
         }
       } else {
         float* piece = p.ws_pieces + (static_cast<size_t>(gw) * 2 + (first_pair ? 0 : 1)) * T::kPieceFloats;
         if (half == 0) {
 #pragma unroll
-          for (int sb = 0; sb < SUB; ++sb)
-#pragma unroll
-            for (int g = 0; g < GS; ++g) {
-              float4* dst = reinterpret_cast<float4*>(piece + (sb * GS + g) * D + c * 8);
-              dst[0] = make_float4(acc[sb][g][0].x, acc[sb][g][0].y, acc[sb][g][1].x, acc[sb][g][1].y);
-              dst[1] = make_float4(acc[sb][g][2].x, acc[sb][g][2].y, acc[sb][g][3].x, acc[sb][g][3].y);
-            }
+          for (int g = 0; g < GS; ++g) {
+            float4* dst = reinterpret_cast<float4*>(piece + (h0 + g) * D + c * 8);
+            dst[0] = make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
+            dst[1] = make_float4(acc[g][2].x, acc[g][2].y, acc[g][3].x, acc[g][3].y);
+          }
         }
         if (lane == 0) {
 #pragma unroll
-          for (int sb = 0; sb < SUB; ++sb)
-#pragma unroll
-            for (int g = 0; g < GS; ++g) {
-              piece[G * D + sb * GS + g] = m_ref[sb][g];
-              piece[G * D + G + sb * GS + g] = l_all[sb][g];
-            }
+          for (int g = 0; g < GS; ++g) {
+            piece[G * D + h0 + g] = m_ref[g];
+            piece[G * D + G + h0 + g] = l_all[g];
+          }
         }
       }
       first_pair = false;
@@ -797,6 +827,7 @@ template <int D, int G>
 struct Instance {
   static constexpr int NW = Shape<D, G>::kWarps;
   static constexpr int S = Shape<D, G>::kStages;
+  static constexpr int NR = NW / Split<G>::kWarps;  // pieces in flight per CTA
   static void* partition_fn() { return reinterpret_cast<void*>(&paged_decode_partition_kernel<D, G, NW, S>); }
 
   static cudaError_t prepare(int dev) {
@@ -820,7 +851,7 @@ struct Instance {
     return cudaSuccess;
   }
 
-  static cudaError_t resident_warps(int num_seqs, int* warps) {
+  static cudaError_t resident_pieces(int num_seqs, int* pieces) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -830,7 +861,7 @@ struct Instance {
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, &paged_decode_partition_kernel<D, G, NW, S>,
                                                       NW * 32, partition_smem_bytes<D, G>(num_seqs));
     if (e != cudaSuccess) return e;
-    *warps = sms * (per_sm > 0 ? per_sm : 1) * NW;
+    *pieces = sms * (per_sm > 0 ? per_sm : 1) * NR;
     return cudaSuccess;
   }
 
@@ -839,7 +870,7 @@ struct Instance {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if ((e = prepare(dev)) != cudaSuccess) return e;
-    const unsigned grid = static_cast<unsigned>((p.num_partitions + NW - 1) / NW);
+    const unsigned grid = static_cast<unsigned>((p.num_partitions + NR - 1) / NR);
     return launch_pdl(paged_decode_partition_kernel<D, G, NW, S>, dim3(grid), dim3(NW * 32),
                       partition_smem_bytes<D, G>(p.num_seqs), stream, p);
   }
@@ -871,13 +902,8 @@ int piece_floats(int head_dim, int group) { return group * head_dim + ((2 * grou
 
 size_t workspace_header_bytes(int num_seqs) { return (static_cast<size_t>(num_seqs + 1) * 4 + 255) & ~size_t(255); }
 
-int partition_warps_per_cta(int head_dim, int group) {
-  if (head_dim == 64) return Shape<64, 1>::kWarps;
-  return group == 4 ? Shape<128, 4>::kWarps : Shape<128, 8>::kWarps;
-}
-
-cudaError_t resident_partition_warps(int head_dim, int group, int num_seqs, int* warps) {
-  return dispatch(head_dim, group, [&](auto inst) { return decltype(inst)::resident_warps(num_seqs, warps); });
+cudaError_t resident_partition_pieces(int head_dim, int group, int num_seqs, int* pieces) {
+  return dispatch(head_dim, group, [&](auto inst) { return decltype(inst)::resident_pieces(num_seqs, pieces); });
 }
 
 cudaError_t launch_decode_partition(const DecodeParams& p, int head_dim, int group, cudaStream_t stream) {

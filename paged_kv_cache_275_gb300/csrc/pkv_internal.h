@@ -98,10 +98,9 @@ cudaError_t launch_kv_append(const AppendParams& p, int num_sms, cudaStream_t st
 int piece_floats(int head_dim, int group);
 // Bytes of the workspace header (block prefix) for num_seqs sequences.
 size_t workspace_header_bytes(int num_seqs);
-// Warps per CTA of the partition kernel for these shapes.
-int partition_warps_per_cta(int head_dim, int group);
-// Resident partition-kernel warps on the current device (the default num_partitions).
-cudaError_t resident_partition_warps(int head_dim, int group, int num_seqs, int* warps);
+// Pieces the partition kernel keeps in flight on the current device: one per warp,
+// or per pair of warps for groups of eight q heads (the default num_partitions).
+cudaError_t resident_partition_pieces(int head_dim, int group, int num_seqs, int* pieces);
 // Decode kernels.  `group` = num_q_heads / num_kv_heads.
 cudaError_t launch_decode_partition(const DecodeParams& p, int head_dim, int group, cudaStream_t stream);
 cudaError_t launch_decode_merge(const DecodeParams& p, int head_dim, int group, cudaStream_t stream);
