@@ -345,6 +345,19 @@ pkv_status pkv_bm_ref_count(pkv_block_manager* bm, int64_t block, int32_t* count
  */
 pkv_status pkv_get_and_clear_device_error(uint32_t* bits, pkv_stream_t stream);
 
+/*
+ * Self-test of failure detection.  Every wait of the attention kernels on a
+ * shared-memory barrier (a staged K/V copy landing) gives up after a time
+ * limit, sets PKV_DEVERR_PIPELINE_TIMEOUT and leaves, so that a copy that never
+ * lands ends in an error the host reads rather than in a hung GPU.  This call
+ * launches one warp on `stream` that runs that same wait, with a limit of
+ * limit_ns nanoseconds, on a barrier that nothing completes: the wait runs
+ * out and the bit is set.  It faults nothing and the context stays usable.
+ * limit_ns must lie in [1000, 1000000000] (1 us .. 1 s), else
+ * PKV_ERR_INVALID_ARGUMENT before any launch.
+ */
+pkv_status pkv_selftest_wait_timeout(uint64_t limit_ns, pkv_stream_t stream);
+
 /* Message of the last failed call on this host thread ("" if none).  Valid until the next call. */
 const char* pkv_last_error_message(void);
 

@@ -11,7 +11,7 @@ from ._capi import (BLOCK_SIZE, DEVERR_BLOCK_ID_OUT_OF_RANGE, DEVERR_COPY_OUT_OF
                     DEVERR_CONTEXT_LEN_TOO_LONG, DEVERR_PIPELINE_TIMEOUT, DEVERR_SLOT_OUT_OF_RANGE, EXPORTS,
                     LIB_PATH, MAX_SEQS, PHASE_ALL, PHASE_MERGE, PHASE_PARTITION, PagedKVError, default_partitions,
                     get_and_clear_device_error, kernel_launch_count, kv_append, load, paged_decode_attention,
-                    workspace_size)
+                    selftest_wait_timeout, workspace_size)
 
 __all__ = [
     "BLOCK_SIZE", "MAX_SEQS", "EXPORTS", "LIB_PATH", "PagedKVError", "PHASE_ALL", "PHASE_MERGE", "PHASE_PARTITION",
@@ -19,5 +19,5 @@ __all__ = [
     "DEVERR_CONTEXT_LEN_TOO_LONG", "DEVERR_PIPELINE_TIMEOUT",
     "kv_append", "paged_decode_attention", "workspace_size", "default_partitions", "get_and_clear_device_error",
     "kernel_launch_count", "load", "copy_blocks", "BlockManager", "DEVERR_COPY_OUT_OF_RANGE", "decode_step",
-    "DEVERR_POSITION_OUT_OF_TABLE", "paged_prefill_attention", "DEVERR_SMEM_ALIGNMENT",
+    "DEVERR_POSITION_OUT_OF_TABLE", "paged_prefill_attention", "DEVERR_SMEM_ALIGNMENT", "selftest_wait_timeout",
 ]

@@ -61,6 +61,7 @@ EXPORTS = (
     "pkv_bm_block_tables",
     "pkv_bm_ref_count",
     "pkv_get_and_clear_device_error",
+    "pkv_selftest_wait_timeout",
     "pkv_last_error_message",
     "pkv_kernel_launch_count",
 )
@@ -112,9 +113,11 @@ def load(path: Path | str | None = None) -> ctypes.CDLL:
         lib.pkv_bm_block_tables.argtypes = [V, V, I32, I32, V, V]
         lib.pkv_bm_ref_count.argtypes = [V, I64, ctypes.POINTER(I32)]
         lib.pkv_get_and_clear_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), V]
+        lib.pkv_selftest_wait_timeout.argtypes = [ctypes.c_uint64, V]
         for name in ("pkv_kv_append", "pkv_decode_workspace_size", "pkv_decode_default_partitions",
                      "pkv_paged_decode_attention", "pkv_paged_decode_attention_split",
-                     "pkv_paged_decode_attention_static", "pkv_get_and_clear_device_error", "pkv_copy_blocks", "pkv_decode_step", "pkv_paged_prefill_attention",
+                     "pkv_paged_decode_attention_static", "pkv_get_and_clear_device_error",
+                     "pkv_selftest_wait_timeout", "pkv_copy_blocks", "pkv_decode_step", "pkv_paged_prefill_attention",
                      "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_num_free", "pkv_bm_add_sequence",
                      "pkv_bm_append_slots", "pkv_bm_fork", "pkv_bm_free_sequence", "pkv_bm_block_tables",
                      "pkv_bm_ref_count"):
@@ -250,6 +253,12 @@ def get_and_clear_device_error(stream: torch.cuda.Stream | None = None) -> int:
     bits = ctypes.c_uint32(0)
     _check(load().pkv_get_and_clear_device_error(ctypes.byref(bits), _stream_handle(stream)))
     return int(bits.value)
+
+
+def selftest_wait_timeout(limit_ns: int, stream: torch.cuda.Stream | None = None) -> None:
+    """Launch one warp that waits, for at most limit_ns, on a shared-memory barrier nothing completes:
+    the bounded wait of the attention kernels gives up and sets PKV_DEVERR_PIPELINE_TIMEOUT."""
+    _check(load().pkv_selftest_wait_timeout(int(limit_ns), _stream_handle(stream)))
 
 
 def kernel_launch_count() -> int:

@@ -276,6 +276,18 @@ pkv_status pkv_copy_blocks(void* k_cache, void* v_cache, const int64_t* src_dst,
   return ok();
 }
 
+pkv_status pkv_selftest_wait_timeout(uint64_t limit_ns, pkv_stream_t stream) {
+  if (limit_ns < 1000 || limit_ns > 1000000000ull)
+    return fail(PKV_ERR_INVALID_ARGUMENT, "limit_ns must lie in [1e3, 1e9] (got %llu)", (unsigned long long)limit_ns);
+  unsigned* err = nullptr;
+  if (pkv_status st = device_state(&err, nullptr); st != PKV_OK) return st;
+  const cudaError_t e =
+      pkv::launch_bounded_wait_selftest(err, limit_ns, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  g_launches.fetch_add(1);
+  return ok();
+}
+
 pkv_status pkv_paged_prefill_attention(const void* q, const void* k_cache, const void* v_cache,
                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
                                        const int32_t* context_lens, const int32_t* query_start,

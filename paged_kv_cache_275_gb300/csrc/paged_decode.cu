@@ -821,6 +821,24 @@ __global__ void __launch_bounds__(G * 32) paged_decode_merge_kernel(const Decode
 }
 
 // ---------------------------------------------------------------------------
+// Self-test of the bounded wait: one warp waits, with the given limit, on a
+// shared-memory barrier that nothing completes.  The wait must give up and the
+// warp report it in the error word, as a partition warp whose copy never lands
+// does, and the kernel returns; nothing faults and the context stays usable.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(32) bounded_wait_selftest_kernel(unsigned* err, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_addr(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const bool landed = mbar_wait(b, 0, limit_ns);
+  if (!__all_sync(kFull, landed) && threadIdx.x == 0) atomicOr(err, kErrTimeout);
+}
+
+// ---------------------------------------------------------------------------
 // Host side: per-instance launch helpers.
 // ---------------------------------------------------------------------------
 template <int D, int G>
@@ -908,6 +926,10 @@ cudaError_t resident_partition_pieces(int head_dim, int group, int num_seqs, int
 
 cudaError_t launch_decode_partition(const DecodeParams& p, int head_dim, int group, cudaStream_t stream) {
   return dispatch(head_dim, group, [&](auto inst) { return decltype(inst)::partition(p, stream); });
+}
+
+cudaError_t launch_bounded_wait_selftest(unsigned* err, unsigned long long limit_ns, cudaStream_t stream) {
+  return launch_pdl(bounded_wait_selftest_kernel, dim3(1), dim3(32), 0, stream, err, limit_ns);
 }
 
 cudaError_t launch_decode_merge(const DecodeParams& p, int head_dim, int group, cudaStream_t stream) {

@@ -101,6 +101,8 @@ size_t workspace_header_bytes(int num_seqs);
 // Pieces the partition kernel keeps in flight on the current device: one per warp,
 // or per pair of warps for groups of eight q heads (the default num_partitions).
 cudaError_t resident_partition_pieces(int head_dim, int group, int num_seqs, int* pieces);
+// One warp waiting on a barrier that nothing completes, for at most limit_ns (the bounded-wait self-test).
+cudaError_t launch_bounded_wait_selftest(unsigned* err, unsigned long long limit_ns, cudaStream_t stream);
 // Decode kernels.  `group` = num_q_heads / num_kv_heads.
 cudaError_t launch_decode_partition(const DecodeParams& p, int head_dim, int group, cudaStream_t stream);
 cudaError_t launch_decode_merge(const DecodeParams& p, int head_dim, int group, cudaStream_t stream);

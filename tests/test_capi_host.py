@@ -125,6 +125,12 @@ def test_workspace_size_with_explicit_partitions(lib):
     assert lib.pkv_decode_workspace_size(4, 2, 1, 64, 3, -1, ctypes.byref(n1)) == 1
 
 
+def test_selftest_rejects_limits_outside_range(lib):
+    for bad in (0, 999, 1_000_000_001, 2**63):
+        assert lib.pkv_selftest_wait_timeout(bad, None) == 1  # PKV_ERR_INVALID_ARGUMENT, before any CUDA call
+        assert b"limit_ns" in lib.pkv_last_error_message()
+
+
 def test_launch_counter_starts_at_zero_without_launches(lib):
     assert lib.pkv_kernel_launch_count() == 0
 

@@ -58,7 +58,7 @@ def test_fused_step_without_rope_equals_separate_calls():
     assert torch.equal(out, ref)
 
 
-@pytest.mark.parametrize("head_dim,hq,hkv", [(64, 2, 1), (64, 8, 2), (128, 8, 8), (128, 32, 4)])
+@pytest.mark.parametrize("head_dim,hq,hkv", [(64, 2, 1), (64, 8, 2), (64, 16, 2), (128, 8, 8), (128, 32, 4)])
 def test_fused_step_every_layout_and_length(head_dim, hq, hkv):
     spec = DecodeSpec(name="lens", description="", num_seqs=20, num_q_heads=hq, num_kv_heads=hkv,
                       head_dim=head_dim, max_blocks_per_seq=5, length_kind="fixed",
