@@ -32,6 +32,7 @@
 //   2 with a lazy rescale: the running max is only raised when a block's max
 //   exceeds it by more than 2^8, which keeps the exp2 arguments bounded and
 //   skips the rescale of the accumulators on almost every block.
+#include <cuda.h>  // CUtensorMap (maps are encoded on the host through the runtime's driver entry point)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -108,14 +109,35 @@ struct Geo {
   }
 };
 
+// Groups of PKV_MMA_MIN_G to 8 q heads run q.K and p.V on the tensor cores (warp-level
+// mma.sync, the group's heads as the N = 8 columns), one warp per ring.  Otherwise
+// the CUDA cores take at most four heads per warp: a group of eight then runs two
+// warps over each staged K/V tile, one per four heads, each tile still read once.
+#ifndef PKV_MMA_MIN_G
+#define PKV_MMA_MIN_G 8
+#endif
+template <int G>
+struct Split {
+  static constexpr bool kMma = G >= PKV_MMA_MIN_G && G <= 8;
+  static constexpr int kHeads = kMma ? G : (G > 4 ? 4 : G);  // q heads per warp
+  static constexpr int kWarps = G / kHeads;                   // warps sharing one ring
+};
+// One ring stage: K tile | V tile | q rows.  The tensor-core path copies K and V as
+// 128-byte-swizzled tensor tiles, whose stages start on 1024-byte boundaries.
+template <int D, int G>
+constexpr int stage_bytes() {
+  return Split<G>::kMma ? (Geo<D, G>::kStageBytes + 1023) / 1024 * 1024 : Geo<D, G>::kStageBytes;
+}
+
 // Launch shape per (head_dim, group): warps per CTA and stages per ring.  At
 // D = 128, four q heads per kv head run best with four warps of three stages
 // (LLaMA-3 shape: 201.6 against 209.6 us with eight warps of two); one or two heads
 // with eight warps of two stages, since they do little arithmetic per byte and more
 // warps keep more copies moving (Qwen3-shape trace: 6.20 against 5.76 TB/s); eight
-// heads, two warps to a ring, with twelve warps of three stages (LLaMA-3-70B shape:
-// 323 us, against 328-330 with 12 x 2 or 16 x 2 and 404 with 8 x 2).  The macros
-// override the D = 128 shape for every group, for sweeps.
+// heads on the CUDA cores, two warps to a ring, with twelve warps of three stages
+// (LLaMA-3-70B shape: 323 us, against 328-330 with 12 x 2 or 16 x 2 and 404 with
+// 8 x 2), and on the tensor cores with eight warps of two.  The macros override the
+// D = 128 shape for every group, for sweeps.
 #ifndef PKV_D64_WARPS
 #define PKV_D64_WARPS 4
 #endif
@@ -129,12 +151,12 @@ struct Shape<128, G> {
 #ifdef PKV_D128_WARPS
   static constexpr int kWarps = PKV_D128_WARPS;
 #else
-  static constexpr int kWarps = G == 4 ? 4 : G == 8 ? 12 : 8;
+  static constexpr int kWarps = G == 4 ? 4 : (G == 8 && !Split<G>::kMma) ? 12 : 8;
 #endif
 #ifdef PKV_D128_STAGES
   static constexpr int kStages = PKV_D128_STAGES;
 #else
-  static constexpr int kStages = G >= 4 ? 3 : 2;
+  static constexpr int kStages = (G == 4 || (G == 8 && !Split<G>::kMma)) ? 3 : 2;
 #endif
 };
 template <int G>
@@ -143,20 +165,13 @@ struct Shape<64, G> {
   static constexpr int kStages = PKV_D64_STAGES;
 };
 
-// Heads of a group are processed four at a time: a group of eight runs two warps
-// over each staged K/V tile, one per four heads, so each warp keeps the registers of
-// a four-head group and every tile is still read from HBM once.
-template <int G>
-struct Split {
-  static constexpr int kHeads = G > 4 ? 4 : G;  // q heads per warp
-  static constexpr int kWarps = G / kHeads;     // warps sharing one ring
-};
-// Shared memory of one CTA: a ring per warp group, a p tile per warp, a barrier per stage.
+// Shared memory of one CTA: a ring per warp group, a p tile per warp, a barrier per
+// stage (and, on the tensor-core path, up to 1024 bytes to align the first stage).
 template <int D, int G, int NW, int S>
 constexpr size_t ring_smem_bytes() {
   constexpr int kRings = NW / Split<G>::kWarps;
-  return size_t(kRings) * S * Geo<D, G>::kStageBytes + size_t(NW) * Geo<D, Split<G>::kHeads>::kPTileBytes +
-         size_t(kRings) * S * 8;
+  return (Split<G>::kMma ? 1024 : 0) + size_t(kRings) * S * stage_bytes<D, G>() +
+         size_t(NW) * Geo<D, Split<G>::kHeads>::kPTileBytes + size_t(kRings) * S * 8;
 }
 template <int D, int G>
 constexpr size_t static_smem_bytes() {
@@ -210,6 +225,40 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
+}
+// 2D tensor copy (box 64 dims x 16 rows of the cache, 128-byte swizzle) into shared memory.
+__device__ __forceinline__ void tensor_load(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+// Warp-level tensor-core operand loads and the m16n8k16 bf16 MMA (fp32 accumulate).
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+               : "=r"(r0), "=r"(r1)
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 __device__ __forceinline__ unsigned long long global_ns() {
   unsigned long long t;
@@ -364,6 +413,94 @@ __device__ __forceinline__ void process_block(const unsigned char* sK, const uns
 }
 
 // ---------------------------------------------------------------------------
+// One block on the tensor cores (groups of up to eight q heads, one warp).
+//
+// The stage holds K and V as 128-byte-swizzled tensor tiles: D / 64 halves of 16
+// rows x 128 bytes (2 KB, 1024-byte aligned), the 16-byte chunk c of row r stored
+// at chunk c ^ (r % 8), so every 8-row ldmatrix touches all 32 banks once.
+//
+//   S^T [16 tokens x 8 heads] = K [16 x D] . q^T [D x 8]       D / 16 MMAs m16n8k16
+//   O^T [D x 8 heads]        += V^T [D x 16] . P^T [16 x 8]    D / 16 MMAs
+//
+// Fragments (g = lane / 4, t = lane % 4): the S^T accumulator holds tokens g and
+// g + 8 of heads 2t and 2t + 1, so a lane owns the running max and sum of its two
+// heads; P goes through a 256-byte shared tile ([token][head] bf16) and comes back
+// transposed by ldmatrix.trans as the B operand; the O^T accumulator o[mt] holds
+// dims 16 mt + g and 16 mt + g + 8 of the same two heads.  Scores are scaled after
+// the MMA (fp32); the weights enter the MMA as bf16 and the sum l takes them in fp32.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t swz_addr(uint32_t tile, int row, int chunk) {
+  return tile + (chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
+}
+
+template <int D, bool kMasked>
+__device__ __forceinline__ void process_block_mma(uint32_t sK, unsigned char* sV_ptr, uint32_t sV, uint32_t sP,
+                                                  const uint32_t (&qf)[D / 16][2], float (&o)[D / 16][4],
+                                                  float (&m)[2], float (&l)[2], float qscale, int lane, int valid) {
+  const int g = lane >> 2, t = lane & 3;
+  const int mi = lane >> 3;  // which 8x8 matrix of an x4 load this lane addresses
+  // Scores: K rows are the M dimension, the heads the N dimension.
+  float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int kk = 0; kk < D / 16; ++kk) {
+    uint32_t a[4];
+    ldsm_x4(swz_addr(sK, ((mi & 1) << 3) | (lane & 7), 2 * kk + (mi >> 1)), a);
+    mma_16816(c, a, qf[kk][0], qf[kk][1]);
+  }
+  float s0 = c[0] * qscale, s1 = c[1] * qscale, s2 = c[2] * qscale, s3 = c[3] * qscale;
+  if (kMasked) {
+    if (g >= valid) s0 = s1 = -INFINITY;
+    if (g + 8 >= valid) s2 = s3 = -INFINITY;
+    // Stale rows past the sequence must not reach the MMA (0 * NaN): zero them.
+    for (int x = lane; x < (kBlockTokens - valid) * (D / 8); x += 32) {
+      const int row = valid + x / (D / 8), chunk = x % (D / 8);
+      *reinterpret_cast<uint4*>(sV_ptr + (swz_addr(0, row, chunk))) = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  // Block max of each of this lane's two heads over the 16 tokens (lanes of equal t).
+  float b0 = fmaxf(s0, s2), b1 = fmaxf(s1, s3);
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    b0 = fmaxf(b0, __shfl_xor_sync(kFull, b0, off));
+    b1 = fmaxf(b1, __shfl_xor_sync(kFull, b1, off));
+  }
+  // Lazy rescale: the running max moves only when a block beats it by more than the slack.
+  if (__any_sync(kFull, b0 > m[0] + kRescaleSlack || b1 > m[1] + kRescaleSlack)) {
+    const float n0 = fmaxf(m[0], b0), n1 = fmaxf(m[1], b1);
+    const float a0 = exp2f(m[0] - n0), a1 = exp2f(m[1] - n1);
+    m[0] = n0;
+    m[1] = n1;
+    l[0] *= a0;
+    l[1] *= a1;
+#pragma unroll
+    for (int mt = 0; mt < D / 16; ++mt) {
+      o[mt][0] *= a0;
+      o[mt][1] *= a1;
+      o[mt][2] *= a0;
+      o[mt][3] *= a1;
+    }
+  }
+  const float p0 = exp2f(s0 - m[0]), p1 = exp2f(s1 - m[1]);
+  const float p2 = exp2f(s2 - m[0]), p3 = exp2f(s3 - m[1]);
+  l[0] += p0 + p2;
+  l[1] += p1 + p3;
+  __syncwarp();  // the previous block's P tile has been read
+  unsigned char* pt = reinterpret_cast<unsigned char*>(__cvta_shared_to_generic(sP));
+  *reinterpret_cast<uint32_t*>(pt + g * 16 + t * 4) = float2_to_bf16x2(p0, p1);
+  *reinterpret_cast<uint32_t*>(pt + (g + 8) * 16 + t * 4) = float2_to_bf16x2(p2, p3);
+  __syncwarp();
+  uint32_t pb0, pb1;
+  ldsm_x2_t(sP + (lane & 15) * 16, pb0, pb1);
+  // O^T += V^T P^T: V rows are the K dimension, dims the M dimension.
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt) {
+    uint32_t a[4];
+    ldsm_x4_t(swz_addr(sV, ((mi >> 1) << 3) | (lane & 7), 2 * mt + (mi & 1)), a);
+    mma_16816(o[mt], a, pb0, pb1);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Fused decode step helpers: rotate-half RoPE of one lane's 8 dims.
 // ---------------------------------------------------------------------------
 // x: this lane's 8 values (dims 8c .. 8c+7 of a head row), y: the 8 values D/2
@@ -415,8 +552,12 @@ __device__ __forceinline__ void advance(Cursor& cur, const int* s_prefix, int nu
 }
 
 template <int D, int G, int NW, int S>
-__global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const DecodeParams p) {
+__global__ void __launch_bounds__(NW * 32)
+    paged_decode_partition_kernel(const DecodeParams p, const __grid_constant__ CUtensorMap map_k,
+                                  const __grid_constant__ CUtensorMap map_v) {
   using T = Geo<D, G>;
+  constexpr bool kMma = Split<G>::kMma;  // q.K and p.V on the tensor cores
+  constexpr int kStage = stage_bytes<D, G>();
   // SP warps share each ring, warp `sub` of a ring taking heads sub * GS .. + GS - 1.
   constexpr int GS = Split<G>::kHeads;
   constexpr int SP = Split<G>::kWarps;
@@ -430,7 +571,11 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
   const int B = p.num_seqs;
   const int hkv = p.num_kv_heads;
   unsigned char* stages = smem;
-  float2* ptiles = reinterpret_cast<float2*>(stages + size_t(NR) * S * T::kStageBytes);
+  if constexpr (kMma) {  // swizzled tensor tiles: the first stage on a 1024-byte boundary
+    const uint32_t a = smem_addr(smem);
+    stages = smem + (((a + 1023u) & ~1023u) - a);
+  }
+  float2* ptiles = reinterpret_cast<float2*>(stages + size_t(NR) * S * kStage);
   uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(ptiles) + NW * TS::kPTileBytes);
   int* s_prefix = reinterpret_cast<int*>(bars + NR * S);
   int* s_len = s_prefix + (B + 1);
@@ -490,7 +635,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
     for (int i = tid; i <= B; i += NW * 32) p.ws_prefix[i] = s_prefix[i];
 
   // --- per-ring stages ----------------------------------------------------------
-  unsigned char* ring_ptr = stages + size_t(rg) * S * T::kStageBytes;
+  unsigned char* ring_ptr = stages + size_t(rg) * S * kStage;
   const uint32_t ring = smem_addr(ring_ptr);
   const uint32_t bar0 = smem_addr(bars + rg * S);
   float2* ptile = ptiles + warp * (TS::kPTileBytes / 8);
@@ -540,12 +685,21 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
     return id;
   };
   auto issue = [&](int stage, const Cursor& cur, int id, bool with_q) {
-    const uint32_t dst = ring + stage * T::kStageBytes;
+    const uint32_t dst = ring + stage * kStage;
     const uint32_t bar = bar0 + 8 * stage;
     mbar_arrive_expect_tx(bar, 2 * T::kTileBytes + (with_q ? T::kQBytes : 0));
-    const size_t tile = (static_cast<size_t>(id) * hkv + cur.kvh) * (kBlockTokens * D);
-    bulk_load(dst, kbase + tile, T::kTileBytes, bar);
-    bulk_load(dst + T::kTileBytes, vbase + tile, T::kTileBytes, bar);
+    if constexpr (kMma) {
+      const int row = (id * hkv + cur.kvh) * kBlockTokens;  // < 2^31: checked on the host
+#pragma unroll
+      for (int h = 0; h < D / 64; ++h) {
+        tensor_load(dst + h * 2048, &map_k, 64 * h, row, bar);
+        tensor_load(dst + T::kTileBytes + h * 2048, &map_v, 64 * h, row, bar);
+      }
+    } else {
+      const size_t tile = (static_cast<size_t>(id) * hkv + cur.kvh) * (kBlockTokens * D);
+      bulk_load(dst, kbase + tile, T::kTileBytes, bar);
+      bulk_load(dst + T::kTileBytes, vbase + tile, T::kTileBytes, bar);
+    }
     if (with_q)
       bulk_load(dst + 2 * T::kTileBytes, qbase + (static_cast<size_t>(cur.b) * p.num_q_heads + cur.kvh * G) * D,
                 T::kQBytes, bar);
@@ -578,6 +732,10 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
   const float qscale = p.qscale;
 
   const int h0 = sub * GS;  // first q head of this warp within the group
+  // Tensor-core path: q^T fragments (bf16), the O^T accumulator, two heads' max and sum.
+  uint32_t qf[D / 16][2];
+  float o_t[D / 16][4];
+  float m2[2], l2[2];
   float2 q[GS][4];          // q[gp]: head h0 + (gp ^ mg), swizzled per lane
   float2 acc[GS][4];        // acc[g]: head h0 + g
   float m_ref[GS];
@@ -588,7 +746,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
   int stage = 0;
   uint32_t phase = 0;
   for (int i = 0; i < n; ++i) {
-    const unsigned char* st_ptr = ring_ptr + stage * T::kStageBytes;
+    const unsigned char* st_ptr = ring_ptr + stage * kStage;
     const bool landed = mbar_wait(bar0 + 8 * stage, phase, kWaitTimeoutNs);
     bool all_landed;
     if constexpr (SP > 1) all_landed = ring_all(landed, ring_bar, SP * 32);  // the ring's warps decide together
@@ -613,25 +771,65 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
         }
         cs_row = p.cos_sin + pos * D;
       }
+      if constexpr (kMma) {
+        if (cs_row != nullptr) {
+          // Rotate the group's q rows in place; the result is rounded to bf16, as the
+          // oracle rounds it, and enters the MMA unchanged.
+          constexpr int kChunks = G * D / 8;
+          constexpr int kPer = (kChunks + 31) / 32;
+          unsigned char* sqw = ring_ptr + stage * kStage + 2 * T::kTileBytes;
+          uint4 rot[kPer];
 #pragma unroll
-      for (int gp = 0; gp < GS; ++gp) {
-        const int head = h0 + (gp ^ mg);
-        uint4 w = lds128(sq + head * (D * 2) + c * 16);
-        if (cs_row != nullptr)
-          w = rope_chunk<D>(w, lds128(sq + head * (D * 2) + ((c * 16 + D) % (D * 2))), cs_row, c);
-        const float2 s2 = make_float2(qscale, qscale);
-        q[gp][0] = __fmul2_rn(bf16x2_to_float2(w.x), s2);
-        q[gp][1] = __fmul2_rn(bf16x2_to_float2(w.y), s2);
-        q[gp][2] = __fmul2_rn(bf16x2_to_float2(w.z), s2);
-        q[gp][3] = __fmul2_rn(bf16x2_to_float2(w.w), s2);
+          for (int x = 0; x < kPer; ++x) {
+            const int idx = lane + 32 * x;
+            if (idx < kChunks) {
+              const int head = idx / (D / 8), ch = idx % (D / 8);
+              rot[x] = rope_chunk<D>(lds128(sq + head * (D * 2) + ch * 16),
+                                     lds128(sq + head * (D * 2) + ((ch * 16 + D) % (D * 2))), cs_row, ch);
+            }
+          }
+          __syncwarp();
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[gp][e] = make_float2(0.f, 0.f);
-        m_ref[gp] = -INFINITY;
-      }
+          for (int x = 0; x < kPer; ++x) {
+            const int idx = lane + 32 * x;
+            if (idx < kChunks)
+              *reinterpret_cast<uint4*>(sqw + (idx / (D / 8)) * (D * 2) + (idx % (D / 8)) * 16) = rot[x];
+          }
+          __syncwarp();
+        }
+        // q^T B fragments: head g (a zero column past the group), dims 16 kk + 2t (+1) and + 8.
+        const int gq = lane >> 2, tq = lane & 3;
 #pragma unroll
-      for (int k = 0; k < TS::kFinal; ++k) {
-        m_mine[k] = -INFINITY;
-        l_mine[k] = 0.f;
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const unsigned char* qrow = sq + gq * (D * 2) + (16 * kk + 2 * tq) * 2;
+          qf[kk][0] = gq < G ? *reinterpret_cast<const uint32_t*>(qrow) : 0u;
+          qf[kk][1] = gq < G ? *reinterpret_cast<const uint32_t*>(qrow + 16) : 0u;
+        }
+#pragma unroll
+        for (int mt = 0; mt < D / 16; ++mt) o_t[mt][0] = o_t[mt][1] = o_t[mt][2] = o_t[mt][3] = 0.f;
+        m2[0] = m2[1] = -INFINITY;
+        l2[0] = l2[1] = 0.f;
+      } else {
+#pragma unroll
+        for (int gp = 0; gp < GS; ++gp) {
+          const int head = h0 + (gp ^ mg);
+          uint4 w = lds128(sq + head * (D * 2) + c * 16);
+          if (cs_row != nullptr)
+            w = rope_chunk<D>(w, lds128(sq + head * (D * 2) + ((c * 16 + D) % (D * 2))), cs_row, c);
+          const float2 s2 = make_float2(qscale, qscale);
+          q[gp][0] = __fmul2_rn(bf16x2_to_float2(w.x), s2);
+          q[gp][1] = __fmul2_rn(bf16x2_to_float2(w.y), s2);
+          q[gp][2] = __fmul2_rn(bf16x2_to_float2(w.z), s2);
+          q[gp][3] = __fmul2_rn(bf16x2_to_float2(w.w), s2);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[gp][e] = make_float2(0.f, 0.f);
+          m_ref[gp] = -INFINITY;
+        }
+#pragma unroll
+        for (int k = 0; k < TS::kFinal; ++k) {
+          m_mine[k] = -INFINITY;
+          l_mine[k] = 0.f;
+        }
       }
       pair_from_start = (cc.blk == 0);
     }
@@ -651,9 +849,10 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
           if (pos >= p.max_position) pos = p.max_position - 1;
           kw = rope_chunk<D>(kw, __ldg(kn + (c + D / 16) % (D / 8)), p.cos_sin + pos * D, c);
         }
-        unsigned char* st_w = ring_ptr + stage * T::kStageBytes;
-        *reinterpret_cast<uint4*>(st_w + row * (D * 2) + c * 16) = kw;
-        *reinterpret_cast<uint4*>(st_w + T::kTileBytes + row * (D * 2) + c * 16) = vw;
+        unsigned char* st_w = ring_ptr + stage * kStage;
+        const uint32_t at = kMma ? swz_addr(0, row, c) : static_cast<uint32_t>(row * (D * 2) + c * 16);
+        *reinterpret_cast<uint4*>(st_w + at) = kw;
+        *reinterpret_cast<uint4*>(st_w + T::kTileBytes + at) = vw;
         int id = __ldg(p.block_tables + static_cast<size_t>(cc.b) * p.max_blocks_per_seq + cc.blk);
         if (id >= 0 && id < p.num_blocks) {
           const size_t dst = ((static_cast<size_t>(id) * hkv + cc.kvh) * kBlockTokens + row) * D;
@@ -664,12 +863,23 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
       if constexpr (SP > 1) ring_sync(ring_bar, SP * 32);  // the row is in the stage for every warp
       else __syncwarp();
     }
-    if (valid >= kBlockTokens)
-      process_block<D, GS, false>(st_ptr, st_ptr + T::kTileBytes, ptile, q, acc, m_ref, m_mine, l_mine, c, half,
-                                  mask, kBlockTokens);
-    else
-      process_block<D, GS, true>(st_ptr, st_ptr + T::kTileBytes, ptile, q, acc, m_ref, m_mine, l_mine, c, half,
-                                 mask, valid);
+    if constexpr (kMma) {
+      const uint32_t sk = ring + stage * kStage;
+      unsigned char* sv_ptr = ring_ptr + stage * kStage + T::kTileBytes;
+      if (valid >= kBlockTokens)
+        process_block_mma<D, false>(sk, sv_ptr, sk + T::kTileBytes, smem_addr(ptile), qf, o_t, m2, l2, qscale, lane,
+                                    kBlockTokens);
+      else
+        process_block_mma<D, true>(sk, sv_ptr, sk + T::kTileBytes, smem_addr(ptile), qf, o_t, m2, l2, qscale, lane,
+                                   valid);
+    } else {
+      if (valid >= kBlockTokens)
+        process_block<D, GS, false>(st_ptr, st_ptr + T::kTileBytes, ptile, q, acc, m_ref, m_mine, l_mine, c, half,
+                                    mask, kBlockTokens);
+      else
+        process_block<D, GS, true>(st_ptr, st_ptr + T::kTileBytes, ptile, q, acc, m_ref, m_mine, l_mine, c, half,
+                                   mask, valid);
+    }
     if constexpr (SP > 1) ring_sync(ring_bar, SP * 32);  // every warp of the ring is done with the stage
     else __syncwarp();
 
@@ -685,6 +895,58 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
 
     const bool last_of_pair = (cc.blk == cc.nblk - 1);
     if (last_of_pair || i == n - 1) {
+      if constexpr (kMma) {
+        // Sum each head's l over the eight lanes that share it, then finish the pair
+        // (O / l in bf16) or park its partial state (O, m, l in fp32).
+        float la = l2[0], lb = l2[1];
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+          la += __shfl_xor_sync(kFull, la, off);
+          lb += __shfl_xor_sync(kFull, lb, off);
+        }
+        const int go = lane >> 2, ha = 2 * (lane & 3), hb = ha + 1;
+        if (pair_from_start && last_of_pair) {
+          __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
+                                (static_cast<size_t>(cc.b) * p.num_q_heads + cc.kvh * G) * D;
+          const float ia = 1.0f / la, ib = 1.0f / lb;
+#pragma unroll
+          for (int mt = 0; mt < D / 16; ++mt) {
+            const int d0 = 16 * mt + go, d1 = d0 + 8;
+            if (ha < G) {
+              orow[ha * D + d0] = __float2bfloat16_rn(o_t[mt][0] * ia);
+              orow[ha * D + d1] = __float2bfloat16_rn(o_t[mt][2] * ia);
+            }
+            if (hb < G) {
+              orow[hb * D + d0] = __float2bfloat16_rn(o_t[mt][1] * ib);
+              orow[hb * D + d1] = __float2bfloat16_rn(o_t[mt][3] * ib);
+            }
+          }
+        } else {
+          float* piece = p.ws_pieces + (static_cast<size_t>(gw) * 2 + (first_pair ? 0 : 1)) * T::kPieceFloats;
+#pragma unroll
+          for (int mt = 0; mt < D / 16; ++mt) {
+            const int d0 = 16 * mt + go, d1 = d0 + 8;
+            if (ha < G) {
+              piece[ha * D + d0] = o_t[mt][0];
+              piece[ha * D + d1] = o_t[mt][2];
+            }
+            if (hb < G) {
+              piece[hb * D + d0] = o_t[mt][1];
+              piece[hb * D + d1] = o_t[mt][3];
+            }
+          }
+          if (go == 0) {
+            if (ha < G) {
+              piece[G * D + ha] = m2[0];
+              piece[G * D + G + ha] = la;
+            }
+            if (hb < G) {
+              piece[G * D + hb] = m2[1];
+              piece[G * D + G + hb] = lb;
+            }
+          }
+        }
+      } else {
       // Combine the token-parity lanes, then finish the pair or park its partial state.
 #pragma unroll
       for (int off = TS::kLanesPerToken; off < 32; off <<= 1)
@@ -737,6 +999,7 @@ __global__ void __launch_bounds__(NW * 32) paged_decode_partition_kernel(const D
             piece[G * D + G + h0 + g] = l_all[g];
           }
         }
+      }
       }
       first_pair = false;
     }
@@ -889,8 +1152,15 @@ struct Instance {
     if (e != cudaSuccess) return e;
     if ((e = prepare(dev)) != cudaSuccess) return e;
     const unsigned grid = static_cast<unsigned>((p.num_partitions + NR - 1) / NR);
+    CUtensorMap mk{}, mv{};
+    if constexpr (Split<G>::kMma) {  // the caches as swizzled tensor tiles
+      const int64_t rows = p.num_blocks * p.num_kv_heads * kBlockTokens;
+      if (rows > INT32_MAX) return cudaErrorInvalidValue;  // tensor-copy row coordinates are 32-bit
+      if ((e = encode_cache_map(&mk, p.k_cache, rows, D)) != cudaSuccess) return e;
+      if ((e = encode_cache_map(&mv, p.v_cache, rows, D)) != cudaSuccess) return e;
+    }
     return launch_pdl(paged_decode_partition_kernel<D, G, NW, S>, dim3(grid), dim3(NW * 32),
-                      partition_smem_bytes<D, G>(p.num_seqs), stream, p);
+                      partition_smem_bytes<D, G>(p.num_seqs), stream, p, mk, mv);
   }
 
   static cudaError_t merge(const DecodeParams& p, cudaStream_t stream) {

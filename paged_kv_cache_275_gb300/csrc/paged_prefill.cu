@@ -728,6 +728,10 @@ cudaError_t launch_t(const PrefillParams& p, int max_query_len, cudaStream_t str
 
 }  // namespace
 
+cudaError_t encode_cache_map(CUtensorMap_st* map, const void* cache, int64_t rows, int head_dim) {
+  return cache_map(map, cache, rows, head_dim);
+}
+
 cudaError_t launch_paged_prefill(const PrefillParams& p, int head_dim, int group, int max_query_len,
                                  cudaStream_t stream) {
   switch (head_dim * 16 + group) {

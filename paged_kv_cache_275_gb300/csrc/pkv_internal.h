@@ -8,6 +8,8 @@
 
 #include <cuda_runtime.h>
 
+struct CUtensorMap_st;  // cuda.h's tensor-map type (CUtensorMap)
+
 namespace pkv {
 
 constexpr int kBlockTokens = 16;  // tokens per KV block
@@ -101,6 +103,9 @@ size_t workspace_header_bytes(int num_seqs);
 // Pieces the partition kernel keeps in flight on the current device: one per warp,
 // or per pair of warps for groups of eight q heads (the default num_partitions).
 cudaError_t resident_partition_pieces(int head_dim, int group, int num_seqs, int* pieces);
+// Tensor map of a cache viewed as [rows = num_blocks * num_kv_heads * 16][head_dim] bf16, box 16 rows x
+// 64 dims, 128-byte swizzle (the tensor-copy layout of the prefill kernel and of the decode tensor-core path).
+cudaError_t encode_cache_map(CUtensorMap_st* map, const void* cache, int64_t rows, int head_dim);
 // One warp waiting on a barrier that nothing completes, for at most limit_ns (the bounded-wait self-test).
 cudaError_t launch_bounded_wait_selftest(unsigned* err, unsigned long long limit_ns, cudaStream_t stream);
 // Decode kernels.  `group` = num_q_heads / num_kv_heads.
