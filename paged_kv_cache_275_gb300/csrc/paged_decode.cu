@@ -110,9 +110,11 @@ struct Geo {
 };
 
 // Groups of PKV_MMA_MIN_G to 8 q heads run q.K and p.V on the tensor cores (warp-level
-// mma.sync, the group's heads as the N = 8 columns), one warp per ring.  Otherwise
-// the CUDA cores take at most four heads per warp: a group of eight then runs two
-// warps over each staged K/V tile, one per four heads, each tile still read once.
+// mma.sync, the group's heads as the N = 8 columns), one warp per ring: at eight heads
+// the CUDA cores are held back by the arithmetic (8 flop per byte), while for four or
+// fewer they are bound by HBM and the tensor cores gain nothing (LLaMA-3-8B shape: 206
+// against 204 us).  Otherwise the CUDA cores take at most four heads per warp: a group
+// of eight then runs two warps over each staged K/V tile, one per four heads.
 #ifndef PKV_MMA_MIN_G
 #define PKV_MMA_MIN_G 8
 #endif
@@ -136,8 +138,8 @@ constexpr int stage_bytes() {
 // warps keep more copies moving (Qwen3-shape trace: 6.20 against 5.76 TB/s); eight
 // heads on the CUDA cores, two warps to a ring, with twelve warps of three stages
 // (LLaMA-3-70B shape: 323 us, against 328-330 with 12 x 2 or 16 x 2 and 404 with
-// 8 x 2), and on the tensor cores with eight warps of two.  The macros override the
-// D = 128 shape for every group, for sweeps.
+// 8 x 2), and on the tensor cores with eight warps of two (201-202 us; 4 x 2 the
+// same, 4 x 4 226).  The macros override the D = 128 shape for every group, for sweeps.
 #ifndef PKV_D64_WARPS
 #define PKV_D64_WARPS 4
 #endif
