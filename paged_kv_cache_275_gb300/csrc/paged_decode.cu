@@ -109,20 +109,18 @@ struct Geo {
   }
 };
 
-// Groups of PKV_MMA_MIN_G to 8 q heads run q.K and p.V on the tensor cores (warp-level
-// mma.sync, the group's heads as the N = 8 columns), one warp per ring: at eight heads
+// Groups of PKV_MMA_MIN_G (at most 8) or more q heads run q.K and p.V on the tensor
+// cores (warp-level mma.sync, the group's heads as the N = 8 columns): at eight heads
 // the CUDA cores are held back by the arithmetic (8 flop per byte), while for four or
 // fewer they are bound by HBM and the tensor cores gain nothing (LLaMA-3-8B shape: 206
-// against 204 us).  Otherwise the CUDA cores take at most four heads per warp: a group
-// of eight then runs two warps over each staged K/V tile, one per four heads.
+// against 204 us).  Either way one warp owns a ring and all the group's heads.
 #ifndef PKV_MMA_MIN_G
 #define PKV_MMA_MIN_G 8
 #endif
+static_assert(PKV_MMA_MIN_G >= 1 && PKV_MMA_MIN_G <= 8, "groups of eight always take the tensor cores");
 template <int G>
 struct Split {
-  static constexpr bool kMma = G >= PKV_MMA_MIN_G && G <= 8;
-  static constexpr int kHeads = kMma ? G : (G > 4 ? 4 : G);  // q heads per warp
-  static constexpr int kWarps = G / kHeads;                   // warps sharing one ring
+  static constexpr bool kMma = G >= PKV_MMA_MIN_G;
 };
 // One ring stage: K tile | V tile | q rows.  The tensor-core path copies K and V as
 // 128-byte-swizzled tensor tiles, whose stages start on 1024-byte boundaries.
@@ -131,15 +129,14 @@ constexpr int stage_bytes() {
   return Split<G>::kMma ? (Geo<D, G>::kStageBytes + 1023) / 1024 * 1024 : Geo<D, G>::kStageBytes;
 }
 
-// Launch shape per (head_dim, group): warps per CTA and stages per ring.  At
+// Launch shape per (head_dim, group): warps per CTA and stages per warp's ring.  At
 // D = 128, four q heads per kv head run best with four warps of three stages
 // (LLaMA-3 shape: 201.6 against 209.6 us with eight warps of two); one or two heads
 // with eight warps of two stages, since they do little arithmetic per byte and more
 // warps keep more copies moving (Qwen3-shape trace: 6.20 against 5.76 TB/s); eight
-// heads on the CUDA cores, two warps to a ring, with twelve warps of three stages
-// (LLaMA-3-70B shape: 323 us, against 328-330 with 12 x 2 or 16 x 2 and 404 with
-// 8 x 2), and on the tensor cores with eight warps of two (201-202 us; 4 x 2 the
-// same, 4 x 4 226).  The macros override the D = 128 shape for every group, for sweeps.
+// heads, on the tensor cores, with eight warps of two as well (LLaMA-3-70B shape:
+// 201-202 us; 4 x 2 the same, 4 x 4 226).  The macros override the D = 128 shape
+// for every group, for sweeps.
 #ifndef PKV_D64_WARPS
 #define PKV_D64_WARPS 4
 #endif
@@ -153,12 +150,12 @@ struct Shape<128, G> {
 #ifdef PKV_D128_WARPS
   static constexpr int kWarps = PKV_D128_WARPS;
 #else
-  static constexpr int kWarps = G == 4 ? 4 : (G == 8 && !Split<G>::kMma) ? 12 : 8;
+  static constexpr int kWarps = G == 4 ? 4 : 8;
 #endif
 #ifdef PKV_D128_STAGES
   static constexpr int kStages = PKV_D128_STAGES;
 #else
-  static constexpr int kStages = (G == 4 || (G == 8 && !Split<G>::kMma)) ? 3 : 2;
+  static constexpr int kStages = G == 4 ? 3 : 2;
 #endif
 };
 template <int G>
@@ -167,13 +164,12 @@ struct Shape<64, G> {
   static constexpr int kStages = PKV_D64_STAGES;
 };
 
-// Shared memory of one CTA: a ring per warp group, a p tile per warp, a barrier per
-// stage (and, on the tensor-core path, up to 1024 bytes to align the first stage).
+// Shared memory of one CTA: a ring and a p tile per warp, a barrier per stage (and, on
+// the tensor-core path, up to 1024 bytes to align the first stage).
 template <int D, int G, int NW, int S>
 constexpr size_t ring_smem_bytes() {
-  constexpr int kRings = NW / Split<G>::kWarps;
-  return (Split<G>::kMma ? 1024 : 0) + size_t(kRings) * S * stage_bytes<D, G>() +
-         size_t(NW) * Geo<D, Split<G>::kHeads>::kPTileBytes + size_t(kRings) * S * 8;
+  return (Split<G>::kMma ? 1024 : 0) + size_t(NW) * S * stage_bytes<D, G>() + size_t(NW) * Geo<D, G>::kPTileBytes +
+         size_t(NW) * S * 8;
 }
 template <int D, int G>
 constexpr size_t static_smem_bytes() {
@@ -268,21 +264,6 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 // Wait for phase `parity` of an mbarrier, giving up after `limit_ns`.
-// Named barrier over the `count` threads of one ring's warps (id 1 + ring; 0 is __syncthreads).
-__device__ __forceinline__ void ring_sync(int id, int count) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-// The same barrier, returning whether `v` holds on every participating thread.
-__device__ __forceinline__ bool ring_all(bool v, int id, int count) {
-  int r;
-  asm volatile(
-      "{\n\t.reg .pred pv, pa;\n\tsetp.ne.s32 pv, %1, 0;\n\tbar.red.and.pred pa, %2, %3, pv;\n\t"
-      "selp.s32 %0, 1, 0, pa;\n\t}"
-      : "=r"(r)
-      : "r"(v ? 1 : 0), "r"(id), "r"(count)
-      : "memory");
-  return r != 0;
-}
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
@@ -560,13 +541,7 @@ __global__ void __launch_bounds__(NW * 32)
   using T = Geo<D, G>;
   constexpr bool kMma = Split<G>::kMma;  // q.K and p.V on the tensor cores
   constexpr int kStage = stage_bytes<D, G>();
-  // SP warps share each ring, warp `sub` of a ring taking heads sub * GS .. + GS - 1.
-  constexpr int GS = Split<G>::kHeads;
-  constexpr int SP = Split<G>::kWarps;
-  constexpr int NR = NW / SP;  // rings (pieces in flight) per CTA
-  using TS = Geo<D, GS>;
-  static_assert(TS::valid() && G % GS == 0 && NW % SP == 0, "unsupported (head_dim, group) geometry");
-  static_assert(SP == 1 || NR <= 15, "one named barrier per ring");
+  static_assert(kMma || T::valid(), "unsupported (head_dim, group) geometry");
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int s_wsum[32];
 
@@ -577,18 +552,15 @@ __global__ void __launch_bounds__(NW * 32)
     const uint32_t a = smem_addr(smem);
     stages = smem + (((a + 1023u) & ~1023u) - a);
   }
-  float2* ptiles = reinterpret_cast<float2*>(stages + size_t(NR) * S * kStage);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(ptiles) + NW * TS::kPTileBytes);
-  int* s_prefix = reinterpret_cast<int*>(bars + NR * S);
+  float2* ptiles = reinterpret_cast<float2*>(stages + size_t(NW) * S * kStage);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<unsigned char*>(ptiles) + NW * T::kPTileBytes);
+  int* s_prefix = reinterpret_cast<int*>(bars + NW * S);
   int* s_len = s_prefix + (B + 1);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  const int rg = warp / SP;   // this warp's ring
-  const int sub = warp % SP;  // its four-head sub-group
-  const int ring_bar = 1 + rg;
-  const bool producer = lane == 0 && sub == 0;
+  const bool producer = lane == 0;  // issues this warp's copies
   pdl_trigger();
   pdl_wait();
 
@@ -636,21 +608,20 @@ __global__ void __launch_bounds__(NW * 32)
   if (blockIdx.x == 0)
     for (int i = tid; i <= B; i += NW * 32) p.ws_prefix[i] = s_prefix[i];
 
-  // --- per-ring stages ----------------------------------------------------------
-  unsigned char* ring_ptr = stages + size_t(rg) * S * kStage;
+  // --- per-warp ring ----------------------------------------------------------
+  unsigned char* ring_ptr = stages + size_t(warp) * S * kStage;
   const uint32_t ring = smem_addr(ring_ptr);
-  const uint32_t bar0 = smem_addr(bars + rg * S);
-  float2* ptile = ptiles + warp * (TS::kPTileBytes / 8);
+  const uint32_t bar0 = smem_addr(bars + warp * S);
+  float2* ptile = ptiles + warp * (T::kPTileBytes / 8);
   if (producer) {
 #pragma unroll
     for (int s = 0; s < S; ++s) mbar_init(bar0 + 8 * s, 1);
     fence_mbar_init();
   }
-  if constexpr (SP > 1) __syncthreads();  // every warp of the CTA is still here
-  else __syncwarp();
+  __syncwarp();
 
   const long long total = static_cast<long long>(hkv) * s_prefix[B];
-  const int gw = blockIdx.x * NR + rg;  // the piece: the same for the warps of a ring
+  const int gw = blockIdx.x * NW + warp;  // this warp's piece
   if (gw >= p.num_partitions || total == 0) return;
   const long long begin = gw * total / p.num_partitions;
   const long long end = (gw + 1) * total / p.num_partitions;
@@ -727,21 +698,21 @@ __global__ void __launch_bounds__(NW * 32)
     next_id = ids[S];
   }
 
-  const int c = lane & (TS::kLanesPerToken - 1);
-  const int half = lane / TS::kLanesPerToken;
-  const int mask = TS::mask_of(c);
-  const int mg = mask % GS;
+  const int c = lane & (T::kLanesPerToken - 1);
+  const int half = lane / T::kLanesPerToken;
+  const int mask = T::mask_of(c);
+  const int mg = mask % G;
   const float qscale = p.qscale;
 
-  const int h0 = sub * GS;  // first q head of this warp within the group
   // Tensor-core path: q^T fragments (bf16), the O^T accumulator, two heads' max and sum.
   uint32_t qf[D / 16][2];
   float o_t[D / 16][4];
   float m2[2], l2[2];
-  float2 q[GS][4];          // q[gp]: head h0 + (gp ^ mg), swizzled per lane
-  float2 acc[GS][4];        // acc[g]: head h0 + g
-  float m_ref[GS];
-  float m_mine[TS::kFinal], l_mine[TS::kFinal];
+  // CUDA-core path: q and the accumulators per head (swizzled per lane), the maxima and sums.
+  float2 q[G][4];  // q[gp]: head gp ^ mg
+  float2 acc[G][4];
+  float m_ref[G];
+  float m_mine[T::kFinal], l_mine[T::kFinal];
   bool pair_from_start = false;
   bool first_pair = true;
 
@@ -750,10 +721,7 @@ __global__ void __launch_bounds__(NW * 32)
   for (int i = 0; i < n; ++i) {
     const unsigned char* st_ptr = ring_ptr + stage * kStage;
     const bool landed = mbar_wait(bar0 + 8 * stage, phase, kWaitTimeoutNs);
-    bool all_landed;
-    if constexpr (SP > 1) all_landed = ring_all(landed, ring_bar, SP * 32);  // the ring's warps decide together
-    else all_landed = __all_sync(kFull, landed);
-    if (!all_landed) {
+    if (!__all_sync(kFull, landed)) {
       // Give up on this piece: flag it, let the copies already in flight land, leave.
       if (lane == 0) atomicOr(p.err, kErrTimeout);
       for (int x = i; x < n && x < i + S; ++x) mbar_wait(bar0 + 8 * (x % S), (x / S) & 1, kDrainTimeoutNs);
@@ -813,8 +781,8 @@ __global__ void __launch_bounds__(NW * 32)
         l2[0] = l2[1] = 0.f;
       } else {
 #pragma unroll
-        for (int gp = 0; gp < GS; ++gp) {
-          const int head = h0 + (gp ^ mg);
+        for (int gp = 0; gp < G; ++gp) {
+          const int head = gp ^ mg;
           uint4 w = lds128(sq + head * (D * 2) + c * 16);
           if (cs_row != nullptr)
             w = rope_chunk<D>(w, lds128(sq + head * (D * 2) + ((c * 16 + D) % (D * 2))), cs_row, c);
@@ -828,7 +796,7 @@ __global__ void __launch_bounds__(NW * 32)
           m_ref[gp] = -INFINITY;
         }
 #pragma unroll
-        for (int k = 0; k < TS::kFinal; ++k) {
+        for (int k = 0; k < T::kFinal; ++k) {
           m_mine[k] = -INFINITY;
           l_mine[k] = 0.f;
         }
@@ -840,7 +808,7 @@ __global__ void __launch_bounds__(NW * 32)
       // Fused step: this block holds position len - 1, the step's new token.  Put its
       // (rotated) K row and its V row into the staged tiles and append them to the cache.
       const int row = (seq_len - 1) % kBlockTokens;
-      if (half == 0 && sub == 0) {
+      if (half == 0) {
         const size_t src = (static_cast<size_t>(cc.b) * hkv + cc.kvh) * D;
         const uint4* kn = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.k_new) + src);
         const uint4* vn = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.v_new) + src);
@@ -862,8 +830,7 @@ __global__ void __launch_bounds__(NW * 32)
           reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(const_cast<void*>(p.v_cache)) + dst)[c] = vw;
         }
       }
-      if constexpr (SP > 1) ring_sync(ring_bar, SP * 32);  // the row is in the stage for every warp
-      else __syncwarp();
+      __syncwarp();
     }
     if constexpr (kMma) {
       const uint32_t sk = ring + stage * kStage;
@@ -876,14 +843,13 @@ __global__ void __launch_bounds__(NW * 32)
                                    valid);
     } else {
       if (valid >= kBlockTokens)
-        process_block<D, GS, false>(st_ptr, st_ptr + T::kTileBytes, ptile, q, acc, m_ref, m_mine, l_mine, c, half,
+        process_block<D, G, false>(st_ptr, st_ptr + T::kTileBytes, ptile, q, acc, m_ref, m_mine, l_mine, c, half,
                                     mask, kBlockTokens);
       else
-        process_block<D, GS, true>(st_ptr, st_ptr + T::kTileBytes, ptile, q, acc, m_ref, m_mine, l_mine, c, half,
+        process_block<D, G, true>(st_ptr, st_ptr + T::kTileBytes, ptile, q, acc, m_ref, m_mine, l_mine, c, half,
                                    mask, valid);
     }
-    if constexpr (SP > 1) ring_sync(ring_bar, SP * 32);  // every warp of the ring is done with the stage
-    else __syncwarp();
+    __syncwarp();
 
     // Refill the stage just consumed with block i + S.
     if (producer && i + S < n) {
@@ -951,22 +917,22 @@ __global__ void __launch_bounds__(NW * 32)
       } else {
       // Combine the token-parity lanes, then finish the pair or park its partial state.
 #pragma unroll
-      for (int off = TS::kLanesPerToken; off < 32; off <<= 1)
+      for (int off = T::kLanesPerToken; off < 32; off <<= 1)
 #pragma unroll
-        for (int g = 0; g < GS; ++g)
+        for (int g = 0; g < G; ++g)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             acc[g][e].x += __shfl_xor_sync(kFull, acc[g][e].x, off);
             acc[g][e].y += __shfl_xor_sync(kFull, acc[g][e].y, off);
           }
 #pragma unroll
-      for (int k = 0; k < TS::kFinal; ++k)
+      for (int k = 0; k < T::kFinal; ++k)
 #pragma unroll
         for (int bit = 1; bit < 32; bit <<= 1)
-          if (TS::sum_bits() & bit) l_mine[k] += __shfl_xor_sync(kFull, l_mine[k], bit);
-      float l_all[GS];
+          if (T::sum_bits() & bit) l_mine[k] += __shfl_xor_sync(kFull, l_mine[k], bit);
+      float l_all[G];
 #pragma unroll
-      for (int g = 0; g < GS; ++g) l_all[g] = __shfl_sync(kFull, l_mine[g % TS::kFinal], TS::src_lane(g));
+      for (int g = 0; g < G; ++g) l_all[g] = __shfl_sync(kFull, l_mine[g % T::kFinal], T::src_lane(g));
 
       if (pair_from_start && last_of_pair) {
         if (half == 0) {
@@ -974,31 +940,31 @@ __global__ void __launch_bounds__(NW * 32)
                                                  (static_cast<size_t>(cc.b) * p.num_q_heads + cc.kvh * G) * D) +
                         c;
 #pragma unroll
-          for (int g = 0; g < GS; ++g) {
+          for (int g = 0; g < G; ++g) {
             const float inv = 1.0f / l_all[g];
             uint4 o;
             o.x = float2_to_bf16x2(acc[g][0].x * inv, acc[g][0].y * inv);
             o.y = float2_to_bf16x2(acc[g][1].x * inv, acc[g][1].y * inv);
             o.z = float2_to_bf16x2(acc[g][2].x * inv, acc[g][2].y * inv);
             o.w = float2_to_bf16x2(acc[g][3].x * inv, acc[g][3].y * inv);
-            orow[(h0 + g) * (D / 8)] = o;
+            orow[g * (D / 8)] = o;
           }
         }
       } else {
         float* piece = p.ws_pieces + (static_cast<size_t>(gw) * 2 + (first_pair ? 0 : 1)) * T::kPieceFloats;
         if (half == 0) {
 #pragma unroll
-          for (int g = 0; g < GS; ++g) {
-            float4* dst = reinterpret_cast<float4*>(piece + (h0 + g) * D + c * 8);
+          for (int g = 0; g < G; ++g) {
+            float4* dst = reinterpret_cast<float4*>(piece + g * D + c * 8);
             dst[0] = make_float4(acc[g][0].x, acc[g][0].y, acc[g][1].x, acc[g][1].y);
             dst[1] = make_float4(acc[g][2].x, acc[g][2].y, acc[g][3].x, acc[g][3].y);
           }
         }
         if (lane == 0) {
 #pragma unroll
-          for (int g = 0; g < GS; ++g) {
-            piece[G * D + h0 + g] = m_ref[g];
-            piece[G * D + G + h0 + g] = l_all[g];
+          for (int g = 0; g < G; ++g) {
+            piece[G * D + g] = m_ref[g];
+            piece[G * D + G + g] = l_all[g];
           }
         }
       }
@@ -1110,7 +1076,6 @@ template <int D, int G>
 struct Instance {
   static constexpr int NW = Shape<D, G>::kWarps;
   static constexpr int S = Shape<D, G>::kStages;
-  static constexpr int NR = NW / Split<G>::kWarps;  // pieces in flight per CTA
   static void* partition_fn() { return reinterpret_cast<void*>(&paged_decode_partition_kernel<D, G, NW, S>); }
 
   static cudaError_t prepare(int dev) {
@@ -1144,7 +1109,7 @@ struct Instance {
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, &paged_decode_partition_kernel<D, G, NW, S>,
                                                       NW * 32, partition_smem_bytes<D, G>(num_seqs));
     if (e != cudaSuccess) return e;
-    *pieces = sms * (per_sm > 0 ? per_sm : 1) * NR;
+    *pieces = sms * (per_sm > 0 ? per_sm : 1) * NW;
     return cudaSuccess;
   }
 
@@ -1153,7 +1118,7 @@ struct Instance {
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if ((e = prepare(dev)) != cudaSuccess) return e;
-    const unsigned grid = static_cast<unsigned>((p.num_partitions + NR - 1) / NR);
+    const unsigned grid = static_cast<unsigned>((p.num_partitions + NW - 1) / NW);
     CUtensorMap mk{}, mv{};
     if constexpr (Split<G>::kMma) {  // the caches as swizzled tensor tiles
       const int64_t rows = p.num_blocks * p.num_kv_heads * kBlockTokens;
