@@ -251,14 +251,16 @@ def test_bad_block_id_and_lengths_are_flagged():
     assert device_errors() == 0
 
 
-def test_largest_batch():
+@pytest.mark.parametrize("head_dim,hq,hkv", [(64, 8, 2), (128, 16, 2)])
+def test_largest_batch(head_dim, hq, hkv):
     """num_seqs = PKV_MAX_SEQS (4096) short sequences, empty ones among them: every CTA ranks and
-    prefixes the whole batch in shared memory."""
+    prefixes the whole batch in shared memory (at D = 128 with eight q heads per kv head, next to the
+    largest ring of swizzled tensor-copy stages)."""
     import random
     rng = random.Random(77)
     lens = tuple(rng.choice([0, rng.randint(1, 40)]) for _ in range(pkv.MAX_SEQS))
-    spec = DecodeSpec(name="max_batch", description="", num_seqs=pkv.MAX_SEQS, num_q_heads=8, num_kv_heads=2,
-                      head_dim=64, max_blocks_per_seq=3, length_kind="fixed", lengths=lens, pool_slack=0.1)
+    spec = DecodeSpec(name="max_batch", description="", num_seqs=pkv.MAX_SEQS, num_q_heads=hq, num_kv_heads=hkv,
+                      head_dim=head_dim, max_blocks_per_seq=3, length_kind="fixed", lengths=lens, pool_slack=0.1)
     c = make_decode_case(spec, seed=78)
     c.slot_mapping[c.context_lens == 0] = -1
     ref, _, _ = oracle_step(c)
