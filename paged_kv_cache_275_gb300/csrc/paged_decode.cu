@@ -984,6 +984,9 @@ __global__ void __launch_bounds__(NW * 32)
 // write zeros for empty sequences.  One CTA per (sequence, kv head), one warp
 // per q head of the group.
 // ---------------------------------------------------------------------------
+#ifndef PKV_MERGE_AHEAD
+#define PKV_MERGE_AHEAD 4
+#endif
 template <int D, int G>
 __global__ void __launch_bounds__(G * 32) paged_decode_merge_kernel(const DecodeParams p) {
   using T = Geo<D, G>;
@@ -1016,29 +1019,48 @@ __global__ void __launch_bounds__(G * 32) paged_decode_merge_kernel(const Decode
   float acc[kPer];
 #pragma unroll
   for (int x = 0; x < kPer; ++x) acc[x] = 0.f;
-  for (long long w = wa; w <= wb; ++w) {
-    const long long st = w * total / W;
-    const long long en = (w + 1) * total / W;
-    if (st == en) continue;  // empty piece
-    const int slot = (w == wa && st < s) ? 1 : 0;
-    const float* piece = p.ws_pieces + (static_cast<size_t>(w) * 2 + slot) * T::kPieceFloats;
-    const float mw = piece[G * D + g];
-    const float lw = piece[G * D + G + g];
-    float a[kPer];
-    if constexpr (kPer == 4) {
-      const float4 v = *reinterpret_cast<const float4*>(piece + g * D + lane * 4);
-      a[0] = v.x; a[1] = v.y; a[2] = v.z; a[3] = v.w;
-    } else {
-      const float2 v = *reinterpret_cast<const float2*>(piece + g * D + lane * 2);
-      a[0] = v.x; a[1] = v.y;
-    }
-    const float mn = fmaxf(M, mw);
-    const float alpha = exp2f(M - mn);
-    const float beta = exp2f(mw - mn);
-    l = l * alpha + lw * beta;
+  // Pieces PKV_MERGE_AHEAD at a time: their states are fetched before any is combined
+  // (a pair spans two or three pieces at the LLaMA-3 shape, five or six at the Qwen3
+  // one), and each piece boundary is computed once.
+  constexpr int kAhead = PKV_MERGE_AHEAD;
+  long long st = wa * total / W;
+  for (long long w0 = wa; w0 <= wb; w0 += kAhead) {
+    float mw[kAhead], lw[kAhead], a[kAhead][kPer];
+    bool use[kAhead];
 #pragma unroll
-    for (int x = 0; x < kPer; ++x) acc[x] = acc[x] * alpha + a[x] * beta;
-    M = mn;
+    for (int u = 0; u < kAhead; ++u) {
+      const long long w = w0 + u;
+      use[u] = false;
+      if (w <= wb) {
+        const long long en = (w + 1) * total / W;
+        if (st < en) {  // an empty piece covers nothing
+          use[u] = true;
+          const int slot = (w == wa && st < s) ? 1 : 0;
+          const float* piece = p.ws_pieces + (static_cast<size_t>(w) * 2 + slot) * T::kPieceFloats;
+          mw[u] = piece[G * D + g];
+          lw[u] = piece[G * D + G + g];
+          if constexpr (kPer == 4) {
+            const float4 v = *reinterpret_cast<const float4*>(piece + g * D + lane * 4);
+            a[u][0] = v.x; a[u][1] = v.y; a[u][2] = v.z; a[u][3] = v.w;
+          } else {
+            const float2 v = *reinterpret_cast<const float2*>(piece + g * D + lane * 2);
+            a[u][0] = v.x; a[u][1] = v.y;
+          }
+        }
+        st = en;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kAhead; ++u) {
+      if (!use[u]) continue;
+      const float mn = fmaxf(M, mw[u]);
+      const float alpha = exp2f(M - mn);
+      const float beta = exp2f(mw[u] - mn);
+      l = l * alpha + lw[u] * beta;
+#pragma unroll
+      for (int x = 0; x < kPer; ++x) acc[x] = acc[x] * alpha + a[u][x] * beta;
+      M = mn;
+    }
   }
   const float inv = 1.0f / l;
   if constexpr (kPer == 4) {
