@@ -19,11 +19,13 @@
 // * Memory pipeline.  Each warp owns a ring of S shared-memory stages.  One
 //   lane issues cp.async.bulk (TMA bulk) copies of the block's K tile and V
 //   tile (each one contiguous 16 x head_dim bf16 run in the
-//   [block][kv head][16][head_dim] layout) plus, at the first block of a
-//   pair, the group's G q rows, completing on an mbarrier.  Block ids are
-//   fetched one refill ahead.  Every mbarrier wait has a time limit.
-// * Compute.  CUDA cores only (a GEMV with G <= 8 rows does not fill an MMA
-//   tile, and the kernel is bound by HBM).  A lane owns 8 consecutive dims
+//   [block][kv head][16][head_dim] layout; 128-byte-swizzled 2D tensor copies
+//   on the tensor-core path) plus, at the first block of a pair, the group's G
+//   q rows, completing on an mbarrier.  Block ids are fetched one refill
+//   ahead.  Every mbarrier wait has a time limit.
+// * Compute, G <= 4.  CUDA cores (a GEMV with four or fewer rows per kv head
+//   is bound by HBM).  Groups of eight heads run their two small products on
+//   the tensor cores instead (process_block_mma).  A lane owns 8 consecutive dims
 //   (one 16-byte shared-memory load per row).  Partial dot products of all
 //   tokens of a block and all G heads are reduced across the lanes of a row
 //   with a transpose-reduction; the lanes' token order and q-head order are
