@@ -77,3 +77,13 @@ def test_reference_arm_line_on_cpu():
     assert line["impl"] == "reference" and line["unit"] == "GB/s" and line["value"] > 0
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["metric"] == bench.METRIC
+
+
+def test_e2e_reports_the_faster_drive_and_both():
+    import bench
+    long_step = bench.e2e_line(6.1e12 * 100, 0.0206, 5.4e12 * 100, 0.0234, 100, 1705472, 1048576)
+    assert long_step["mode"] == "pipelined" and long_step["value"] == long_step["pipelined"]["value"]
+    assert long_step["serial"]["value"] < long_step["value"]
+    short_step = bench.e2e_line(2.3e12, 0.07, 3.1e12, 0.05, 1000, 10, 20)
+    assert short_step["mode"] == "serial" and short_step["value"] == short_step["serial"]["value"]
+    assert short_step["h2d_bytes_per_step"] == 10 and short_step["d2h_bytes_per_step"] == 20
