@@ -155,8 +155,8 @@ pkv_status pkv_decode_default_partitions(int32_t num_seqs, int32_t num_q_heads, 
  * finished output row or a partial softmax state) and the merge kernel.
  * Arithmetic: fp32 accumulation, one round-to-nearest-even to bf16 at the end.
  * With eight q heads per kv head the two products run on the tensor cores
- * (bf16 operands, fp32 accumulation) and the softmax weights are rounded to
- * bf16 for the P.V product; with four or fewer they stay in fp32.
+ * (fp32 accumulation; each softmax weight enters P.V as two bf16 parts, about
+ * 16 significant bits); with four or fewer the weights stay in fp32.
  */
 pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,
                                       const int32_t* block_tables, int32_t max_blocks_per_seq,

@@ -111,7 +111,7 @@ struct Geo {
   }
 };
 
-// Groups of PKV_MMA_MIN_G (at most 8) or more q heads run q.K and p.V on the tensor
+// Groups of PKV_MMA_MIN_G (4 or 8) or more q heads run q.K and p.V on the tensor
 // cores (warp-level mma.sync, the group's heads as the N = 8 columns): at eight heads
 // the CUDA cores are held back by the arithmetic (8 flop per byte), while for four or
 // fewer they are bound by HBM and the tensor cores gain nothing (LLaMA-3-8B shape: 206
@@ -119,7 +119,8 @@ struct Geo {
 #ifndef PKV_MMA_MIN_G
 #define PKV_MMA_MIN_G 8
 #endif
-static_assert(PKV_MMA_MIN_G >= 1 && PKV_MMA_MIN_G <= 8, "groups of eight always take the tensor cores");
+static_assert(PKV_MMA_MIN_G == 4 || PKV_MMA_MIN_G == 8,
+              "groups of eight always take the tensor cores; four may (their p tile holds the two 256-byte P tiles)");
 template <int G>
 struct Split {
   static constexpr bool kMma = G >= PKV_MMA_MIN_G;
@@ -405,14 +406,15 @@ __device__ __forceinline__ void process_block(const unsigned char* sK, const uns
 // at chunk c ^ (r % 8), so every 8-row ldmatrix touches all 32 banks once.
 //
 //   S^T [16 tokens x 8 heads] = K [16 x D] . q^T [D x 8]       D / 16 MMAs m16n8k16
-//   O^T [D x 8 heads]        += V^T [D x 16] . P^T [16 x 8]    D / 16 MMAs
+//   O^T [D x 8 heads]        += V^T [D x 16] . P^T [16 x 8]    2 D / 16 MMAs (P = hi + lo)
 //
 // Fragments (g = lane / 4, t = lane % 4): the S^T accumulator holds tokens g and
 // g + 8 of heads 2t and 2t + 1, so a lane owns the running max and sum of its two
-// heads; P goes through a 256-byte shared tile ([token][head] bf16) and comes back
-// transposed by ldmatrix.trans as the B operand; the O^T accumulator o[mt] holds
+// heads; P goes through two 256-byte shared tiles ([token][head] bf16: the high
+// part of each weight and its remainder) and comes back transposed by
+// ldmatrix.trans as the B operands of two MMAs; the O^T accumulator o[mt] holds
 // dims 16 mt + g and 16 mt + g + 8 of the same two heads.  Scores are scaled after
-// the MMA (fp32); the weights enter the MMA as bf16 and the sum l takes them in fp32.
+// the MMA (fp32); the weights reach P.V to within 2^-16 and the sum l adds them in fp32.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t swz_addr(uint32_t tile, int row, int chunk) {
   return tile + (chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4);
@@ -465,23 +467,33 @@ __device__ __forceinline__ void process_block_mma(uint32_t sK, unsigned char* sV
       o[mt][3] *= a1;
     }
   }
-  const float p0 = exp2f(s0 - m[0]), p1 = exp2f(s1 - m[1]);
-  const float p2 = exp2f(s2 - m[0]), p3 = exp2f(s3 - m[1]);
+  const float p0 = exp2f(s0 - m[0]), p1 = exp2f(s1 - m[1]);  // token g: heads 2t, 2t + 1
+  const float p2 = exp2f(s2 - m[0]), p3 = exp2f(s3 - m[1]);  // token g + 8
   l[0] += p0 + p2;
   l[1] += p1 + p3;
-  __syncwarp();  // the previous block's P tile has been read
+  // Each weight as bf16 hi + bf16 lo (the rounded-off rest): about 16 significant bits,
+  // so P.V carries the fp32 weights to within 2^-16 and the result does not depend on
+  // which running max a weight was taken against (how the stream was cut).
+  const uint32_t h01 = float2_to_bf16x2(p0, p1), h23 = float2_to_bf16x2(p2, p3);
+  const float2 r01 = bf16x2_to_float2(h01), r23 = bf16x2_to_float2(h23);
+  const uint32_t l01 = float2_to_bf16x2(p0 - r01.x, p1 - r01.y), l23 = float2_to_bf16x2(p2 - r23.x, p3 - r23.y);
+  __syncwarp();  // the previous block's P tiles have been read
   unsigned char* pt = reinterpret_cast<unsigned char*>(__cvta_shared_to_generic(sP));
-  *reinterpret_cast<uint32_t*>(pt + g * 16 + t * 4) = float2_to_bf16x2(p0, p1);
-  *reinterpret_cast<uint32_t*>(pt + (g + 8) * 16 + t * 4) = float2_to_bf16x2(p2, p3);
+  *reinterpret_cast<uint32_t*>(pt + g * 16 + t * 4) = h01;
+  *reinterpret_cast<uint32_t*>(pt + (g + 8) * 16 + t * 4) = h23;
+  *reinterpret_cast<uint32_t*>(pt + 256 + g * 16 + t * 4) = l01;
+  *reinterpret_cast<uint32_t*>(pt + 256 + (g + 8) * 16 + t * 4) = l23;
   __syncwarp();
-  uint32_t pb0, pb1;
-  ldsm_x2_t(sP + (lane & 15) * 16, pb0, pb1);
+  uint32_t ph0, ph1, pl0, pl1;
+  ldsm_x2_t(sP + (lane & 15) * 16, ph0, ph1);
+  ldsm_x2_t(sP + 256 + (lane & 15) * 16, pl0, pl1);
   // O^T += V^T P^T: V rows are the K dimension, dims the M dimension.
 #pragma unroll
   for (int mt = 0; mt < D / 16; ++mt) {
     uint32_t a[4];
     ldsm_x4_t(swz_addr(sV, ((mi >> 1) << 3) | (lane & 7), 2 * mt + (mi & 1)), a);
-    mma_16816(o[mt], a, pb0, pb1);
+    mma_16816(o[mt], a, ph0, ph1);
+    mma_16816(o[mt], a, pl0, pl1);
   }
 }
 
@@ -544,6 +556,7 @@ __global__ void __launch_bounds__(NW * 32)
   constexpr bool kMma = Split<G>::kMma;  // q.K and p.V on the tensor cores
   constexpr int kStage = stage_bytes<D, G>();
   static_assert(kMma || T::valid(), "unsupported (head_dim, group) geometry");
+  static_assert(!kMma || T::kPTileBytes >= 512, "the tensor-core path keeps two 256-byte P tiles per warp");
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int s_wsum[32];
 

@@ -15,6 +15,13 @@ from workloads import BLOCK_SIZE, SPECS, DecodeSpec, make_decode_case, make_gene
 pytestmark = pytest.mark.gpu
 
 
+# The Qwen3 workload with eight q heads per kv head (64 q / 8 kv): the tensor-core path.
+QWEN3_G8 = DecodeSpec(name="qwen3_g8", description="Qwen3 lengths, 64 q / 8 kv heads, D 128", num_seqs=32,
+                      num_q_heads=64, num_kv_heads=8, head_dim=128, max_blocks_per_seq=128, length_kind="uniform",
+                      length_range=(128, 2048), pool_slack=0.10)
+BOTH_PATHS = pytest.mark.parametrize("shape", ["qwen3_0.6b", QWEN3_G8], ids=["G2_cuda_cores", "G8_tensor_cores"])
+
+
 def _run(c, num_partitions=0):
     g = c.to("cuda")
     out = gpu_step(g, num_partitions)
@@ -131,16 +138,18 @@ def test_random_shapes(seed):
 # ---------------------------------------------------------------------------
 # Invariants and special cases
 # ---------------------------------------------------------------------------
-def test_single_token_returns_its_value_exactly():
-    c = make_decode_case("qwen3_0.6b", seed=7, lengths=[1] * 8)
+@BOTH_PATHS
+def test_single_token_returns_its_value_exactly(shape):
+    c = make_decode_case(shape, seed=7, lengths=[1] * 8)
     g, out = _run(c, 0)
     # The one cached token is the appended one.
-    expect = c.new_v.repeat_interleave(2, dim=1)
+    expect = c.new_v.repeat_interleave(c.q.shape[1] // c.k_cache.shape[1], dim=1)
     assert torch.equal(out.cpu(), expect)
 
 
-def test_block_relabelling_is_bit_identical():
-    c = make_decode_case("qwen3_0.6b", seed=8)
+@BOTH_PATHS
+def test_block_relabelling_is_bit_identical(shape):
+    c = make_decode_case(shape, seed=8)
     _, out1 = _run(c, 0)
     perm = torch.randperm(c.num_blocks, generator=make_generator(3))
     kc2 = torch.empty_like(c.k_cache)
@@ -155,8 +164,9 @@ def test_block_relabelling_is_bit_identical():
     assert torch.equal(out1, out2)
 
 
-def test_repeated_runs_are_bit_identical():
-    c = make_decode_case("llama3_8b", seed=9, num_seqs=48)
+@pytest.mark.parametrize("shape", ["llama3_8b", "llama3_70b"])
+def test_repeated_runs_are_bit_identical(shape):
+    c = make_decode_case(shape, seed=9, num_seqs=48)
     g = c.to("cuda")
     pkv.kv_append(g.new_k, g.new_v, g.slot_mapping, g.k_cache, g.v_cache)
     outs = []
@@ -167,9 +177,10 @@ def test_repeated_runs_are_bit_identical():
     assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
 
 
-def test_poisoned_unused_slots_do_not_leak():
+@BOTH_PATHS
+def test_poisoned_unused_slots_do_not_leak(shape):
     """NaN in every slot no sequence owns and garbage past each table row: output unchanged."""
-    c = make_decode_case("qwen3_0.6b", seed=10)
+    c = make_decode_case(shape, seed=10)
     _, clean = _run(c, 0)
     used = torch.zeros(c.num_blocks * BLOCK_SIZE, dtype=torch.bool)
     for sid in range(c.spec.num_seqs):
@@ -188,19 +199,25 @@ def test_poisoned_unused_slots_do_not_leak():
     assert device_errors() == 0
 
 
-def test_partition_counts_agree():
-    """Cutting the block stream differently changes only fp32 rounding."""
-    c = make_decode_case("qwen3_0.6b", seed=11)
+@BOTH_PATHS
+def test_partition_counts_agree(shape):
+    """Cutting the block stream differently changes only rounding: the fp32 sums' order, and on the
+    tensor-core path also the running maxima the bf16 weights are rounded against."""
+    c = make_decode_case(shape, seed=11)
     _, base = _run(c, 1)
+    share = []
     for parts in (2, 7, 100, 1000, 0):
         _, out = _run(c, parts)
         d = (out.float() - base.float()).abs()
         assert d.max().item() <= 2 * 2 ** -8 * max(1.0, base.float().abs().max().item())
-        assert (d > 0).float().mean().item() < 0.05
+        share.append((d > 0).float().mean().item())
+    print(f"{c.spec.name}: share of outputs that differ from one piece per pair: {share}")
+    assert max(share) < 0.05
 
 
-def test_huge_scale_selects_argmax():
-    c = make_decode_case("qwen3_0.6b", seed=12, lengths=[5, 40, 300])
+@BOTH_PATHS
+def test_huge_scale_selects_argmax(shape):
+    c = make_decode_case(shape, seed=12, lengths=[5, 40, 300])
     g = c.to("cuda")
     pkv.kv_append(g.new_k, g.new_v, g.slot_mapping, g.k_cache, g.v_cache)
     out = torch.empty_like(g.q)
