@@ -5,7 +5,11 @@ import torch
 
 import paged_kv_cache_275_gb300 as pkv
 from gpu_util import device_errors
-from workloads import make_decode_case, make_prefill_case, rope_cos_sin
+from workloads import DecodeSpec, make_decode_case, make_prefill_case, rope_cos_sin
+
+# Eight q heads per kv head: the tensor-core path (its K/V tensor maps travel as kernel parameters).
+G8 = DecodeSpec(name="g8_graph", description="", num_seqs=24, num_q_heads=32, num_kv_heads=4, head_dim=128,
+                max_blocks_per_seq=64, length_kind="uniform", length_range=(1, 1000), pool_slack=0.1)
 
 pytestmark = pytest.mark.gpu
 
@@ -23,8 +27,9 @@ def _capture(fn):
     return g
 
 
-def test_decode_step_graph_replay_is_bit_identical():
-    c = make_decode_case("qwen3_0.6b", seed=90).to("cuda")
+@pytest.mark.parametrize("shape", ["qwen3_0.6b", G8], ids=["G2", "G8"])
+def test_decode_step_graph_replay_is_bit_identical(shape):
+    c = make_decode_case(shape, seed=90).to("cuda")
     B, hq, d = c.q.shape
     ws = torch.empty(pkv.workspace_size(B, hq, c.k_cache.shape[1], d, c.block_tables.shape[1]), dtype=torch.uint8,
                      device="cuda")
@@ -48,8 +53,9 @@ def test_decode_step_graph_replay_is_bit_identical():
     assert device_errors() == 0
 
 
-def test_fused_step_graph_replay_is_bit_identical():
-    c = make_decode_case("tiny", seed=91).to("cuda")
+@pytest.mark.parametrize("shape", ["tiny", G8], ids=["tiny", "G8"])
+def test_fused_step_graph_replay_is_bit_identical(shape):
+    c = make_decode_case(shape, seed=91).to("cuda")
     B, hq, d = c.q.shape
     table = rope_cos_sin(c.block_tables.shape[1] * 16, d, 1e4).cuda()
     ws = torch.empty(pkv.workspace_size(B, hq, c.k_cache.shape[1], d, c.block_tables.shape[1]), dtype=torch.uint8,
