@@ -46,6 +46,16 @@ def test_length_distributions():
     assert 200 < med < 5000
 
 
+def test_llama3_70b_layer_shares_the_8b_lengths():
+    """The LLaMA-3-70B layer (eight q heads per kv head) draws the same lengths and pool as the 8B one."""
+    a, b = SPECS["llama3_8b"], SPECS["llama3_70b"]
+    assert (b.num_q_heads, b.num_kv_heads, b.head_dim) == (64, 8, 128)
+    assert (b.num_seqs, b.length_range, b.max_blocks_per_seq) == (a.num_seqs, a.length_range, a.max_blocks_per_seq)
+    assert draw_lengths(a, make_generator(0)) == draw_lengths(b, make_generator(0))
+    c = make_decode_case("llama3_70b", seed=0, num_seqs=4)
+    assert c.q.shape == (4, 64, 128) and c.k_cache.shape[1:] == (8, BLOCK_SIZE, 128)
+
+
 def test_allocator_takes_block_only_when_full_and_frees_all():
     g = make_generator(3)
     a = BlockAllocator(10, g)
