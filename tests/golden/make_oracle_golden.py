@@ -1,8 +1,8 @@
 """Write ``oracle_regression.json``: a small decode problem and the oracle's fp64 answer.
 
 This script calls only ``oracle/``.  The file pins the oracle against itself
-across machines (the x86 development box and the Arm GPU host must give the
-same fp64 values to 1e-13); it is not a correctness pin -- the pages print no
+across CPU architectures (an x86 and an Arm build must give the same fp64
+values to 1e-13); it is not a correctness pin -- the pages print no
 worked numerical example, so correctness is pinned by closed forms,
 invariants and brute force in ``tests/test_oracle_pins.py``.
 
