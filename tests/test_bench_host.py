@@ -32,6 +32,40 @@ def _rank_main(rank, world, port, q):
         d.close()
 
 
+def _reference_rank_main(rank, world, port, q):
+    import contextlib
+    import io
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), WORLD_SIZE=str(world), RANK=str(rank),
+                      LOCAL_RANK=str(rank), CUDA_VISIBLE_DEVICES="")
+    sys.path.insert(0, str(ROOT))
+    import bench
+    buf = io.StringIO()
+    with contextlib.redirect_stdout(buf):
+        rc = bench.main(["--impl", "reference", "--workload", "tiny", "--steps", "3", "--warmup", "3",
+                         "--reference-budget", "2"])
+    q.put((rank, rc, buf.getvalue()))
+
+
+def test_reference_arm_under_two_ranks_prints_once():
+    """Launched as N ranks, the reference arm runs and prints on rank 0 only; the others exit 0."""
+    import json
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_reference_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    results = sorted(q.get(timeout=300) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    (r0, rc0, out0), (r1, rc1, out1) = results
+    assert rc0 == 0 and rc1 == 0
+    lines = [x for x in out0.splitlines() if x.startswith("{")]
+    assert len(lines) == 1 and json.loads(lines[0])["impl"] == "reference"
+    assert not [x for x in out1.splitlines() if x.startswith("{")]
+
+
 def test_replica_aggregation_over_gloo():
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
