@@ -182,7 +182,7 @@ pkv_status pkv_paged_decode_attention_split(const void* q, const void* k_cache, 
                                             int32_t phases, pkv_stream_t stream);
 
 /* Bytes of the built-in scratch area behind pkv_paged_decode_attention_static (per device). */
-#define PKV_STATIC_WORKSPACE_BYTES (8u * 1024u * 1024u)
+#define PKV_STATIC_WORKSPACE_BYTES (16u * 1024u * 1024u)
 
 /*
  * Decode attention without a caller workspace, for callers that cannot
@@ -195,8 +195,10 @@ pkv_status pkv_paged_decode_attention_split(const void* q, const void* k_cache, 
  * workspace.  Scratch comes from one fixed array of PKV_STATIC_WORKSPACE_BYTES
  * inside the library, which every GPU that loads the library holds until the
  * process exits.  Shapes whose scratch need is larger return
- * PKV_ERR_UNSUPPORTED with a message (at the default partition count every
- * built shape needs about 5 MB on a 152-SM GB300).  The first call on a device,
+ * PKV_ERR_UNSUPPORTED with a message (at the default partition count on a
+ * 152-SM GB300 the built shapes need at most about 10.1 MB, eight q heads per
+ * kv head at head_dim 128 with 4096 sequences; four heads about 5.1 MB).  The
+ * first call on a device,
  * with that device current, looks up the array's device address
  * (cudaGetSymbolAddress); make that first call before any stream capture.
  * Every call shares the array and it keeps the last call's contents (nothing

@@ -30,7 +30,7 @@ def _static_call(lib, g, out) -> int:
         torch.cuda.current_stream().cuda_stream)
 
 
-@pytest.mark.parametrize("name,num_seqs", [("qwen3_0.6b", None), ("llama3_8b", 64), ("tiny", None)])
+@pytest.mark.parametrize("name,num_seqs", [("qwen3_0.6b", None), ("llama3_8b", 64), ("llama3_70b", 64), ("tiny", None)])
 def test_static_scratch_entry_matches_workspace_entry(name, num_seqs):
     lib = pkv.load()
     g = make_decode_case(name, seed=21, num_seqs=num_seqs).to("cuda")
