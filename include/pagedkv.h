@@ -114,6 +114,14 @@ pkv_status pkv_kv_append(const void* k, const void* v, const int64_t* slot_mappi
 /*
  * Bytes of device workspace one attention call needs.
  *
+ * This replaces a query of the form size_t workspace_bytes(num_seqs,
+ * num_q_heads, head_dim, max_blocks_per_seq, block_size): the workspace holds
+ * two partial softmax states per piece, each G * head_dim + 4 * ceil(G / 2)
+ * floats (G = num_q_heads / num_kv_heads), so it depends on num_kv_heads and
+ * on num_partitions; the default num_partitions depends on the device, so the
+ * query can fail and returns a status, the size through `bytes`.  block_size
+ * is always 16 and is checked by the attention call.
+ *
  * num_partitions is the number of contiguous, equal-length pieces the whole
  * batch's (sequence, kv head, block) stream is cut into (one warp each; a
  * piece that covers only part of a (sequence, kv head) pair leaves a partial
@@ -157,6 +165,10 @@ pkv_status pkv_decode_default_partitions(int32_t num_seqs, int32_t num_q_heads, 
  * With eight q heads per kv head the two products run on the tensor cores
  * (fp32 accumulation; each softmax weight enters P.V as two bf16 parts, about
  * 16 significant bits); with four or fewer the weights stay in fp32.
+ *
+ * If pkv_get_and_clear_device_error reports PKV_DEVERR_PIPELINE_TIMEOUT after
+ * the call, the outputs of the call are undefined: a piece whose wait gave up
+ * wrote no partial state, and the merge combined whatever the workspace held.
  */
 pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache, const void* v_cache,
                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -203,7 +215,10 @@ pkv_status pkv_paged_decode_attention_split(const void* q, const void* k_cache, 
  * (cudaGetSymbolAddress); make that first call before any stream capture.
  * Every call shares the array and it keeps the last call's contents (nothing
  * in it needs to start at zero), so calls that may overlap on the GPU race:
- * serialise them on one stream.  Calls no allocating routine.
+ * serialise them on one stream.  Calls no allocating routine.  As for
+ * pkv_paged_decode_attention, a PKV_DEVERR_PIPELINE_TIMEOUT bit after the call
+ * means its outputs are undefined (here the merge may combine an earlier
+ * call's states left in the shared array).
  */
 pkv_status pkv_paged_decode_attention_static(const void* q, const void* k_cache, const void* v_cache,
                                              const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -347,7 +362,14 @@ pkv_status pkv_bm_ref_count(pkv_block_manager* bm, int64_t block, int32_t* count
 /*
  * Synchronises `stream`, then returns and clears the current device's sticky
  * error word (a mask of PKV_DEVERR_* bits; 0 = no device-side error since the
- * last clear).
+ * last clear).  The word is unsigned (uint32_t, not int32_t) because it is a
+ * set of independent flags, each set by an atomic OR on the device.
+ *
+ * The word's device address is looked up once per device ordinal and kept for
+ * the life of the process (as is the scratch address behind
+ * pkv_paged_decode_attention_static); after a cudaDeviceReset, which destroys
+ * the context those addresses belong to, this library must not be called
+ * again on that device in the same process.
  */
 pkv_status pkv_get_and_clear_device_error(uint32_t* bits, pkv_stream_t stream);
 

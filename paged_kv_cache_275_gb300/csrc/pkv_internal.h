@@ -100,8 +100,8 @@ cudaError_t launch_kv_append(const AppendParams& p, int num_sms, cudaStream_t st
 int piece_floats(int head_dim, int group);
 // Bytes of the workspace header (block prefix) for num_seqs sequences.
 size_t workspace_header_bytes(int num_seqs);
-// Pieces the partition kernel keeps in flight on the current device: one per warp,
-// or per pair of warps for groups of eight q heads (the default num_partitions).
+// Pieces the partition kernel keeps in flight on the current device: one per warp
+// (the default num_partitions).
 cudaError_t resident_partition_pieces(int head_dim, int group, int num_seqs, int* pieces);
 // Tensor map of a cache viewed as [rows = num_blocks * num_kv_heads * 16][head_dim] bf16, box 16 rows x
 // 64 dims, 128-byte swizzle (the tensor-copy layout of the prefill kernel and of the decode tensor-core path).

@@ -35,6 +35,14 @@ MUTATIONS = {
     "prefill_causal_off_by_one": ("prefix + i + 1, out_row);", "prefix + i, out_row);"),
     "table_row_stride": ("P->block_tables[(int64_t)b * P->max_blocks_per_seq + logical_block]",
                          "P->block_tables[(int64_t)b * P->block_size + logical_block]"),
+    "copy_k_only": ("            v_cache[dst * per_block + e] = v_cache[src * per_block + e];\n", ""),
+    "copy_block_stride_without_heads": ("const int64_t per_block = (int64_t)num_kv_heads * block_size * head_dim;",
+                                        "const int64_t per_block = (int64_t)block_size * head_dim;"),
+    "copy_pairs_reversed": ("const int64_t src = src_dst[2 * i], dst = src_dst[2 * i + 1];",
+                            "const int64_t src = src_dst[2 * (num_pairs - 1 - i)], "
+                            "dst = src_dst[2 * (num_pairs - 1 - i) + 1];"),
+    "copy_src_dst_swapped": ("const int64_t src = src_dst[2 * i], dst = src_dst[2 * i + 1];",
+                             "const int64_t dst = src_dst[2 * i], src = src_dst[2 * i + 1];"),
 }
 
 

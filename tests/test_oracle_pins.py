@@ -301,6 +301,54 @@ def test_append_rejects_out_of_range_and_duplicate_slots():
     assert st & oracle.DUPLICATE_SLOT
 
 
+# ---------------------------------------------------------------------------
+# Block copy (copy-on-write of shared blocks)
+# ---------------------------------------------------------------------------
+def test_copy_blocks_equals_numpy_block_assignment_in_pair_order():
+    """The copy half of copy-on-write ("v0版本介绍", section 为什么需要推理框架: requests share
+    prompt blocks, so a shared block is copied before one of its users appends into it),
+    restated as numpy block assignment cache[dst] = cache[src] for K and V, pair by pair in
+    order, on a pool whose every element holds a distinct bit pattern.  The pairs include a
+    chain (a -> b, then b -> c: c must end up with a's contents, which fixes the order of
+    application) and an out-of-range pair (flagged, skipped, nothing written).  Catches a
+    per-block stride without the kv heads, V left uncopied or copied from K, pairs applied
+    out of order, and swapped source and destination."""
+    nb, hkv, D = 10, 3, 8
+    n_el = nb * hkv * BLOCK_SIZE * D
+    # Distinct finite bf16 bit patterns (exponent field kept away from 0xff: no NaN or inf).
+    bits = (np.arange(n_el, dtype=np.int64) % 0x3f00 + 0x0100).astype(np.int16)
+    kc = torch.from_numpy(bits.reshape(nb, hkv, BLOCK_SIZE, D).copy()).view(torch.bfloat16)
+    vc = torch.from_numpy((-bits).reshape(nb, hkv, BLOCK_SIZE, D).copy()).view(torch.bfloat16)
+    assert len(np.unique(kc.view(torch.int16).numpy())) == n_el
+    pairs = np.array([[1, 4], [4, 7], [2, 9], [0, nb], [8, 3]], dtype=np.int64)
+
+    k_ref = kc.view(torch.int16).numpy().copy()
+    v_ref = vc.view(torch.int16).numpy().copy()
+    for src, dst in pairs.tolist():
+        if 0 <= src < nb and 0 <= dst < nb:
+            k_ref[dst] = k_ref[src]
+            v_ref[dst] = v_ref[src]
+    assert np.array_equal(k_ref[7], kc.view(torch.int16).numpy()[1])  # the chain carried block 1 to block 7
+
+    st = oracle.copy_blocks(kc, vc, torch.from_numpy(pairs))
+    assert st == oracle.BLOCK_ID_OUT_OF_RANGE
+    assert np.array_equal(kc.view(torch.int16).numpy(), k_ref)
+    assert np.array_equal(vc.view(torch.int16).numpy(), v_ref)
+
+
+def test_copy_blocks_with_no_valid_pair_changes_nothing():
+    nb, hkv, D = 3, 2, 8
+    g = make_generator(24)
+    kc = randn_bf16((nb, hkv, BLOCK_SIZE, D), g)
+    vc = randn_bf16((nb, hkv, BLOCK_SIZE, D), g)
+    k0, v0 = kc.clone(), vc.clone()
+    st = oracle.copy_blocks(kc, vc, torch.tensor([[-1, 0], [1, 3]], dtype=torch.int64))
+    assert st == oracle.BLOCK_ID_OUT_OF_RANGE
+    assert torch.equal(kc.view(torch.int16), k0.view(torch.int16))
+    assert torch.equal(vc.view(torch.int16), v0.view(torch.int16))
+    assert oracle.copy_blocks(kc, vc, torch.zeros((0, 2), dtype=torch.int64)) == oracle.OK
+
+
 def test_append_then_attend_equals_contiguous_attention():
     """Write each sequence token by token through the allocator's slots, then attend:
     equals SDPA over the tokens as written.  Ties the append layout to the gather."""
