@@ -14,11 +14,14 @@
 // tile.  Keys advance 128 at a time (8 pages of 16), so S = Q K^T is an N = 128
 // MMA and O += P V an N = D one: at N = 64 an MMA is bound by reading its
 // operands from shared memory, at N = 128 by the math.
-//   * warp 8: TMA producer.  Each page half (16 tokens x 64 dims) is a 2D
+//   * warp 8: TMA producer.  Each page (16 tokens x D of one kv head) is one 4D
 //     tensor-map copy with 128-byte swizzle, gathered through the block table into
 //     a K ring (3 slots) and a V ring (2 slots), one copy per lane; mbarrier
-//     completion by transaction bytes.  It also zeroes the rows of the last V
-//     tile past the end of the keys.
+//     completion by transaction bytes.  Per-copy cost, not bytes, bounds the copy
+//     engine at 16-token pages, so a page travels as one copy: its two 8-row groups,
+//     each the two 64-dim halves one after the other, a layout both products read
+//     with 8-row groups one descriptor stride apart.  It also zeroes the rows of the
+//     last V tile past the end of the keys.
 //   * warp 9 (one lane): MMA issuer.  tcgen05.mma kind::f16 (bf16 in, fp32
 //     accumulate): S = Q_t K^T into tile t's TMEM S buffer (M 128, N 128); once
 //     the softmax has written P over S, O_t += P V (M 128, N = D, P read from
@@ -75,6 +78,10 @@ struct Pf {
   static constexpr int kQTile = kHalves * kQHalf;  // one tile's Q
   static constexpr int kKVHalf = kKeys * 128;      // 16 KB: 128 keys x 64 dims
   static constexpr int kTile = kHalves * kKVHalf;  // one K (or V) tile of a step
+  // A K or V tile is 8 pages of 16 keys, each page one tensor copy laid out as two 8-row
+  // groups, each group the page's 64-dim halves one after the other: [group][half][8 rows][128 B].
+  static constexpr int kGroupBytes = kHalves * 1024;  // stride between 8-key groups (descriptor SBO)
+  static constexpr int kPageBytes = 2 * kGroupBytes;  // one page of one kv head
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kTiles * kQTile;
   static constexpr int kOffV = kOffK + kKStages * kTile;
@@ -124,25 +131,26 @@ __device__ __forceinline__ bool bar_wait(uint32_t b, uint32_t parity) {
   }
   return false;
 }
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t b) {
+// 4D tensor copy: one page of one kv head (box 64 dims x 8 rows x halves x 2 row groups).
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int group, uint32_t b) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-          dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(b)
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %2, %2, %3}], "
+      "[%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(group), "r"(b)
       : "memory");
 }
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// Shared-memory matrix descriptor: 128-byte swizzle with 8-row groups 1024 bytes
-// apart (the stride byte offset).  K-major operands are one swizzle atom (64
-// elements) wide across the 16-element K of an MMA; an MN-major operand (V, read
-// as N = D) may span two atoms along N, `lbo` bytes apart.
-__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo = 1024) {
+// Shared-memory matrix descriptor: 128-byte swizzle with 8-row groups `sbo` bytes
+// apart (the stride byte offset; 1024 when the groups are packed).  K-major operands
+// are one swizzle atom (64 elements) wide across the 16-element K of an MMA; an
+// MN-major operand (V, read as N = D) may span two atoms along N, `lbo` bytes apart.
+__device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo = 1024, uint32_t sbo = 1024) {
   uint64_t d = (addr & 0x3FFFFu) >> 4;
   d |= uint64_t(lbo >> 4) << 16;     // leading byte offset (MN-major: next 64-wide atom along N)
-  d |= uint64_t(1024 >> 4) << 32;    // stride byte offset: 8 rows x 128 B
+  d |= uint64_t(sbo >> 4) << 32;     // stride byte offset: between 8-row groups
   d |= uint64_t(1) << 46;            // descriptor version
   d |= uint64_t(2) << 61;            // 128-byte swizzle
   return d;
@@ -247,6 +255,12 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 __device__ __forceinline__ uint32_t swz(int r, int chunk) {
   return static_cast<uint32_t>((r >> 3) * 1024 + (r & 7) * 128 + ((chunk ^ (r & 7)) << 4));
 }
+// Byte offset of chunk `chunk` of key `r` (0..127), dims half `h`, in a K or V tile of pages.
+template <int D>
+__device__ __forceinline__ uint32_t kv_off(int r, int h, int chunk) {
+  return static_cast<uint32_t>((r >> 4) * Pf<D>::kPageBytes + ((r >> 3) & 1) * Pf<D>::kGroupBytes + h * 1024 +
+                               (r & 7) * 128 + ((chunk ^ (r & 7)) << 4));
+}
 
 // ---------------------------------------------------------------------------
 // The kernel
@@ -273,11 +287,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   // longest, the launch order approximates longest-processing-time-first and the last
   // wave holds the shortest tiles.  Ranked in shared memory when num_seqs <= kThreads,
   // in the V ring (not yet in use) and a spare word of the barrier area.
+  // The sequences' chunk starts are staged beside the lengths in the same pass, so that the
+  // picked sequence's q0, C and L need no second round trip to memory.
   int b = blockIdx.z;
+  int q0, C, L;
   if (p.num_seqs <= kThreads) {
     int* s_lens = reinterpret_cast<int*>(smem + T::kOffV);
+    int* s_qs = s_lens + kThreads;
     int& s_pick = *reinterpret_cast<int*>(smem + T::kOffBar + kTmemSlotOffset + 4);
-    if (tid < p.num_seqs) s_lens[tid] = p.context_lens[tid];
+    if (tid < p.num_seqs) {
+      s_lens[tid] = p.context_lens[tid];
+      s_qs[tid] = p.query_start[tid];
+    }
+    if (tid == 0) s_qs[p.num_seqs] = p.query_start[p.num_seqs];
     __syncthreads();
     if (tid < p.num_seqs) {
       const int mine = s_lens[tid];
@@ -290,11 +312,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncthreads();
     b = s_pick;
+    q0 = s_qs[b];
+    C = s_qs[b + 1] - q0;
+    L = s_lens[b];
+  } else {
+    q0 = p.query_start[b];
+    C = p.query_start[b + 1] - q0;
+    L = p.context_lens[b];
   }
-
-  const int q0 = p.query_start[b];
-  const int C = p.query_start[b + 1] - q0;
-  int L = p.context_lens[b];
   const int cap = p.max_blocks_per_seq * kBlockTokens;
   if (C < 0 || L < C || L > cap) {
     if (tid == 0 && tile == 0) atomicOr(p.err, kErrLenTooLong);
@@ -332,6 +357,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mma_drained = q_ready + 8 * kTiles;             // [tile]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::kOffBar + kTmemSlotOffset);
 
+  // The producer's first two windows of block ids are requested before the set-up barrier,
+  // ahead of the softmax warps' Q loads, which would otherwise queue in front of them.
+  constexpr int kPages = kKeys / kBlockTokens;  // pages per step
+  const int npages = (kv_end + kBlockTokens - 1) / kBlockTokens;
+  const int32_t* table = p.block_tables + static_cast<size_t>(b) * p.max_blocks_per_seq;
+  int raw_cur = 0, raw_next = 0;
+  if (warp == kProducerWarp) {
+    if (lane < npages) raw_cur = __ldg(table + lane);
+    if (32 + lane < npages) raw_next = __ldg(table + 32 + lane);
+  }
+
   if (tid == 0) {
     for (int s = 0; s < kKStages; ++s) {
       bar_init(k_full + 8 * s, 1);
@@ -367,34 +403,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---------------- TMA producer (whole warp) ----------------
     // Block ids come from a 32-page window held one per lane, with the next
     // window already in flight, so no copy waits on a dependent table load.
-    constexpr int kPages = kKeys / kBlockTokens;  // pages per step
-    static_assert(32 % kPages == 0 && kPages * T::kHalves <= 32, "a step's pages sit in one window, one copy per lane");
-    const int npages = (kv_end + kBlockTokens - 1) / kBlockTokens;
-    const int32_t* table = p.block_tables + static_cast<size_t>(b) * p.max_blocks_per_seq;
-    auto fetch = [&](int page) -> int {
+    static_assert(32 % kPages == 0, "a step's pages sit in one window, one copy per lane");
+    auto check = [&](int page, int id) -> int {
       if (page >= npages) return 0;
-      const int id = __ldg(table + page);
       if (id < 0 || id >= p.num_blocks) {
         atomicOr(p.err, kErrBlockId);
         return 0;
       }
       return id;
     };
+    auto fetch = [&](int page) -> int { return page < npages ? check(page, __ldg(table + page)) : 0; };
     int win = 0;
-    int id_cur = fetch(lane), id_next = fetch(32 + lane);
+    int id_cur = check(lane, raw_cur), id_next = check(32 + lane, raw_next);
     int prev_id = 0;  // this lane's page id of the previous step (for its V)
     int issued_k = 0, issued_v = 0;
-    // One copy per lane (page lane / halves, half lane % halves): a thread's tensor
-    // copies issue one after another, slowly, while copies from different lanes go
-    // out together.
-    const int my_pg = lane / T::kHalves, my_h = lane % T::kHalves;
+    // One copy per lane, lane = page of the step: a thread's tensor copies issue one
+    // after another, slowly, while copies from different lanes go out together.  A
+    // copy moves a whole page of the kv head (both dims halves, 4 KB at D = 128).
+    const int my_pg = lane;
     auto issue = [&](int j, int my_id, uint32_t dst, const CUtensorMap* map, uint32_t full) {
       const int pages = min(kPages, npages - j * kPages);
-      if (lane == 0) bar_expect_tx(full, static_cast<uint32_t>(pages * T::kHalves * kBlockTokens * 128));
+      if (lane == 0) bar_expect_tx(full, static_cast<uint32_t>(pages * T::kPageBytes));
       __syncwarp();
-      if (my_pg < pages)
-        tma_load_2d(dst + my_h * T::kKVHalf + my_pg * (kBlockTokens * 128), map, 64 * my_h,
-                    (my_id * p.num_kv_heads + kvh) * kBlockTokens, full);
+      if (my_pg < pages) tma_load_4d(dst + my_pg * T::kPageBytes, map, 2 * (my_id * p.num_kv_heads + kvh), full);
     };
     for (int j = 0; j <= nsteps && !failed; ++j) {
       int my_id = 0;
@@ -436,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int idx = lane; idx < (kKeys - first) * T::kHalves * 8; idx += 32) {
           const int r = first + idx / (T::kHalves * 8);
           const int rem = idx % (T::kHalves * 8);
-          *reinterpret_cast<uint4*>(vt + (rem / 8) * T::kKVHalf + swz(r, rem % 8)) = make_uint4(0u, 0u, 0u, 0u);
+          *reinterpret_cast<uint4*>(vt + kv_off<D>(r, rem / 8, rem % 8)) = make_uint4(0u, 0u, 0u, 0u);
         }
         fence_async_smem();
         __syncwarp();
@@ -468,8 +499,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int h = 0; h < T::kHalves; ++h)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_bf16<kIdS>(tmem + col_s(t), sdesc(qt + h * T::kQHalf + kk * 32), sdesc(kt + h * T::kKVHalf + kk * 32),
-                         (h | kk) != 0);
+          mma_bf16<kIdS>(tmem + col_s(t), sdesc(qt + h * T::kQHalf + kk * 32),
+                         sdesc(kt + h * 1024 + kk * 32, 1024, T::kGroupBytes), (h | kk) != 0);
       mma_commit(s_full + 8 * t);
     };
     for (int t = 0; t < n_tiles; ++t)
@@ -501,8 +532,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t d_s = tmem + col_s(t);
 #pragma unroll
           for (int kk = 0; kk < kKeys / 16; ++kk)
-            mma_bf16_ts<kIdPV>(tmem + col_o(t), d_s + kk * 8, sdesc(vt + kk * 16 * 128, T::kKVHalf), (j | kk) != 0);
+            mma_bf16_ts<kIdPV>(tmem + col_o(t), d_s + kk * 8, sdesc(vt + kk * T::kPageBytes, 1024, T::kGroupBytes),
+                               (j | kk) != 0);
           if (last) mma_commit(o_full + 8 * t);
+          // The last reader of this V slot is issued: release it as soon as that P.V retires, not
+          // after the S of the next step, so that the producer can fetch step j + 2's V a step earlier.
+          if (t == n_tiles - 1) mma_commit(v_empty + 8 * sv);
         }
         __syncwarp();
         if (!last) {
@@ -518,10 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (failed) break;
-      if (lane == 0) {
-        mma_commit(v_empty + 8 * sv);
-        if (!last) mma_commit(k_empty + 8 * ((j + 1) % kKStages));  // both tiles' S of step j + 1 are in
-      }
+      if (lane == 0 && !last) mma_commit(k_empty + 8 * ((j + 1) % kKStages));  // both tiles' S of step j + 1 are in
       __syncwarp();
     }
     if (failed && lane == 0) atomicOr(p.err, kErrTimeout);
@@ -702,6 +734,26 @@ cudaError_t cache_map(CUtensorMap* map, const void* cache, int64_t rows, int hea
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// The cache as pages for the prefill kernel: 4D [row groups][halves][8 rows][64 dims] bf16
+// (rows = num_blocks * num_kv_heads * 16, two 8-row groups a page), box 64 x 8 x halves x 2:
+// one copy moves a whole page of one kv head into [group][half][8 rows][128 B], 128-byte
+// swizzle (each half's 8 rows one swizzle atom).
+cudaError_t page_map(CUtensorMap* map, const void* cache, int64_t rows, int head_dim) {
+  EncodeTiled enc = nullptr;
+  cudaError_t e = encoder(&enc);
+  if (e != cudaSuccess) return e;
+  const cuuint32_t halves = static_cast<cuuint32_t>(head_dim / 64);
+  const cuuint64_t row_bytes = static_cast<cuuint64_t>(head_dim) * 2;
+  const cuuint64_t dims[4] = {64, 8, halves, static_cast<cuuint64_t>(rows / 8)};
+  const cuuint64_t strides[3] = {row_bytes, 128, 8 * row_bytes};
+  const cuuint32_t box[4] = {64, 8, halves, 2};
+  const cuuint32_t elem[4] = {1, 1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(cache), dims, strides, box, elem,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int D, int G>
 cudaError_t launch_t(const PrefillParams& p, int max_query_len, cudaStream_t stream) {
   constexpr int kCtaTokens = kTiles * kRows / G;
@@ -720,8 +772,8 @@ cudaError_t launch_t(const PrefillParams& p, int max_query_len, cudaStream_t str
   }
   CUtensorMap mk, mv;
   const int64_t rows = p.num_blocks * p.num_kv_heads * kBlockTokens;
-  if ((e = cache_map(&mk, p.k_cache, rows, D)) != cudaSuccess) return e;
-  if ((e = cache_map(&mv, p.v_cache, rows, D)) != cudaSuccess) return e;
+  if ((e = page_map(&mk, p.k_cache, rows, D)) != cudaSuccess) return e;
+  if ((e = page_map(&mv, p.v_cache, rows, D)) != cudaSuccess) return e;
   const dim3 grid((max_query_len + kCtaTokens - 1) / kCtaTokens, p.num_kv_heads, p.num_seqs);
   return launch_pdl(paged_prefill_kernel<D, G>, grid, dim3(kThreads), Pf<D>::kSmem, stream, p, mk, mv);
 }
