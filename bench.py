@@ -11,15 +11,19 @@ bf16 N(0, 1) data from a seeded generator.
 
 Reported (one JSON line on rank 0):
   value       algorithmic GB/s of the step (attention + append bytes) with the
-              inputs resident in HBM, device-timed with CUDA events;
+              inputs resident in HBM, device-timed with CUDA events: the median
+              of repeated timed passes of K steps (at least --passes, and about
+              --min-seconds of timed work, so the clock samples cover it);
   e2e         the same metric through the public API with every step's inputs
               copied from pinned host memory and its output read back, inside
               the timed region; the copies run on their own streams, double-
               buffered, overlapping the neighbouring steps' kernels (the serial
-              form, copies and kernels one after another, is reported beside it);
+              form, copies and kernels one after another, is reported beside it
+              and never replaces it);
   roofline    the partition kernel (dominant): algorithmic bytes per launch /
-              its mean duration (CUDA events on the launching stream) against
-              the measured HBM copy bandwidth;
+              its mean duration (CUDA events on the launching stream, taken in
+              passes interleaved with the value passes) against the measured
+              HBM copy bandwidth;
   cpu_baseline  the fp64 CPU oracle on the host cores, on the same workload.
 ``--impl reference`` times that oracle as the reference arm.
 
@@ -293,6 +297,57 @@ def cpu_baseline(case_cpu, target_s: float = 10.0, max_s: float = 30.0) -> dict:
                                         f"{t1:.1f} s"}}
 
 
+def trace_cpu_baseline(sampled=(0, 50, 99)) -> dict:
+    """The fp64 oracle on the continuous-batching trace, on its sampled steps: every layer of each
+    sampled step with all host threads, and one layer of each with one thread.  The oracle replays
+    a step's work (the joins' prompt appends, the step's appends, attention) on one CPU pool pair
+    of the trace's shape; the values are random, the schedule (slots, tables, lengths) the trace's."""
+    import oracle
+    from workloads import TRACE, TraceGenerator, make_generator, randn_bf16
+    from workloads import algorithmic_bytes as ab
+    spec = TRACE
+    tg = TraceGenerator(spec, seed=0)
+    H, Hkv, D, NL = spec.num_q_heads, spec.num_kv_heads, spec.head_dim, spec.num_layers
+    g = make_generator(2)
+    kc = randn_bf16((tg.num_blocks, Hkv, 16, D), g)
+    vc = randn_bf16((tg.num_blocks, Hkv, 16, D), g)
+    threads = os.cpu_count() or 1
+    res = {"all": [0.0, 0, 0], "one": [0.0, 0, 0]}   # seconds, seq-layers, bytes
+    for st in tg.steps():
+        if st.step not in sampled:
+            continue
+        B = len(st.seq_ids)
+        js = torch.cat([st.join_slots[x] for x in st.joined]) if st.joined else None
+        nbytes = ab(st.context_lens, H, Hkv, D) + append_bytes(B + (0 if js is None else js.numel()), Hkv, D)
+        for layer in range(NL + 1):
+            kind, nt = ("all", threads) if layer < NL else ("one", 1)
+            q = randn_bf16((B, H, D), g)
+            nk, nv = randn_bf16((B, Hkv, D), g), randn_bf16((B, Hkv, D), g)
+            pk = randn_bf16((js.numel(), Hkv, D), g) if js is not None else None
+            pv = randn_bf16((js.numel(), Hkv, D), g) if js is not None else None
+            t = time.perf_counter()
+            if js is not None and oracle.kv_append(pk, pv, js, kc, vc) != oracle.OK:
+                raise RuntimeError("oracle prompt append failed on the trace")
+            if oracle.kv_append(nk, nv, st.slot_mapping, kc, vc) != oracle.OK:
+                raise RuntimeError("oracle append failed on the trace")
+            _, status = oracle.paged_decode_attention(q, kc, vc, st.block_tables, st.context_lens, D ** -0.5,
+                                                      num_threads=nt)
+            res[kind][0] += time.perf_counter() - t
+            if status != oracle.OK:
+                raise RuntimeError("oracle attention failed on the trace")
+            res[kind][1] += B
+            res[kind][2] += nbytes
+
+    def line(kind, cores, sample):
+        sec, n, b = res[kind]
+        return {"value": round(n / sec, 2), "unit": "seq·layer/s", "gbs": round(b / sec / 1e9, 4), "cores": cores,
+                "kind": "oracle", "sample": sample, "seconds": round(sec, 2)}
+
+    out = line("all", threads, f"steps {list(sampled)} x all {NL} layers, fp64, {threads} threads")
+    out["single_thread"] = line("one", 1, f"steps {list(sampled)} x one layer, fp64, one thread")
+    return out
+
+
 def run_reference(args, dist: Dist) -> dict | None:
     """Reference arm: the fp64 CPU oracle on the host cores, rank 0 only."""
     if dist.rank != 0:
@@ -373,18 +428,17 @@ def fused_step_timing(pkv, g, spec, out, ws, stream, K: int, W: int, bytes_step:
 
 
 def e2e_line(pipe_value: float, pipe_s: float, serial_value: float, serial_s: float, K: int, h2d: int,
-             d2h: int) -> dict:
-    """The end-to-end figure: the faster of the two ways of driving the API (the pipelined loop wins
-    on steps long enough to hide its extra stream and event work, the serial one on short steps);
-    both are reported."""
-    pipe = {"value": round(pipe_value / 1e9, 2), "ms_per_step": round(1e3 * pipe_s / K, 4),
-            "copies": "two device slots; step i+1's inputs in and step i-1's output out on two copy "
-                      "streams while step i computes"}
-    serial = {"value": round(serial_value / 1e9, 2), "ms_per_step": round(1e3 * serial_s / K, 4),
-              "copies": "in, kernels, out, one after another on the compute stream"}
-    best, mode = (pipe, "pipelined") if pipe_value >= serial_value else (serial, "serial")
-    return {"value": best["value"], "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "ms_per_step": best["ms_per_step"], "mode": mode, "pipelined": pipe, "serial": serial}
+             d2h: int, passes: int) -> dict:
+    """The end-to-end figure is the pipelined drive, fixed in advance: the way a serving loop would
+    overlap its transfers with the neighbouring steps' kernels.  The serial drive (copy in, kernels,
+    copy out on one stream) is reported beside it and never replaces it."""
+    return {"value": round(pipe_value / 1e9, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": round(1e3 * pipe_s / K, 4), "mode": "pipelined",
+            "copies": "two device slots; step i+1's inputs in and step i-1's output out on two copy streams "
+                      "while step i computes",
+            "passes": passes, "timing": "median of the passes, each K steps",
+            "serial": {"value": round(serial_value / 1e9, 2), "ms_per_step": round(1e3 * serial_s / K, 4),
+                       "copies": "in, kernels, out, one after another on the compute stream"}}
 
 
 def run_ours(args, dist: Dist) -> dict | None:
@@ -466,32 +520,47 @@ def run_ours(args, dist: Dist) -> dict | None:
     ev_part = ([torch.cuda.Event(enable_timing=True) for _ in range(K)],
                [torch.cuda.Event(enable_timing=True) for _ in range(K)])
     t_begin, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def value_pass() -> float:
+        """K steps bracketed by a barrier and a device synchronisation on both sides.  The step loop
+        carries no events between its kernels: an event recorded between two launches would stand
+        between them in the stream and end their programmatic overlap."""
+        dist.barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            t_begin.record(stream)
+            for _ in range(K):
+                step()
+            t_end.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize()
+        dist.barrier()
+        return t_begin.elapsed_time(t_end) / 1e3
+
+    def roofline_pass() -> list[float]:
+        """The same K steps with events around each partition launch on its stream (the roofline)."""
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                step(ev_part, i)
+        stream.synchronize()
+        return [ev_part[0][i].elapsed_time(ev_part[1][i]) for i in range(K)]
+
+    # Repeated passes: at least --passes, and enough for about --min-seconds of timed steps, so that
+    # the clock sampler sees the timed region many times; the median pass is the reported one.
+    first = value_pass()
+    passes = max(args.passes, math.ceil(args.min_seconds / max(first, 1e-6)))
+    passes = int(dist.max(float(min(passes, args.max_passes))))
     launches0 = pkv.kernel_launch_count()
-    dist.barrier()
-    torch.cuda.synchronize()
     wall0 = time.time()
-    # The step loop carries no events between its kernels: an event recorded between two launches
-    # would stand between them in the stream and end their programmatic overlap.
-    with torch.cuda.stream(stream):
-        t_begin.record(stream)
-        for i in range(K):
-            step()
-        t_end.record(stream)
-    stream.synchronize()
-    torch.cuda.synchronize()
-    dist.barrier()
+    pass_s, part_ms = [], []
+    for _ in range(passes):
+        pass_s.append(value_pass())
+        part_ms.extend(roofline_pass())
     wall1 = time.time()
     launches = pkv.kernel_launch_count() - launches0
-    elapsed = t_begin.elapsed_time(t_end) / 1e3
-    # The partition kernel's own duration (the roofline): the same K steps again, with events
-    # around each partition launch on its stream.
-    with torch.cuda.stream(stream):
-        for i in range(K):
-            step(ev_part, i)
-    stream.synchronize()
-    part_ms = [ev_part[0][i].elapsed_time(ev_part[1][i]) for i in range(K)]
     if pkv.get_and_clear_device_error(stream) != 0:
         raise RuntimeError("device error during the timed region")
+    elapsed = statistics.median(pass_s)
 
     # End to end through the public API: this step's inputs staged in one pinned host buffer and sent
     # with one copy, the kernels reading views of its device twin, the output read back to pinned memory.
@@ -531,16 +600,21 @@ def run_ours(args, dist: Dist) -> dict | None:
             e2e_step()
     stream.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    dist.barrier()
-    torch.cuda.synchronize()
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(K):
-            e2e_step()
-        e1.record(stream)
-    stream.synchronize()
-    dist.barrier()
-    serial_elapsed = e0.elapsed_time(e1) / 1e3
+
+    def serial_pass() -> float:
+        dist.barrier()
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(K):
+                e2e_step()
+            e1.record(stream)
+        stream.synchronize()
+        dist.barrier()
+        return e0.elapsed_time(e1) / 1e3
+
+    e2e_passes = int(dist.max(float(max(5, min(passes, math.ceil(args.min_seconds / 4 / max(first, 1e-6)))))))
+    serial_elapsed = statistics.median([serial_pass() for _ in range(e2e_passes)])
     if not torch.equal(out_host, out.cpu()):
         raise RuntimeError("e2e output read-back mismatch")
 
@@ -588,12 +662,16 @@ def run_ours(args, dist: Dist) -> dict | None:
     pipelined(max(W, 2))
     stream.synchronize()
     p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    dist.barrier()
-    torch.cuda.synchronize()
-    pipelined(K, p0, p1)
-    stream.synchronize()
-    dist.barrier()
-    e2e_elapsed = p0.elapsed_time(p1) / 1e3
+
+    def pipelined_pass() -> float:
+        dist.barrier()
+        torch.cuda.synchronize()
+        pipelined(K, p0, p1)
+        stream.synchronize()
+        dist.barrier()
+        return p0.elapsed_time(p1) / 1e3
+
+    e2e_elapsed = statistics.median([pipelined_pass() for _ in range(e2e_passes)])
     for h, o in zip(hosts_out[:min(K, 2)], slots_out):
         if not torch.equal(h, o.cpu()):
             raise RuntimeError("pipelined e2e output read-back mismatch")
@@ -615,6 +693,9 @@ def run_ours(args, dist: Dist) -> dict | None:
     line = {
         "metric": METRIC, "value": round(value / 1e9, 2), "unit": UNIT, "n_gpus": dist.world, "steps": K,
         "warmup": W, "ms_per_step": round(1e3 * slowest / K, 4), "higher_is_better": True, "scaling": "weak",
+        "passes": passes, "timing": "median of the passes, each K steps bracketed by a barrier and a device "
+                                    "synchronisation; ms_per_step of the fastest and slowest pass beside it",
+        "ms_per_step_min_max": [round(1e3 * min(pass_s) / K, 4), round(1e3 * max(pass_s) / K, 4)],
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{spec.name}: {spec.description}", "num_seqs": B, "num_q_heads": hq,
                    "num_kv_heads": hkv, "head_dim": D, "block_size": 16,
@@ -636,8 +717,12 @@ def run_ours(args, dist: Dist) -> dict | None:
                      "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, profiles/traffic.txt "
                                        f"(kernel source {source_hash('paged_decode_partition_kernel')})",
                      "algorithmic_bytes_per_launch": bytes_attn,
-                     "mean_launch_us": round(part_mean_s * 1e6, 2)},
-        "e2e": e2e_line(e2e_value, e2e_elapsed, serial_value, serial_elapsed, K, h2d, d2h),
+                     "mean_launch_us": round(part_mean_s * 1e6, 2),
+                     "launches_timed": len(part_ms),
+                     "launch_us_min_median_max": [round(1e3 * min(part_ms), 2),
+                                                  round(1e3 * statistics.median(part_ms), 2),
+                                                  round(1e3 * max(part_ms), 2)]},
+        "e2e": e2e_line(e2e_value, e2e_elapsed, serial_value, serial_elapsed, K, h2d, d2h, e2e_passes),
         "gpu_launches": launches,
         "clocks": clocks,
         "parity": parity,
@@ -735,6 +820,57 @@ def append_component(args, pkv, peak: float, peak_kind: str) -> dict:
                             "note": "one token per sequence: launch latency, not bandwidth"}}
 
 
+def chain_component(args, pkv, peak: float, peak_kind: str) -> dict:
+    """Decode calls back to back: per-call time of chains of partition-only, partition + merge, and
+    append + partition + merge calls on --workload (CUDA events at each end of a chain of --steps calls,
+    the median of 5 chains), for each partition count in --chain-partitions (0 = the default)."""
+    dev = torch.device("cuda", 0)
+    c = make_decode_case(args.workload, seed=0).to(dev)
+    s = c.spec
+    B, hq, hkv, D = s.num_seqs, s.num_q_heads, s.num_kv_heads, s.head_dim
+    nbytes = algorithmic_bytes(c.context_lens.cpu(), hq, hkv, D)
+    out = torch.empty_like(c.q)
+    stream = torch.cuda.Stream(dev)
+    default = pkv.default_partitions(B, hq, hkv, D, s.max_blocks_per_seq)
+    rows = []
+    for parts in [int(x) or default for x in args.chain_partitions.split(",")]:
+        ws = torch.empty(pkv.workspace_size(B, hq, hkv, D, s.max_blocks_per_seq, parts), dtype=torch.uint8,
+                         device=dev)
+
+        def attend(ph):
+            pkv.paged_decode_attention(c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens, c.scale, out,
+                                       num_partitions=parts, phases=ph, workspace=ws, stream=stream)
+
+        def append():
+            pkv.kv_append(c.new_k, c.new_v, c.slot_mapping, c.k_cache, c.v_cache, stream=stream)
+
+        row = {"num_partitions": parts}
+        for label, fn in (("partition_us", lambda: attend(pkv.PHASE_PARTITION)),
+                          ("partition_merge_us", lambda: attend(pkv.PHASE_ALL)),
+                          ("append_partition_merge_us", lambda: (append(), attend(pkv.PHASE_ALL)))):
+            with torch.cuda.stream(stream):
+                for _ in range(args.warmup):
+                    fn()
+                ts = []
+                for _ in range(5):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    for _ in range(args.steps):
+                        fn()
+                    e1.record(stream)
+                    stream.synchronize()
+                    ts.append(e0.elapsed_time(e1) / args.steps * 1e3)
+            row[label] = round(statistics.median(ts), 2)
+        row["partition_frac"] = round(nbytes / (row["partition_us"] * 1e-6) / 1e9 / peak, 4)
+        row["partition_merge_frac"] = round(nbytes / (row["partition_merge_us"] * 1e-6) / 1e9 / peak, 4)
+        if pkv.get_and_clear_device_error(stream) != 0:
+            raise RuntimeError("device error during the chain timing")
+        rows.append(row)
+    return {"component": "chain", "metric": "decode calls back to back: microseconds per call",
+            "workload": f"{s.name}: {s.description}", "algorithmic_bytes_per_call": nbytes, "chain_length": args.steps,
+            "frac_of": f"{peak_kind} HBM copy bandwidth ({peak} GB/s)", "rows": rows}
+
+
 def run_component(args) -> dict:
     import numpy as np
 
@@ -810,10 +946,14 @@ def run_component(args) -> dict:
         sec = e0.elapsed_time(e1) / 1e3
         if pkv.get_and_clear_device_error() != 0:
             raise RuntimeError("device error during the trace")
+        peak_gbs = bytes_total / sec / 1e9
         return {"component": "trace", "metric": "continuous-batching trace seq·layer/s", "value": round(
-            seq_layers / sec, 1), "unit": "seq·layer/s", "gbs": round(bytes_total / sec / 1e9, 1),
+            seq_layers / sec, 1), "unit": "seq·layer/s", "gbs": round(peak_gbs, 1),
+                "frac_of_measured_hbm": round(peak_gbs / peak, 4), "frac_of_nominal_8TBps": round(
+                    peak_gbs / NOMINAL_HBM_GBS, 4),
                 "seconds": round(sec, 4), "host_wall_seconds": round(wall, 4),
                 "gpu_launches": pkv.kernel_launch_count() - launches0,
+                "cpu_baseline": trace_cpu_baseline() if args.cpu_seconds > 0 else None,
                 "config": {"workload": f"{spec.name}: {NL} layers, <= {spec.max_seqs} sequences, {spec.steps} "
                                        f"decode steps, Poisson({spec.join_rate}) joins / finishes",
                            "seq_layers": seq_layers, "algorithmic_bytes": bytes_total}}
@@ -858,6 +998,8 @@ def run_component(args) -> dict:
                              "compulsory_bytes_per_launch": prefill_compulsory_bytes(c)}}
     if args.component == "kv_append":
         return append_component(args, pkv, peak, peak_kind)
+    if args.component == "chain":
+        return chain_component(args, pkv, peak, peak_kind)
     # copy_blocks: copy-on-write of 4096 distinct block pairs of the Qwen3/LLaMA-3 kv layout.
     dev = torch.device("cuda", 0)
     g = make_generator(7)
@@ -895,7 +1037,11 @@ def run_component(args) -> dict:
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--passes", type=int, default=25, help="least number of timed passes of --steps steps")
+    ap.add_argument("--min-seconds", type=float, default=1.5,
+                    help="timed passes continue until about this much timed GPU work")
+    ap.add_argument("--max-passes", type=int, default=5000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=sorted(SPECS), default="llama3_8b")
@@ -905,8 +1051,10 @@ def main(argv=None) -> int:
                     help="seconds the reference arm's warm-up + timed steps should take")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per partition launch from an ncu capture of the current kernel")
-    ap.add_argument("--component", choices=("copy_blocks", "block_manager", "prefill", "trace", "kv_append"), default=None,
-                    help="measure one component instead of the decode step")
+    ap.add_argument("--component", choices=("copy_blocks", "block_manager", "prefill", "trace", "kv_append", "chain"),
+                    default=None, help="measure one component instead of the decode step")
+    ap.add_argument("--chain-partitions", default="0",
+                    help="chain component: comma-separated num_partitions values (0 = the library default)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
