@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // proves the previous P.V retired, and no barrier can run two phases ahead
   // of its waiter.
   const uint32_t bar = s_base + T::kOffBar;
-  constexpr uint32_t kBarBytes = 8 * (2 * kKStages + 2 * kVStages + 1 + 5 * kTiles);
+  constexpr uint32_t kBarBytes = 8 * (2 * kKStages + 2 * kVStages + 1 + 6 * kTiles);
   static_assert(kBarBytes <= kTmemSlotOffset, "the barriers must end below the TMEM slot");
   const uint32_t k_full = bar, k_empty = k_full + 8 * kKStages, v_full = k_empty + 8 * kKStages,
                  v_empty = v_full + 8 * kVStages, v_tail = v_empty + 8 * kVStages,
@@ -354,7 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       p_full = s_full + 8 * kTiles,                   // [tile]
       o_full = p_full + 8 * kTiles,                   // [tile]
       q_ready = o_full + 8 * kTiles,                  // [tile]
-      mma_drained = q_ready + 8 * kTiles;             // [tile]
+      mma_drained = q_ready + 8 * kTiles,             // [tile]
+      o_staged = mma_drained + 8 * kTiles;            // [tile]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + T::kOffBar + kTmemSlotOffset);
 
   // The producer's first two windows of block ids are requested before the set-up barrier,
@@ -384,6 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bar_init(o_full + 8 * t, 1);
       bar_init(q_ready + 8 * t, 128);
       bar_init(mma_drained + 8 * t, 1);
+      bar_init(o_staged + 8 * t, kRows);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -568,21 +570,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int t = warp >> 2;
     const int r = tid & (kRows - 1);
     const int i = i0 + t * kTokens + r / G;  // chunk token of this row
-    const int g = r % G;
     const bool row_ok = i < C;
-    // Stage Q rows (zero rows past the chunk) in the swizzled K-major layout.
+    // Stage Q (zero rows past the chunk) in the swizzled K-major layout.  The tile's 128
+    // threads load it together, consecutive threads taking consecutive 16-byte chunks of a
+    // row, so that a warp reads two whole rows (a token's G head rows are contiguous).
+    constexpr int kChunks = D / 8;  // 16-byte chunks of a row
+    const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q);
     {
-      const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(p.q) +
-                                                        (static_cast<size_t>(q0 + (row_ok ? i : 0)) * p.num_q_heads +
-                                                         kvh * G + g) * D);
       unsigned char* qt = smem + T::kOffQ + t * T::kQTile;
-#pragma unroll
-      for (int h = 0; h < T::kHalves; ++h)
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch) {
-          const uint4 v = row_ok ? __ldg(src + h * 8 + ch) : make_uint4(0u, 0u, 0u, 0u);
-          *reinterpret_cast<uint4*>(qt + h * T::kQHalf + swz(r, ch)) = v;
-        }
+#pragma unroll 4
+      for (int c = r; c < kRows * kChunks; c += kRows) {
+        const int rr = c / kChunks, ch = c % kChunks;
+        const int ii = i0 + t * kTokens + rr / G;
+        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+        if (ii < C)
+          v = __ldg(reinterpret_cast<const uint4*>(qg + (static_cast<size_t>(q0 + ii) * p.num_q_heads + kvh * G +
+                                                         rr % G) * D) + ch);
+        *reinterpret_cast<uint4*>(qt + (ch / 8) * T::kQHalf + swz(rr, ch % 8)) = v;
+      }
       fence_async_smem();
       bar_arrive(q_ready + 8 * t);
     }
@@ -663,23 +668,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_before_sync();
       bar_arrive(p_full + 8 * t);
     }
-    // Epilogue: O / l, bf16, one 2*D-byte row per thread.
+    // Epilogue: O / l in bf16.  Each thread writes its row into the tile's Q buffer (every S
+    // that read it has retired: the O-final commit follows them), chunks XOR-swizzled by row;
+    // then the tile's 128 threads store the rows together, a warp two whole rows at a time.
+    bool staged = false;
+    unsigned char* ot = smem + T::kOffQ + t * T::kQTile;
     if (!failed && __all_sync(0xffffffffu, bar_wait(o_full + 8 * t, 0))) {
       tc_after_sync();
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
-                                            (static_cast<size_t>(q0 + i) * p.num_q_heads + kvh * G + g) * D);
 #pragma unroll
       for (int c0 = 0; c0 < D; c0 += 32) {
         float o[32];
         tmem_ld32(o_cols + c0, o);
-        if (row_ok) {
 #pragma unroll
-          for (int x = 0; x < 32; x += 8)
-            dst[(c0 + x) / 8] = make_uint4(pack_bf16(o[x] * inv, o[x + 1] * inv), pack_bf16(o[x + 2] * inv, o[x + 3] * inv),
-                                           pack_bf16(o[x + 4] * inv, o[x + 5] * inv),
-                                           pack_bf16(o[x + 6] * inv, o[x + 7] * inv));
-        }
+        for (int x = 0; x < 32; x += 8)
+          *reinterpret_cast<uint4*>(ot + r * (2 * D) + ((((c0 + x) / 8) ^ (r & (kChunks - 1))) << 4)) =
+              make_uint4(pack_bf16(o[x] * inv, o[x + 1] * inv), pack_bf16(o[x + 2] * inv, o[x + 3] * inv),
+                         pack_bf16(o[x + 4] * inv, o[x + 5] * inv), pack_bf16(o[x + 6] * inv, o[x + 7] * inv));
+      }
+      staged = true;
+    } else {
+      failed = true;
+    }
+    // Every thread of the tile arrives, staged or not, so that the bounded wait below ends.
+    bar_arrive(o_staged + 8 * t);
+    if (__all_sync(0xffffffffu, staged && bar_wait(o_staged + 8 * t, 0))) {
+      __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.out);
+#pragma unroll 4
+      for (int c = r; c < kRows * kChunks; c += kRows) {
+        const int rr = c / kChunks, ch = c % kChunks;
+        const int ii = i0 + t * kTokens + rr / G;
+        if (ii < C)
+          reinterpret_cast<uint4*>(og + (static_cast<size_t>(q0 + ii) * p.num_q_heads + kvh * G + rr % G) * D)[ch] =
+              *reinterpret_cast<const uint4*>(ot + rr * (2 * D) + ((ch ^ (rr & (kChunks - 1))) << 4));
       }
     } else {
       failed = true;
