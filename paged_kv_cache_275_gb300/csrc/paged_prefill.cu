@@ -16,7 +16,8 @@
 // operands from shared memory, at N = 128 by the math.
 //   * warp 8: TMA producer.  Each page (16 tokens x D of one kv head) is one 4D
 //     tensor-map copy with 128-byte swizzle, gathered through the block table into
-//     a K ring (3 slots) and a V ring (2 slots), one copy per lane; mbarrier
+//     one ring of five K and V tiles (filled in the order the MMAs read them), one
+//     copy per lane; mbarrier
 //     completion by transaction bytes.  Per-copy cost, not bytes, bounds the copy
 //     engine at 16-token pages, so a page travels as one copy: its two 8-row groups,
 //     each the two 64-dim halves one after the other, a layout both products read
@@ -52,14 +53,15 @@ namespace {
 constexpr int kRows = 128;    // MMA M: query rows of one tile (chunk tokens x group heads)
 constexpr int kTiles = 2;     // query tiles per CTA; every K/V tile feeds both
 constexpr int kKeys = 128;    // keys per step (MMA N of S, MMA K of P.V)
-#ifndef PKV_PF_KSTAGES
-#define PKV_PF_KSTAGES 3
+#ifndef PKV_PF_RING
+#define PKV_PF_RING 5
 #endif
-#ifndef PKV_PF_VSTAGES
-#define PKV_PF_VSTAGES 2
-#endif
-constexpr int kKStages = PKV_PF_KSTAGES;  // K ring depth
-constexpr int kVStages = PKV_PF_VSTAGES;  // V ring depth
+// One ring of K and V tiles, filled in the order the MMAs first read them and freed in the
+// same order: tile n = 2 j is K of key step j, n = 2 j + 1 its V.  Tile n sits in slot
+// n % kRing.  (Separate K and V rings left V a step and a half of lead at most, shorter
+// than its copies take once the copies queue; one ring gives either about two steps.)
+constexpr int kRing = PKV_PF_RING;
+static_assert(kRing >= 3, "the ring must hold a step's K and V and the next K");
 constexpr int kProducerWarp = 4 * kTiles;  // warps 0-7 softmax (four per tile)
 constexpr int kMmaWarp = kProducerWarp + 1;
 constexpr int kThreads = 32 * (kMmaWarp + 1);
@@ -83,9 +85,8 @@ struct Pf {
   static constexpr int kGroupBytes = kHalves * 1024;  // stride between 8-key groups (descriptor SBO)
   static constexpr int kPageBytes = 2 * kGroupBytes;  // one page of one kv head
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kTiles * kQTile;
-  static constexpr int kOffV = kOffK + kKStages * kTile;
-  static constexpr int kOffBar = kOffV + kVStages * kTile;
+  static constexpr int kOffKV = kOffQ + kTiles * kQTile;
+  static constexpr int kOffBar = kOffKV + kRing * kTile;
   // The dynamic shared memory is requested 1024-byte aligned (checked at run time),
   // so no alignment slack: 224.5 KB at D = 128.
   static constexpr int kRaw = kOffBar + 512;  // barriers, TMEM slot, sequence pick
@@ -292,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   int b = blockIdx.z;
   int q0, C, L;
   if (p.num_seqs <= kThreads) {
-    int* s_lens = reinterpret_cast<int*>(smem + T::kOffV);
+    int* s_lens = reinterpret_cast<int*>(smem + T::kOffKV + (kRing - 1) * T::kTile);
     int* s_qs = s_lens + kThreads;
     int& s_pick = *reinterpret_cast<int*>(smem + T::kOffBar + kTmemSlotOffset + 4);
     if (tid < p.num_seqs) {
@@ -339,18 +340,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nsteps = (kv_end + kKeys - 1) / kKeys;
   const bool tail = kv_end < nsteps * kKeys;       // the last step has keys past the end
 
-  // Barriers.  K and V rings: a slot frees when every tile's MMA that reads it has
+  // Barriers.  K/V ring: a slot frees when every tile's MMA that reads it has
   // retired.  Per tile: S ready, P ready, O final, Q staged, MMAs drained.  Each
   // tile has one S buffer (P is written over it), so S of step j + 1 is issued
   // after P.V of step j by the same thread: the S-ready arrival of a step also
   // proves the previous P.V retired, and no barrier can run two phases ahead
   // of its waiter.
   const uint32_t bar = s_base + T::kOffBar;
-  constexpr uint32_t kBarBytes = 8 * (2 * kKStages + 2 * kVStages + 1 + 6 * kTiles);
+  constexpr uint32_t kBarBytes = 8 * (2 * kRing + 1 + 6 * kTiles);
   static_assert(kBarBytes <= kTmemSlotOffset, "the barriers must end below the TMEM slot");
-  const uint32_t k_full = bar, k_empty = k_full + 8 * kKStages, v_full = k_empty + 8 * kKStages,
-                 v_empty = v_full + 8 * kVStages, v_tail = v_empty + 8 * kVStages,
-                 s_full = v_tail + 8,                 // [tile]
+  const uint32_t r_full = bar, r_empty = r_full + 8 * kRing,  // [slot]
+      v_tail = r_empty + 8 * kRing, s_full = v_tail + 8,    // s_full: [tile]
       p_full = s_full + 8 * kTiles,                   // [tile]
       o_full = p_full + 8 * kTiles,                   // [tile]
       q_ready = o_full + 8 * kTiles,                  // [tile]
@@ -370,13 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (tid == 0) {
-    for (int s = 0; s < kKStages; ++s) {
-      bar_init(k_full + 8 * s, 1);
-      bar_init(k_empty + 8 * s, 1);
-    }
-    for (int s = 0; s < kVStages; ++s) {
-      bar_init(v_full + 8 * s, 1);
-      bar_init(v_empty + 8 * s, 1);
+    for (int s = 0; s < kRing; ++s) {
+      bar_init(r_full + 8 * s, 1);
+      bar_init(r_empty + 8 * s, 1);
     }
     bar_init(v_tail, 1);
     for (int t = 0; t < kTiles; ++t) {
@@ -417,8 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto fetch = [&](int page) -> int { return page < npages ? check(page, __ldg(table + page)) : 0; };
     int win = 0;
     int id_cur = check(lane, raw_cur), id_next = check(32 + lane, raw_next);
-    int prev_id = 0;  // this lane's page id of the previous step (for its V)
-    int issued_k = 0, issued_v = 0;
+    int issued = 0;  // ring tiles issued
     // One copy per lane, lane = page of the step: a thread's tensor copies issue one
     // after another, slowly, while copies from different lanes go out together.  A
     // copy moves a whole page of the kv head (both dims halves, 4 KB at D = 128).
@@ -429,42 +424,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (my_pg < pages) tma_load_4d(dst + my_pg * T::kPageBytes, map, 2 * (my_id * p.num_kv_heads + kvh), full);
     };
-    for (int j = 0; j <= nsteps && !failed; ++j) {
-      int my_id = 0;
-      if (j < nsteps) {  // K of step j
-        const int s = j % kKStages;
-        if (j >= kKStages && !__all_sync(0xffffffffu, bar_wait(k_empty + 8 * s, ((j / kKStages) + 1) & 1))) {
-          failed = true;
-          break;
-        }
-        const int first_page = j * kPages;
+    int my_id = 0;  // this lane's page id of the current step (its K and its V)
+    for (int n = 0; n < 2 * nsteps && !failed; ++n) {  // tile n: K (even) or V (odd) of step n / 2
+      const int jn = n >> 1, slot = n % kRing;
+      if (n >= kRing && !__all_sync(0xffffffffu, bar_wait(r_empty + 8 * slot, ((n / kRing) + 1) & 1))) {
+        failed = true;
+        break;
+      }
+      if ((n & 1) == 0) {
+        const int first_page = jn * kPages;
         if (first_page / 32 != win) {  // slide the window
           ++win;
           id_cur = id_next;
           id_next = fetch(32 * (win + 1) + lane);
         }
         my_id = __shfl_sync(0xffffffffu, id_cur, (first_page % 32) + min(my_pg, kPages - 1));
-        issue(j, my_id, s_base + T::kOffK + s * T::kTile, &map_k, k_full + 8 * s);
-        issued_k = j + 1;
       }
-      if (j >= 1) {  // V of step j - 1 uses the ids its K used
-        const int jv = j - 1, sv = jv % kVStages;
-        if (jv >= kVStages && !__all_sync(0xffffffffu, bar_wait(v_empty + 8 * sv, ((jv / kVStages) + 1) & 1))) {
-          failed = true;
-          break;
-        }
-        issue(jv, prev_id, s_base + T::kOffV + sv * T::kTile, &map_v, v_full + 8 * sv);
-        issued_v = jv + 1;
-      }
-      prev_id = my_id;
+      issue(jn, my_id, s_base + T::kOffKV + slot * T::kTile, (n & 1) ? &map_v : &map_k, r_full + 8 * slot);
+      issued = n + 1;
     }
     if (!failed && tail) {
       // Keys past the CTA's end in the last V tile (a page's tail, or pages not
       // copied): zero their rows once the copy has landed, so that stale or NaN
       // data never meets p = 0, then release the tile to the MMA warps.
-      const int jv = nsteps - 1, sv = jv % kVStages;
-      if (__all_sync(0xffffffffu, bar_wait(v_full + 8 * sv, (jv / kVStages) & 1))) {
-        unsigned char* vt = smem + T::kOffV + sv * T::kTile;
+      const int jv = nsteps - 1, nv = 2 * jv + 1;
+      if (__all_sync(0xffffffffu, bar_wait(r_full + 8 * (nv % kRing), (nv / kRing) & 1))) {
+        unsigned char* vt = smem + T::kOffKV + (nv % kRing) * T::kTile;
         const int first = kv_end - jv * kKeys;
         for (int idx = lane; idx < (kKeys - first) * T::kHalves * 8; idx += 32) {
           const int r = first + idx / (T::kHalves * 8);
@@ -480,10 +465,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (failed && lane == 0) {  // let the copies still in flight land before the CTA exits
       atomicOr(p.err, kErrTimeout);
-      for (int j = issued_k > kKStages ? issued_k - kKStages : 0; j < issued_k; ++j)
-        bar_wait(k_full + 8 * (j % kKStages), (j / kKStages) & 1);
-      for (int j = issued_v > kVStages ? issued_v - kVStages : 0; j < issued_v; ++j)
-        bar_wait(v_full + 8 * (j % kVStages), (j / kVStages) & 1);
+      for (int n = issued > kRing ? issued - kRing : 0; n < issued; ++n)
+        bar_wait(r_full + 8 * (n % kRing), (n / kRing) & 1);
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
@@ -495,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr uint32_t kIdS = idesc_bf16(kKeys, false);
     constexpr uint32_t kIdPV = idesc_bf16(D, true);
     auto issue_s = [&](int t, int j) {  // lane 0
-      const uint32_t kt = s_base + T::kOffK + (j % kKStages) * T::kTile;
+      const uint32_t kt = s_base + T::kOffKV + ((2 * j) % kRing) * T::kTile;
       const uint32_t qt = s_base + T::kOffQ + t * T::kQTile;
 #pragma unroll
       for (int h = 0; h < T::kHalves; ++h)
@@ -507,23 +490,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     for (int t = 0; t < n_tiles; ++t)
       if (!bar_wait(q_ready + 8 * t, 0)) failed = true;
-    if (!failed && !bar_wait(k_full, 0)) failed = true;
+    if (!failed && !bar_wait(r_full, 0)) failed = true;  // K of step 0: tile 0, slot 0
     if (!failed) {
       if (lane == 0) {
         tc_after_sync();
         for (int t = 0; t < n_tiles; ++t) issue_s(t, 0);
-        mma_commit(k_empty);
+        mma_commit(r_empty);
       }
       __syncwarp();
     }
     for (int j = 0; j < nsteps && !failed; ++j) {
-      const int sv = j % kVStages;
+      const int nv = 2 * j + 1, sv = nv % kRing;       // V of step j
+      const int nk = 2 * j + 2, sk = nk % kRing;       // K of step j + 1
       const bool last = j == nsteps - 1;
-      if (!(last && tail ? bar_wait(v_tail, 0) : bar_wait(v_full + 8 * sv, (j / kVStages) & 1))) {
+      if (!(last && tail ? bar_wait(v_tail, 0) : bar_wait(r_full + 8 * sv, (nv / kRing) & 1))) {
         failed = true;
         break;
       }
-      const uint32_t vt = s_base + T::kOffV + sv * T::kTile;
+      const uint32_t vt = s_base + T::kOffKV + sv * T::kTile;
       for (int t = 0; t < n_tiles && !failed; ++t) {
         if (!bar_wait(p_full + 8 * t, j & 1)) {
           failed = true;
@@ -538,12 +522,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                (j | kk) != 0);
           if (last) mma_commit(o_full + 8 * t);
           // The last reader of this V slot is issued: release it as soon as that P.V retires, not
-          // after the S of the next step, so that the producer can fetch step j + 2's V a step earlier.
-          if (t == n_tiles - 1) mma_commit(v_empty + 8 * sv);
+          // after the S of the next step, so that the producer can refill it sooner.
+          if (t == n_tiles - 1) mma_commit(r_empty + 8 * sv);
         }
         __syncwarp();
         if (!last) {
-          if (t == 0 && !bar_wait(k_full + 8 * ((j + 1) % kKStages), ((j + 1) / kKStages) & 1)) {
+          if (t == 0 && !bar_wait(r_full + 8 * sk, (nk / kRing) & 1)) {
             failed = true;
             break;
           }
@@ -555,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (failed) break;
-      if (lane == 0 && !last) mma_commit(k_empty + 8 * ((j + 1) % kKStages));  // both tiles' S of step j + 1 are in
+      if (lane == 0 && !last) mma_commit(r_empty + 8 * sk);  // both tiles' S of step j + 1 are in
       __syncwarp();
     }
     if (failed && lane == 0) atomicOr(p.err, kErrTimeout);
