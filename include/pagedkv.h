@@ -80,7 +80,10 @@ typedef enum pkv_status {
 #define PKV_DEVERR_POSITION_OUT_OF_TABLE 0x40u /* decode_step: context_len - 1 >= max_position (last table row used) */
 #define PKV_DEVERR_SMEM_ALIGNMENT 0x80u        /* prefill: dynamic shared memory not 1024-byte aligned (tile skipped) */
 
-/* Largest num_seqs one attention call accepts. */
+/* Most sequences one partition + merge launch pair handles.  A decode call with more runs as
+   consecutive slices of at most PKV_MAX_SEQS sequences, in order on the same stream and workspace
+   (the workspace query sizes it for the largest slice); only the split-phase entry point with a
+   phase mask other than PKV_PHASE_ALL keeps the limit. */
 #define PKV_MAX_SEQS 4096
 
 /* Phases of one attention call (see pkv_paged_decode_attention_split). */
@@ -128,13 +131,16 @@ pkv_status pkv_kv_append(const void* k, const void* v, const int64_t* slot_mappi
  * softmax state that the merge phase combines).  0 picks the default for the
  * current device: the number of warps the GPU keeps resident.  The same
  * num_partitions must be passed to the attention call.  Requires a CUDA device
- * when num_partitions == 0.
+ * when num_partitions == 0.  With num_seqs > PKV_MAX_SEQS the batch runs in
+ * slices and the size is the largest slice's need (each slice's stream is cut
+ * into num_partitions pieces, or its own default count).
  */
 pkv_status pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                      int32_t head_dim, int32_t max_blocks_per_seq, int32_t num_partitions,
                                      size_t* bytes);
 
-/* The default num_partitions for these shapes on the current device (what 0 means). */
+/* The default num_partitions for these shapes on the current device (what 0 means; for
+   num_seqs > PKV_MAX_SEQS, that of a full slice of PKV_MAX_SEQS sequences). */
 pkv_status pkv_decode_default_partitions(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                                          int32_t head_dim, int32_t max_blocks_per_seq,
                                          int32_t* num_partitions);
@@ -183,7 +189,9 @@ pkv_status pkv_paged_decode_attention(const void* q, const void* k_cache, const 
  * PKV_PHASE_MERGE only the merge kernel (which reads what the partition phase
  * left in the workspace, so it must follow a partition phase with identical
  * arguments on the same workspace), PKV_PHASE_ALL both.  The result does not
- * depend on num_partitions beyond fp32 rounding.
+ * depend on num_partitions beyond fp32 rounding.  A phase mask other than
+ * PKV_PHASE_ALL needs num_seqs <= PKV_MAX_SEQS (PKV_ERR_UNSUPPORTED otherwise:
+ * the slices of a larger batch share the workspace).
  */
 pkv_status pkv_paged_decode_attention_split(const void* q, const void* k_cache, const void* v_cache,
                                             const int32_t* block_tables, int32_t max_blocks_per_seq,

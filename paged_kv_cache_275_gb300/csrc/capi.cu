@@ -72,12 +72,15 @@ pkv_status device_state(unsigned** err, int* sms) {
   return PKV_OK;
 }
 
-// Shape checks shared by the workspace query and the attention call.
-pkv_status check_decode_shapes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                               int32_t max_blocks_per_seq) {
+// Sequences of a decode call handled by one partition + merge launch pair (larger batches are
+// cut on the host into consecutive slices of at most this many).
+int32_t launch_seqs(int32_t num_seqs) { return num_seqs < PKV_MAX_SEQS ? num_seqs : PKV_MAX_SEQS; }
+
+// Shape checks shared by the workspace query and the attention calls.  `per_launch` is the most
+// sequences one kernel launch sees (decode slices the batch; prefill takes it whole).
+pkv_status check_shapes(int32_t num_seqs, int32_t per_launch, int32_t num_q_heads, int32_t num_kv_heads,
+                        int32_t head_dim, int32_t max_blocks_per_seq) {
   if (num_seqs < 0) return fail(PKV_ERR_INVALID_ARGUMENT, "num_seqs must be >= 0 (got %d)", num_seqs);
-  if (num_seqs > PKV_MAX_SEQS)
-    return fail(PKV_ERR_UNSUPPORTED, "num_seqs %d exceeds PKV_MAX_SEQS (%d)", num_seqs, PKV_MAX_SEQS);
   if (num_q_heads <= 0 || num_kv_heads <= 0)
     return fail(PKV_ERR_INVALID_ARGUMENT, "head counts must be positive (q %d, kv %d)", num_q_heads, num_kv_heads);
   if (num_q_heads % num_kv_heads != 0)
@@ -90,10 +93,14 @@ pkv_status check_decode_shapes(int32_t num_seqs, int32_t num_q_heads, int32_t nu
     return fail(PKV_ERR_UNSUPPORTED, "head_dim %d not built (64 or 128)", head_dim);
   if (max_blocks_per_seq <= 0)
     return fail(PKV_ERR_INVALID_ARGUMENT, "max_blocks_per_seq must be positive (got %d)", max_blocks_per_seq);
-  if (static_cast<int64_t>(num_seqs) * max_blocks_per_seq * num_kv_heads >= (int64_t{1} << 31) ||
+  if (static_cast<int64_t>(per_launch) * max_blocks_per_seq * num_kv_heads >= (int64_t{1} << 31) ||
       static_cast<int64_t>(max_blocks_per_seq) * PKV_BLOCK_SIZE >= (int64_t{1} << 31))
-    return fail(PKV_ERR_UNSUPPORTED, "num_seqs * max_blocks_per_seq * num_kv_heads must stay below 2^31");
+    return fail(PKV_ERR_UNSUPPORTED, "sequences per launch * max_blocks_per_seq * num_kv_heads must stay below 2^31");
   return PKV_OK;
+}
+pkv_status check_decode_shapes(int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                               int32_t max_blocks_per_seq) {
+  return check_shapes(num_seqs, launch_seqs(num_seqs), num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
 }
 
 constexpr int32_t kMaxPartitions = 1 << 20;
@@ -116,6 +123,26 @@ pkv_status default_partitions(int32_t num_seqs, int32_t num_kv_heads, int32_t he
 size_t workspace_bytes_for(int32_t num_seqs, int32_t head_dim, int32_t group, int32_t num_partitions) {
   return pkv::workspace_header_bytes(num_seqs) +
          static_cast<size_t>(num_partitions) * 2 * pkv::piece_floats(head_dim, group) * sizeof(float);
+}
+
+// Workspace one decode call needs: the most any of its slices needs (a slice of PKV_MAX_SEQS and,
+// when the batch does not divide evenly, the shorter last one; each at its own default partition
+// count unless one is given).
+pkv_status decode_workspace_need(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim, int32_t group,
+                                 int32_t max_blocks_per_seq, int32_t num_partitions, size_t* need) {
+  *need = 0;
+  const int32_t sizes[2] = {launch_seqs(num_seqs), num_seqs > PKV_MAX_SEQS ? num_seqs % PKV_MAX_SEQS : 0};
+  for (int32_t n : sizes) {
+    if (n == 0) continue;
+    int32_t parts = num_partitions;
+    if (parts == 0)
+      if (pkv_status st = default_partitions(n, num_kv_heads, head_dim, group, max_blocks_per_seq, &parts);
+          st != PKV_OK)
+        return st;
+    const size_t b = workspace_bytes_for(n, head_dim, group, parts);
+    if (b > *need) *need = b;
+  }
+  return PKV_OK;
 }
 
 }  // namespace
@@ -151,51 +178,65 @@ static pkv_status decode_impl(const void* q, const void* k_cache, const void* v_
       (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u))
     return fail(PKV_ERR_INVALID_ARGUMENT, "q, caches, out and workspace must be 16-byte aligned");
   const int group = num_q_heads / num_kv_heads;
-  if (num_partitions == 0) {
-    if (pkv_status st = default_partitions(num_seqs, num_kv_heads, head_dim, group, max_blocks_per_seq,
-                                           &num_partitions);
-        st != PKV_OK)
-      return st;
-  }
-  const size_t need = workspace_bytes_for(num_seqs, head_dim, group, num_partitions);
+  if (num_seqs > PKV_MAX_SEQS && phases != PKV_PHASE_ALL)
+    return fail(PKV_ERR_UNSUPPORTED, "phases other than PKV_PHASE_ALL need num_seqs <= PKV_MAX_SEQS (%d)",
+                PKV_MAX_SEQS);
+  size_t need = 0;
+  if (pkv_status st = decode_workspace_need(num_seqs, num_kv_heads, head_dim, group, max_blocks_per_seq,
+                                            num_partitions, &need);
+      st != PKV_OK)
+    return st;
   if (workspace_bytes < need)
     return fail(PKV_ERR_INVALID_ARGUMENT, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
 
   unsigned* err = nullptr;
   if (pkv_status st = device_state(&err, nullptr); st != PKV_OK) return st;
-  pkv::DecodeParams p{};
-  p.q = q;
-  p.k_cache = k_cache;
-  p.v_cache = v_cache;
-  p.block_tables = block_tables;
-  p.context_lens = context_lens;
-  p.out = out;
-  p.ws_prefix = static_cast<int32_t*>(workspace);
-  p.ws_pieces = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + pkv::workspace_header_bytes(num_seqs));
-  p.err = err;
-  p.num_blocks = num_blocks;
-  p.num_seqs = num_seqs;
-  p.num_q_heads = num_q_heads;
-  p.num_kv_heads = num_kv_heads;
-  p.max_blocks_per_seq = max_blocks_per_seq;
-  p.num_partitions = num_partitions;
-  p.qscale = scale * 1.4426950408889634f;
-  if (fused) {
-    p.k_new = fused->k_new;
-    p.v_new = fused->v_new;
-    p.cos_sin = fused->cos_sin;
-    p.max_position = fused->max_position;
-  }
+  // A batch larger than PKV_MAX_SEQS runs as consecutive slices of at most that many sequences,
+  // each a partition + merge pair on the same stream and workspace (a slice's merge has read the
+  // workspace before the next slice's partition kernel, which waits for it, writes it).
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (phases & PKV_PHASE_PARTITION) {
-    const cudaError_t e = pkv::launch_decode_partition(p, head_dim, group, s);
-    if (e != cudaSuccess) return cuda_fail(e, "partition kernel launch");
-    g_launches.fetch_add(1);
-  }
-  if (phases & PKV_PHASE_MERGE) {
-    const cudaError_t e = pkv::launch_decode_merge(p, head_dim, group, s);
-    if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
-    g_launches.fetch_add(1);
+  const size_t q_row = static_cast<size_t>(num_q_heads) * head_dim * 2;  // bytes of one sequence's q / out
+  const size_t kv_row = static_cast<size_t>(num_kv_heads) * head_dim * 2;
+  for (int32_t s0 = 0; s0 < num_seqs; s0 += PKV_MAX_SEQS) {
+    const int32_t n = launch_seqs(num_seqs - s0);
+    int32_t parts = num_partitions;
+    if (parts == 0)
+      if (pkv_status st = default_partitions(n, num_kv_heads, head_dim, group, max_blocks_per_seq, &parts);
+          st != PKV_OK)
+        return st;
+    pkv::DecodeParams p{};
+    p.q = static_cast<const unsigned char*>(q) + s0 * q_row;
+    p.k_cache = k_cache;
+    p.v_cache = v_cache;
+    p.block_tables = block_tables + static_cast<size_t>(s0) * max_blocks_per_seq;
+    p.context_lens = context_lens + s0;
+    p.out = static_cast<unsigned char*>(out) + s0 * q_row;
+    p.ws_prefix = static_cast<int32_t*>(workspace);
+    p.ws_pieces = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + pkv::workspace_header_bytes(n));
+    p.err = err;
+    p.num_blocks = num_blocks;
+    p.num_seqs = n;
+    p.num_q_heads = num_q_heads;
+    p.num_kv_heads = num_kv_heads;
+    p.max_blocks_per_seq = max_blocks_per_seq;
+    p.num_partitions = parts;
+    p.qscale = scale * 1.4426950408889634f;
+    if (fused) {
+      p.k_new = static_cast<const unsigned char*>(fused->k_new) + s0 * kv_row;
+      p.v_new = static_cast<const unsigned char*>(fused->v_new) + s0 * kv_row;
+      p.cos_sin = fused->cos_sin;
+      p.max_position = fused->max_position;
+    }
+    if (phases & PKV_PHASE_PARTITION) {
+      const cudaError_t e = pkv::launch_decode_partition(p, head_dim, group, s);
+      if (e != cudaSuccess) return cuda_fail(e, "partition kernel launch");
+      g_launches.fetch_add(1);
+    }
+    if (phases & PKV_PHASE_MERGE) {
+      const cudaError_t e = pkv::launch_decode_merge(p, head_dim, group, s);
+      if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+      g_launches.fetch_add(1);
+    }
   }
   return ok();
 }
@@ -294,7 +335,9 @@ pkv_status pkv_paged_prefill_attention(const void* q, const void* k_cache, const
                                        int32_t max_query_len, int32_t num_seqs, int32_t num_q_heads,
                                        int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks, int32_t block_size,
                                        float scale, void* out, pkv_stream_t stream) {
-  if (pkv_status st = check_decode_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
+  if (num_seqs > 65535)
+    return fail(PKV_ERR_UNSUPPORTED, "num_seqs %d exceeds 65535 (one grid row of CTAs per sequence)", num_seqs);
+  if (pkv_status st = check_shapes(num_seqs, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
       st != PKV_OK)
     return st;
   if (block_size != PKV_BLOCK_SIZE)
@@ -342,7 +385,7 @@ pkv_status pkv_decode_default_partitions(int32_t num_seqs, int32_t num_q_heads, 
   if (pkv_status st = check_decode_shapes(num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
       st != PKV_OK)
     return st;
-  if (pkv_status st = default_partitions(num_seqs, num_kv_heads, head_dim, num_q_heads / num_kv_heads,
+  if (pkv_status st = default_partitions(launch_seqs(num_seqs), num_kv_heads, head_dim, num_q_heads / num_kv_heads,
                                          max_blocks_per_seq, num_partitions);
       st != PKV_OK)
     return st;
@@ -357,14 +400,12 @@ pkv_status pkv_decode_workspace_size(int32_t num_seqs, int32_t num_q_heads, int3
     return st;
   if (num_partitions < 0 || num_partitions > kMaxPartitions)
     return fail(PKV_ERR_INVALID_ARGUMENT, "num_partitions out of range (got %d)", num_partitions);
-  const int group = num_q_heads / num_kv_heads;
-  if (num_partitions == 0) {
-    if (pkv_status st = default_partitions(num_seqs, num_kv_heads, head_dim, group, max_blocks_per_seq,
-                                           &num_partitions);
-        st != PKV_OK)
-      return st;
-  }
-  *bytes = workspace_bytes_for(num_seqs, head_dim, group, num_partitions);
+  size_t need = 0;
+  if (pkv_status st = decode_workspace_need(num_seqs, num_kv_heads, head_dim, num_q_heads / num_kv_heads,
+                                            max_blocks_per_seq, num_partitions, &need);
+      st != PKV_OK)
+    return st;
+  *bytes = need;
   return ok();
 }
 

@@ -97,7 +97,8 @@ def test_attention_rejects_bad_arguments(lib):
     assert attention(lib, d=256) == 2
     assert attention(lib, bs=8) == 2
     assert attention(lib, B=-1) == 1
-    assert attention(lib, B=5000) == 2 and "PKV_MAX_SEQS" in msg(lib)
+    assert attention(lib, B=5000, phases=1) == 2 and "PKV_MAX_SEQS" in msg(lib)   # split phases: one slice only
+    assert attention(lib, B=5000) == 1 and "workspace too small" in msg(lib)        # sliced, checked as a whole
     assert attention(lib, W=0) == 1
     assert attention(lib, nb=0) == 1
     assert attention(lib, scale=float("inf")) == 1

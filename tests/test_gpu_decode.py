@@ -287,6 +287,40 @@ def test_largest_batch(head_dim, hq, hkv):
     assert device_errors() == 0
 
 
+def test_batch_larger_than_one_launch():
+    """5000 sequences (more than PKV_MAX_SEQS = 4096 per launch pair): the call runs as a slice of 4096
+    and one of 904 on the same workspace.  Its output equals, bit for bit, two calls made on those
+    slices, and matches the oracle; the fused decode step too.  (Lengths of 16 to 40 tokens, or
+    empty: a one- or two-token sequence can give outputs above 4, where one bf16 rounding step alone
+    exceeds the 1e-2 absolute tolerance.)"""
+    import random
+    rng = random.Random(79)
+    n = pkv.MAX_SEQS + 904
+    lens = tuple(rng.choice([0, rng.randint(16, 40)]) for _ in range(n))
+    spec = DecodeSpec(name="over_max_batch", description="", num_seqs=n, num_q_heads=16, num_kv_heads=2,
+                      head_dim=128, max_blocks_per_seq=3, length_kind="fixed", lengths=lens, pool_slack=0.1)
+    c = make_decode_case(spec, seed=80)
+    c.slot_mapping[c.context_lens == 0] = -1
+    ref, _, _ = oracle_step(c)
+    before = pkv.kernel_launch_count()
+    g, out = _run(c, 0)
+    assert pkv.kernel_launch_count() - before == 1 + 2 * 2   # append, then two partition + merge pairs
+    assert_close(out, ref, "5000 sequences")
+    parts = torch.empty_like(g.q)
+    for lo, hi in ((0, pkv.MAX_SEQS), (pkv.MAX_SEQS, n)):
+        pkv.paged_decode_attention(g.q[lo:hi], g.k_cache, g.v_cache, g.block_tables[lo:hi].contiguous(),
+                                   g.context_lens[lo:hi].contiguous(), g.scale, parts[lo:hi])
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), parts.view(torch.int16))
+    g2 = c.to("cuda")
+    step_out = torch.empty_like(g2.q)
+    pkv.decode_step(g2.q, g2.new_k, g2.new_v, g2.k_cache, g2.v_cache, g2.block_tables, g2.context_lens, g2.scale,
+                    step_out)
+    torch.cuda.synchronize()
+    assert_close(step_out, ref, "5000 sequences, fused step")
+    assert device_errors() == 0
+
+
 def test_host_errors_raise_before_launch():
     c = make_decode_case("tiny", seed=15).to("cuda")
     before = pkv.kernel_launch_count()
