@@ -120,8 +120,9 @@ pkv_status default_partitions(int32_t num_seqs, int32_t num_kv_heads, int32_t he
   return PKV_OK;
 }
 
-size_t workspace_bytes_for(int32_t num_seqs, int32_t head_dim, int32_t group, int32_t num_partitions) {
-  return pkv::workspace_header_bytes(num_seqs) +
+size_t workspace_bytes_for(int32_t num_seqs, int32_t num_kv_heads, int32_t head_dim, int32_t group,
+                           int32_t num_partitions) {
+  return pkv::workspace_header_bytes(num_seqs, num_kv_heads) +
          static_cast<size_t>(num_partitions) * 2 * pkv::piece_floats(head_dim, group) * sizeof(float);
 }
 
@@ -139,7 +140,7 @@ pkv_status decode_workspace_need(int32_t num_seqs, int32_t num_kv_heads, int32_t
       if (pkv_status st = default_partitions(n, num_kv_heads, head_dim, group, max_blocks_per_seq, &parts);
           st != PKV_OK)
         return st;
-    const size_t b = workspace_bytes_for(n, head_dim, group, parts);
+    const size_t b = workspace_bytes_for(n, num_kv_heads, head_dim, group, parts);
     if (b > *need) *need = b;
   }
   return PKV_OK;
@@ -212,7 +213,9 @@ static pkv_status decode_impl(const void* q, const void* k_cache, const void* v_
     p.context_lens = context_lens + s0;
     p.out = static_cast<unsigned char*>(out) + s0 * q_row;
     p.ws_prefix = static_cast<int32_t*>(workspace);
-    p.ws_pieces = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) + pkv::workspace_header_bytes(n));
+    p.ws_pairs = reinterpret_cast<int32_t*>(static_cast<unsigned char*>(workspace) + pkv::workspace_prefix_bytes(n));
+    p.ws_pieces = reinterpret_cast<float*>(static_cast<unsigned char*>(workspace) +
+                                           pkv::workspace_header_bytes(n, num_kv_heads));
     p.err = err;
     p.num_blocks = num_blocks;
     p.num_seqs = n;

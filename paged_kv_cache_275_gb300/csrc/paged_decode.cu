@@ -817,6 +817,10 @@ __global__ void __launch_bounds__(NW * 32)
         }
       }
       pair_from_start = (cc.blk == 0);
+      // Record where the pair starts for the merge: this piece, and the slot its state goes to
+      // if the pair is cut (the piece's first pair, or a later one).
+      if (pair_from_start && lane == 0)
+        p.ws_pairs[2 * (static_cast<size_t>(cc.b) * hkv + cc.kvh)] = gw * 2 + (first_pair ? 0 : 1);
     }
     const int valid = seq_len - cc.blk * kBlockTokens;
     if (p.k_new != nullptr && cc.blk == cc.nblk - 1) {
@@ -877,6 +881,7 @@ __global__ void __launch_bounds__(NW * 32)
     }
 
     const bool last_of_pair = (cc.blk == cc.nblk - 1);
+    if (last_of_pair && lane == 0) p.ws_pairs[2 * (static_cast<size_t>(cc.b) * hkv + cc.kvh) + 1] = gw;
     if (last_of_pair || i == n - 1) {
       if constexpr (kMma) {
         // Sum each head's l over the eight lanes that share it, then finish the pair
@@ -1000,7 +1005,7 @@ __global__ void __launch_bounds__(NW * 32)
 // per q head of the group.
 // ---------------------------------------------------------------------------
 #ifndef PKV_MERGE_AHEAD
-#define PKV_MERGE_AHEAD 4
+#define PKV_MERGE_AHEAD 8
 #endif
 template <int D, int G>
 __global__ void __launch_bounds__(G * 32) paged_decode_merge_kernel(const DecodeParams p) {
@@ -1013,44 +1018,45 @@ __global__ void __launch_bounds__(G * 32) paged_decode_merge_kernel(const Decode
   const int lane = threadIdx.x & 31;
   pdl_trigger();
   pdl_wait();
-  const int* prefix = p.ws_prefix;
-  const int nblk = prefix[b + 1] - prefix[b];
+  // One round trip finds the pair's pieces: the partition kernel recorded the piece holding the
+  // pair's first block (and the state slot there) and the piece holding its last block.
+  const int len = p.context_lens[b];
+  const int rec_a = p.ws_pairs[2 * static_cast<size_t>(blockIdx.x)];
+  const int wb = p.ws_pairs[2 * static_cast<size_t>(blockIdx.x) + 1];
+  const int total_blocks = p.ws_prefix[p.num_seqs];
   __nv_bfloat16* orow = static_cast<__nv_bfloat16*>(p.out) +
                         (static_cast<size_t>(b) * p.num_q_heads + kvh * G + g) * D + lane * kPer;
-  if (nblk == 0) {
+  if (len <= 0) {  // an empty sequence (a negative length reads as empty): zeros
 #pragma unroll
     for (int e = 0; e < kPer; ++e) orow[e] = __float2bfloat16_rn(0.f);
     return;
   }
-  const long long total = static_cast<long long>(hkv) * prefix[p.num_seqs];
+  const int wa = rec_a >> 1;
+  if (wa == wb) return;  // whole pair in one piece: already written
+  // With more pieces than items some pieces are empty and hold no state: only then are piece
+  // bounds needed (piece w covers items [w N / P, (w + 1) N / P)).
+  const long long total = static_cast<long long>(hkv) * total_blocks;
   const long long W = p.num_partitions;
-  const long long s = static_cast<long long>(hkv) * prefix[b] + static_cast<long long>(kvh) * nblk;
-  const long long e = s + nblk;
-  const long long wa = ((s + 1) * W - 1) / total;  // piece holding block s
-  const long long wb = (e * W - 1) / total;        // piece holding block e - 1
-  if (wa == wb) return;                            // whole pair in one piece: already written
+  const bool may_be_empty = W > total;
 
   float M = -INFINITY, l = 0.f;
   float acc[kPer];
 #pragma unroll
   for (int x = 0; x < kPer; ++x) acc[x] = 0.f;
-  // Pieces PKV_MERGE_AHEAD at a time: their states are fetched before any is combined
-  // (a pair spans two or three pieces at the LLaMA-3 shape, five or six at the Qwen3
-  // one), and each piece boundary is computed once.
+  // Pieces PKV_MERGE_AHEAD at a time: their states are all fetched before any is combined
+  // (a pair spans two or three pieces at the LLaMA-3 shape, five or six at the Qwen3 one).
   constexpr int kAhead = PKV_MERGE_AHEAD;
-  long long st = wa * total / W;
-  for (long long w0 = wa; w0 <= wb; w0 += kAhead) {
+  for (int w0 = wa; w0 <= wb; w0 += kAhead) {
     float mw[kAhead], lw[kAhead], a[kAhead][kPer];
     bool use[kAhead];
 #pragma unroll
     for (int u = 0; u < kAhead; ++u) {
-      const long long w = w0 + u;
+      const int w = w0 + u;
       use[u] = false;
       if (w <= wb) {
-        const long long en = (w + 1) * total / W;
-        if (st < en) {  // an empty piece covers nothing
+        if (!may_be_empty || w * total / W < (w + 1) * total / W) {  // an empty piece covers nothing
           use[u] = true;
-          const int slot = (w == wa && st < s) ? 1 : 0;
+          const int slot = w == wa ? (rec_a & 1) : 0;
           const float* piece = p.ws_pieces + (static_cast<size_t>(w) * 2 + slot) * T::kPieceFloats;
           mw[u] = piece[G * D + g];
           lw[u] = piece[G * D + G + g];
@@ -1062,7 +1068,6 @@ __global__ void __launch_bounds__(G * 32) paged_decode_merge_kernel(const Decode
             a[u][0] = v.x; a[u][1] = v.y;
           }
         }
-        st = en;
       }
     }
 #pragma unroll
@@ -1192,7 +1197,12 @@ cudaError_t dispatch(int head_dim, int group, F&& f) {
 
 int piece_floats(int head_dim, int group) { return group * head_dim + ((2 * group + 3) / 4) * 4; }
 
-size_t workspace_header_bytes(int num_seqs) { return (static_cast<size_t>(num_seqs + 1) * 4 + 255) & ~size_t(255); }
+size_t workspace_prefix_bytes(int num_seqs) { return (static_cast<size_t>(num_seqs + 1) * 4 + 255) & ~size_t(255); }
+
+size_t workspace_header_bytes(int num_seqs, int num_kv_heads) {
+  return workspace_prefix_bytes(num_seqs) +
+         ((static_cast<size_t>(num_seqs) * num_kv_heads * 8 + 255) & ~size_t(255));
+}
 
 cudaError_t resident_partition_pieces(int head_dim, int group, int num_seqs, int* pieces) {
   return dispatch(head_dim, group, [&](auto inst) { return decltype(inst)::resident_pieces(num_seqs, pieces); });

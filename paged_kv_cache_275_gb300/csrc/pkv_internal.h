@@ -45,6 +45,9 @@ struct DecodeParams {
   const int32_t* context_lens;
   void* out;
   int32_t* ws_prefix;  // workspace: int32 [num_seqs + 1] block prefix over sequences
+  int32_t* ws_pairs;   // workspace: int32 [num_seqs * num_kv_heads][2]: per (sequence, kv head) pair, the
+                       // piece holding its first block (times 2, plus the state slot there) and the piece
+                       // holding its last block
   float* ws_pieces;    // workspace: fp32 partial states, [num_partitions][2][piece_floats]
   unsigned* err;
   int64_t num_blocks;
@@ -98,8 +101,9 @@ cudaError_t launch_kv_append(const AppendParams& p, int num_sms, cudaStream_t st
 
 // Number of fp32 values in one partial-state piece for these shapes.
 int piece_floats(int head_dim, int group);
-// Bytes of the workspace header (block prefix) for num_seqs sequences.
-size_t workspace_header_bytes(int num_seqs);
+// Bytes of the workspace header (block prefix, then the pair records) for num_seqs sequences.
+size_t workspace_prefix_bytes(int num_seqs);
+size_t workspace_header_bytes(int num_seqs, int num_kv_heads);
 // Pieces the partition kernel keeps in flight on the current device: one per warp
 // (the default num_partitions).
 cudaError_t resident_partition_pieces(int head_dim, int group, int num_seqs, int* pieces);

@@ -9,7 +9,8 @@ sum 2^(m_p - M) l_p), and checks, before any rounding to bf16:
   - two different ways of cutting the stream give the same result to 1e-5 relative;
   - each equals the fp64 oracle (unrounded) to 1e-5 relative.
 Relative means normwise over all cut rows: ||x - y||_2 / ||y||_2.  The states' slots are found
-with the same integer arithmetic as the merge kernel's (restated in test_split_k_bookkeeping.py).
+with the integer arithmetic restated in test_split_k_bookkeeping.py, and the pair records the merge
+kernel reads are checked against that model's walk.
 """
 import numpy as np
 import pytest
@@ -18,7 +19,7 @@ import torch
 import paged_kv_cache_275_gb300 as pkv
 from gpu_util import device_errors, oracle_step
 from test_gpu_decode import QWEN3_G8
-from test_split_k_bookkeeping import merge_view
+from test_split_k_bookkeeping import merge_view, walk
 from workloads import make_decode_case
 
 pytestmark = pytest.mark.gpu
@@ -32,7 +33,14 @@ def parked_combination(ws: torch.Tensor, lens_blocks, hkv: int, G: int, D: int, 
     raw = ws.cpu()
     prefix = raw[:4 * (B + 1)].view(torch.int32).numpy()
     assert list(prefix) == list(np.concatenate([[0], np.cumsum(lens_blocks)]))
-    header = ((B + 1) * 4 + 255) & ~255
+    # Workspace: block prefix int32 [B + 1], then the pair records int32 [B * Hkv][2], each 256-byte aligned.
+    rec_at = ((B + 1) * 4 + 255) & ~255
+    header = rec_at + ((B * hkv * 8 + 255) & ~255)
+    recs = raw[rec_at:rec_at + B * hkv * 8].view(torch.int32).numpy().reshape(B, hkv, 2)
+    model: dict = {}
+    walk(list(lens_blocks), hkv, P, model)
+    for (b, k), (rec_a, rec_b) in model.items():   # the records the merge reads are the modelled walk's
+        assert (int(recs[b, k, 0]), int(recs[b, k, 1])) == (rec_a, rec_b), (b, k)
     pf = G * D + ((2 * G + 3) // 4) * 4
     pieces = raw[header:header + P * 2 * pf * 4].view(torch.float32).numpy().astype(np.float64).reshape(P, 2, pf)
     N = hkv * int(prefix[-1])

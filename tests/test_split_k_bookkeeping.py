@@ -3,15 +3,17 @@
 The batch's (sequence, kv head, block) items form one sequence-major stream of N items, cut into P
 pieces, piece w holding items [floor(w N / P), floor((w + 1) N / P)).  Walking its piece, a warp
 writes a pair's output itself when it saw the whole pair, and otherwise parks a partial state in
-slot 0 (the first pair it finishes) or slot 1 (a later one).  The merge finds a cut pair's pieces
-without any record of the walk: wa = floor(((s + 1) P - 1) / N) holds the pair's first item s,
-wb = floor((e P - 1) / N) its last item e - 1, and piece wa's state is in slot 1 exactly when the
-piece began before s.
+slot 0 (the first pair it finishes) or slot 1 (a later one).  The walk also records, for every pair,
+the piece holding its first block with the slot its state takes there, and the piece holding its
+last block; the merge reads those records.  The same pieces follow from the integer arithmetic alone:
+wa = floor(((s + 1) P - 1) / N) holds the pair's first item s, wb = floor((e P - 1) / N) its last item
+e - 1, and piece wa's state is in slot 1 exactly when the piece began before s.
 
 This test restates that integer arithmetic in Python and checks the scheme on random length mixes
 and partition counts, with empty pieces (P > N) and empty sequences:
 - every pair is finished exactly once;
-- a cut pair's states are exactly the non-empty pieces wa..wb, in the slots the merge reads;
+- a cut pair's states are exactly the non-empty pieces wa..wb, in the slots the merge reads, and the
+  records the walk leaves find the same states;
 - no piece parks more than two states.
 The CUDA kernels' own use of it is checked on the GPU (every partition count against the oracle).
 """
@@ -20,8 +22,9 @@ import random
 import pytest
 
 
-def walk(lens_blocks: list[int], hkv: int, P: int):
-    """Simulate the partition kernel's walk: (states, outputs) keyed by pair (b, kvh)."""
+def walk(lens_blocks: list[int], hkv: int, P: int, records: dict | None = None):
+    """Simulate the partition kernel's walk: (states, outputs) keyed by pair (b, kvh).  `records`, if
+    given, receives what the walk writes for the merge: pair -> [first piece * 2 + slot, last piece]."""
     items = [(b, k, j) for b, nb in enumerate(lens_blocks) for k in range(hkv) for j in range(nb)]
     N = len(items)
     states: dict[tuple[int, int], list[tuple[int, int]]] = {}
@@ -35,8 +38,12 @@ def walk(lens_blocks: list[int], hkv: int, P: int):
             b, k, j = items[i]
             if i == st or j == 0:
                 from_start = j == 0
+                if from_start and records is not None:
+                    records.setdefault((b, k), [None, None])[0] = 2 * w + (0 if first_pair else 1)
             nb = lens_blocks[b]
             last_of_pair = j == nb - 1
+            if last_of_pair and records is not None:
+                records.setdefault((b, k), [None, None])[1] = w
             if last_of_pair or i == en - 1:
                 if from_start and last_of_pair:
                     assert (b, k) not in outputs
@@ -46,6 +53,21 @@ def walk(lens_blocks: list[int], hkv: int, P: int):
                     parked[w] += 1
                 first_pair = False
     return N, states, outputs, parked
+
+
+def record_view(records: dict, lens_blocks: list[int], hkv: int, P: int, N: int, b: int, kvh: int):
+    """What the merge kernel computes from the walk's records: None if one piece finished the pair,
+    else its (piece, slot) states.  Piece bounds are used only to skip empty pieces (P > N)."""
+    rec_a, wb = records[(b, kvh)]
+    wa = rec_a // 2
+    if wa == wb:
+        return None
+    got = []
+    for w in range(wa, wb + 1):
+        if P > N and w * N // P == (w + 1) * N // P:
+            continue
+        got.append((w, rec_a % 2 if w == wa else 0))
+    return got
 
 
 def merge_view(lens_blocks: list[int], hkv: int, P: int, N: int, b: int, kvh: int):
@@ -79,7 +101,8 @@ def test_every_pair_is_finished_once_and_the_merge_finds_its_states(seed):
         lens_blocks[0] = 3
     n_items = hkv * sum(lens_blocks)
     for P in sorted({1, 2, 3, rng.randint(1, 50), n_items, n_items + 7, 3 * n_items}):
-        N, states, outputs, parked = walk(lens_blocks, hkv, P)
+        records: dict = {}
+        N, states, outputs, parked = walk(lens_blocks, hkv, P, records)
         assert N == n_items
         assert max(parked) <= 2
         for b, nb in enumerate(lens_blocks):
@@ -88,6 +111,7 @@ def test_every_pair_is_finished_once_and_the_merge_finds_its_states(seed):
                     assert (b, k) not in outputs and (b, k) not in states  # zeros come from the merge kernel
                     continue
                 view = merge_view(lens_blocks, hkv, P, N, b, k)
+                assert record_view(records, lens_blocks, hkv, P, N, b, k) == view  # the records find the same states
                 if view is None:
                     assert (b, k) in outputs and (b, k) not in states
                 else:
