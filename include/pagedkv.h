@@ -216,8 +216,9 @@ pkv_status pkv_paged_decode_attention_split(const void* q, const void* k_cache, 
  * inside the library, which every GPU that loads the library holds until the
  * process exits.  Shapes whose scratch need is larger return
  * PKV_ERR_UNSUPPORTED with a message (at the default partition count on a
- * 152-SM GB300 the built shapes need at most about 10.1 MB, eight q heads per
- * kv head at head_dim 128 with 4096 sequences; four heads about 5.1 MB).  The
+ * 152-SM GB300 the built shapes need at most about 10.4 MB, eight q heads per
+ * kv head at head_dim 128 with 4096 sequences of 8 kv heads; four heads about
+ * 5.4 MB).  The
  * first call on a device,
  * with that device current, looks up the array's device address
  * (cudaGetSymbolAddress); make that first call before any stream capture.
