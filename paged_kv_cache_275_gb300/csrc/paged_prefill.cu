@@ -140,6 +140,13 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(group), "r"(b)
       : "memory");
 }
+// 16 bytes global -> shared without a register round trip; src_bytes 0 writes zeros and reads nothing.
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -556,22 +563,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int i = i0 + t * kTokens + r / G;  // chunk token of this row
     const bool row_ok = i < C;
     // Stage Q (zero rows past the chunk) in the swizzled K-major layout.  The tile's 128
-    // threads load it together, consecutive threads taking consecutive 16-byte chunks of a
-    // row, so that a warp reads two whole rows (a token's G head rows are contiguous).
+    // threads copy it together, consecutive threads taking consecutive 16-byte chunks of a
+    // row, so that a warp reads two whole rows (a token's G head rows are contiguous); the
+    // copies go global -> shared directly, all sixteen of a thread in flight at once.
     constexpr int kChunks = D / 8;  // 16-byte chunks of a row
     const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q);
     {
-      unsigned char* qt = smem + T::kOffQ + t * T::kQTile;
-#pragma unroll 4
+      const uint32_t qt = s_base + T::kOffQ + t * T::kQTile;
+#pragma unroll
       for (int c = r; c < kRows * kChunks; c += kRows) {
         const int rr = c / kChunks, ch = c % kChunks;
         const int ii = i0 + t * kTokens + rr / G;
-        uint4 v = make_uint4(0u, 0u, 0u, 0u);
-        if (ii < C)
-          v = __ldg(reinterpret_cast<const uint4*>(qg + (static_cast<size_t>(q0 + ii) * p.num_q_heads + kvh * G +
-                                                         rr % G) * D) + ch);
-        *reinterpret_cast<uint4*>(qt + (ch / 8) * T::kQHalf + swz(rr, ch % 8)) = v;
+        const bool in_chunk = ii < C;
+        const __nv_bfloat16* src =
+            in_chunk ? qg + (static_cast<size_t>(q0 + ii) * p.num_q_heads + kvh * G + rr % G) * D + ch * 8 : qg;
+        cp_async_16(qt + (ch / 8) * T::kQHalf + swz(rr, ch % 8), src, in_chunk ? 16u : 0u);
       }
+      cp_async_wait_all();
       fence_async_smem();
       bar_arrive(q_ready + 8 * t);
     }

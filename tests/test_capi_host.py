@@ -117,12 +117,13 @@ def test_attention_zero_sequences_is_a_noop(lib):
 def test_workspace_size_with_explicit_partitions(lib):
     n = ctypes.c_size_t(0)
     assert lib.pkv_decode_workspace_size(128, 32, 8, 128, 256, 1000, ctypes.byref(n)) == 0
-    header = ((128 + 1) * 4 + 255) // 256 * 256
+    # Block prefix int32 [B + 1], then the merge's pair records int32 [B * Hkv][2], each 256-byte aligned.
+    header = ((128 + 1) * 4 + 255) // 256 * 256 + (128 * 8 * 8 + 255) // 256 * 256
     piece = 4 * 128 + 8                                  # G * D + round_up(2G, 4) floats
     assert n.value == header + 1000 * 2 * piece * 4
     n1 = ctypes.c_size_t(0)
     assert lib.pkv_decode_workspace_size(4, 2, 1, 64, 3, 12, ctypes.byref(n1)) == 0
-    assert n1.value == 256 + 12 * 2 * (2 * 64 + 4) * 4
+    assert n1.value == 256 + 256 + 12 * 2 * (2 * 64 + 4) * 4
     assert lib.pkv_decode_workspace_size(4, 2, 1, 64, 3, -1, ctypes.byref(n1)) == 1
 
 
