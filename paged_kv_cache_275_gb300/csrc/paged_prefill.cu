@@ -147,6 +147,16 @@ __device__ __forceinline__ void cp_async_16(uint32_t dst, const void* src, uint3
 __device__ __forceinline__ void cp_async_wait_all() {
   asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
+// 3D tensor store shared -> global (one half of a tile's output rows), tracked by a bulk group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int x, int y, int z, uint32_t src) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z), "r"(src)
+               : "memory");
+}
+__device__ __forceinline__ void tma_store_commit_and_wait_read() {
+  asm volatile("cp.async.bulk.commit_group;\n\tcp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_before_sync() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_after_sync() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -276,7 +286,7 @@ __device__ __forceinline__ uint32_t kv_off(int r, int h, int chunk) {
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap map_k,
-                         const __grid_constant__ CUtensorMap map_v) {
+                         const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_out) {
   using T = Pf<D>;
   constexpr int kTokens = kRows / G;            // chunk tokens per 128-row tile
   constexpr int kCtaTokens = kTiles * kTokens;  // chunk tokens per CTA
@@ -660,9 +670,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_before_sync();
       bar_arrive(p_full + 8 * t);
     }
-    // Epilogue: O / l in bf16.  Each thread writes its row into the tile's Q buffer (every S
-    // that read it has retired: the O-final commit follows them), chunks XOR-swizzled by row;
-    // then the tile's 128 threads store the rows together, a warp two whole rows at a time.
+    // Epilogue: O / l in bf16, staged in the tile's Q buffer (every S that read it has retired:
+    // the O-final commit follows them) in Q's own layout, the 128-byte-swizzled dims halves of
+    // rows ordered token-major, head-minor, which is a tensor box of the output.  A tile whose
+    // rows all lie in the chunk then leaves as one tensor store per half; the last, partial tile
+    // of a chunk is stored by the tile's 128 threads together, a warp two whole rows at a time.
     bool staged = false;
     unsigned char* ot = smem + T::kOffQ + t * T::kQTile;
     if (!failed && __all_sync(0xffffffffu, bar_wait(o_full + 8 * t, 0))) {
@@ -673,11 +685,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         float o[32];
         tmem_ld32(o_cols + c0, o);
 #pragma unroll
-        for (int x = 0; x < 32; x += 8)
-          *reinterpret_cast<uint4*>(ot + r * (2 * D) + ((((c0 + x) / 8) ^ (r & (kChunks - 1))) << 4)) =
+        for (int x = 0; x < 32; x += 8) {
+          const int ch = (c0 + x) / 8;
+          *reinterpret_cast<uint4*>(ot + (ch / 8) * T::kQHalf + swz(r, ch % 8)) =
               make_uint4(pack_bf16(o[x] * inv, o[x + 1] * inv), pack_bf16(o[x + 2] * inv, o[x + 3] * inv),
                          pack_bf16(o[x + 4] * inv, o[x + 5] * inv), pack_bf16(o[x + 6] * inv, o[x + 7] * inv));
+        }
       }
+      fence_async_smem();  // the tensor store reads the rows through the async proxy
       staged = true;
     } else {
       failed = true;
@@ -685,14 +700,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Every thread of the tile arrives, staged or not, so that the bounded wait below ends.
     bar_arrive(o_staged + 8 * t);
     if (__all_sync(0xffffffffu, staged && bar_wait(o_staged + 8 * t, 0))) {
-      __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.out);
+      const int tok0 = i0 + t * kTokens;
+      // The tensor map spans num_seqs * max_query_len tokens; a chunk longer than max_query_len (an
+      // error the device flags) can put rows past that, which the threads store instead.
+      const int64_t map_tokens = static_cast<int64_t>(p.num_seqs) * p.max_query_len;
+      if (tok0 + kTokens <= C && static_cast<int64_t>(q0) + tok0 + kTokens <= (map_tokens < INT32_MAX ? map_tokens : INT32_MAX)) {
+        if (r == 0) {
+#pragma unroll
+          for (int h = 0; h < T::kHalves; ++h)
+            tma_store_3d(&map_out, 64 * h, kvh * G, q0 + tok0, s_base + T::kOffQ + t * T::kQTile + h * T::kQHalf);
+          tma_store_commit_and_wait_read();  // the buffer is read before the CTA may leave
+        }
+      } else {
+        __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.out);
 #pragma unroll 4
-      for (int c = r; c < kRows * kChunks; c += kRows) {
-        const int rr = c / kChunks, ch = c % kChunks;
-        const int ii = i0 + t * kTokens + rr / G;
-        if (ii < C)
-          reinterpret_cast<uint4*>(og + (static_cast<size_t>(q0 + ii) * p.num_q_heads + kvh * G + rr % G) * D)[ch] =
-              *reinterpret_cast<const uint4*>(ot + rr * (2 * D) + ((ch ^ (rr & (kChunks - 1))) << 4));
+        for (int c = r; c < kRows * kChunks; c += kRows) {
+          const int rr = c / kChunks, ch = c % kChunks;
+          const int ii = tok0 + rr / G;
+          if (ii < C)
+            reinterpret_cast<uint4*>(og + (static_cast<size_t>(q0 + ii) * p.num_q_heads + kvh * G + rr % G) * D)[ch] =
+                *reinterpret_cast<const uint4*>(ot + (ch / 8) * T::kQHalf + swz(rr, ch % 8));
+        }
       }
     } else {
       failed = true;
@@ -767,6 +795,26 @@ cudaError_t page_map(CUtensorMap* map, const void* cache, int64_t rows, int head
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// The output as [tokens][num_q_heads][head_dim] bf16 for tensor stores: box 64 dims x G heads x kTokens
+// tokens, 128-byte swizzle.  `tokens` bounds the box coordinates only (stores land in whole tiles of rows
+// that lie in a chunk, below the call's total token count).
+cudaError_t out_map(CUtensorMap* map, void* out, int64_t tokens, int num_q_heads, int head_dim, int group,
+                    int tile_tokens) {
+  EncodeTiled enc = nullptr;
+  cudaError_t e = encoder(&enc);
+  if (e != cudaSuccess) return e;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(num_q_heads),
+                              static_cast<cuuint64_t>(tokens)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(head_dim) * 2,
+                                 static_cast<cuuint64_t>(num_q_heads) * head_dim * 2};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(tile_tokens)};
+  const cuuint32_t elem[3] = {1, 1, 1};
+  const CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, out, dims, strides, box, elem,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int D, int G>
 cudaError_t launch_t(const PrefillParams& p, int max_query_len, cudaStream_t stream) {
   constexpr int kCtaTokens = kTiles * kRows / G;
@@ -787,8 +835,12 @@ cudaError_t launch_t(const PrefillParams& p, int max_query_len, cudaStream_t str
   const int64_t rows = p.num_blocks * p.num_kv_heads * kBlockTokens;
   if ((e = page_map(&mk, p.k_cache, rows, D)) != cudaSuccess) return e;
   if ((e = page_map(&mv, p.v_cache, rows, D)) != cudaSuccess) return e;
+  CUtensorMap mo;
+  int64_t tokens = static_cast<int64_t>(p.num_seqs) * max_query_len;
+  if (tokens > INT32_MAX) tokens = INT32_MAX;
+  if ((e = out_map(&mo, p.out, tokens, p.num_q_heads, D, G, kRows / G)) != cudaSuccess) return e;
   const dim3 grid((max_query_len + kCtaTokens - 1) / kCtaTokens, p.num_kv_heads, p.num_seqs);
-  return launch_pdl(paged_prefill_kernel<D, G>, grid, dim3(kThreads), Pf<D>::kSmem, stream, p, mk, mv);
+  return launch_pdl(paged_prefill_kernel<D, G>, grid, dim3(kThreads), Pf<D>::kSmem, stream, p, mk, mv, mo);
 }
 
 }  // namespace
