@@ -132,6 +132,27 @@ __device__ __forceinline__ bool bar_wait(uint32_t b, uint32_t parity) {
   }
   return false;
 }
+__device__ __forceinline__ bool bar_test(uint32_t b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(b), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait that polls without suspending the thread: a completed phase costs the
+// caller one non-blocking test (a suspending try_wait costs a few hundred cycles of
+// issue when the tensor pipe is streaming operands out of shared memory).
+__device__ __forceinline__ bool bar_poll(uint32_t b, uint32_t parity) {
+  if (bar_test(b, parity)) return true;
+  const unsigned long long t0 = now_ns();
+  for (uint32_t it = 1; it < (1u << 30); ++it) {
+    if (bar_test(b, parity)) return true;
+    if ((it & 63u) == 0 && now_ns() - t0 > kWaitNs) return false;
+  }
+  return false;
+}
 // 4D tensor copy: one page of one kv head (box 64 dims x 8 rows x halves x 2 row groups).
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int group, uint32_t b) {
   asm volatile(
@@ -487,50 +508,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == kMmaWarp) {
-    // ---------------- MMA issuer (one lane) ----------------
+    // ---------------- MMA issuer (lane 0 alone) ----------------
     // Ping-pong over the two tiles: S of both for step 0, then per step j and tile
     // t: O_t += P_t V_j as soon as P_t is ready, followed at once by S_t of step
     // j + 1.  The tensor pipe runs one tile's MMAs while the other tile's softmax
     // runs.  S = Q K^T is N = 128 keys, P V is N = D.
-    constexpr uint32_t kIdS = idesc_bf16(kKeys, false);
-    constexpr uint32_t kIdPV = idesc_bf16(D, true);
-    auto issue_s = [&](int t, int j) {  // lane 0
-      const uint32_t kt = s_base + T::kOffKV + ((2 * j) % kRing) * T::kTile;
-      const uint32_t qt = s_base + T::kOffQ + t * T::kQTile;
+    // The issuer shares its SM sub-partition with two softmax warps whose dense
+    // floating-point runs leave it few issue slots, and the pipe idles whenever the
+    // issuer is late at a group boundary.  So lane 0 runs the loop alone (no warp
+    // collectives), waits by polling without suspending, and does a step's copy waits
+    // (V of the step and K of the next) before the tiles' groups, so that a tile's
+    // P.V and next S issue back to back.
+    if (lane == 0) {
+      constexpr uint32_t kIdS = idesc_bf16(kKeys, false);
+      constexpr uint32_t kIdPV = idesc_bf16(D, true);
+      const uint32_t q_base = s_base + T::kOffQ, kv_base = s_base + T::kOffKV;
+      auto issue_s = [&](int t, int j) {
+        const uint32_t kt = kv_base + ((2 * j) % kRing) * T::kTile;
+        const uint32_t qt = q_base + t * T::kQTile;
 #pragma unroll
-      for (int h = 0; h < T::kHalves; ++h)
+        for (int h = 0; h < T::kHalves; ++h)
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_bf16<kIdS>(tmem + col_s(t), sdesc(qt + h * T::kQHalf + kk * 32),
-                         sdesc(kt + h * 1024 + kk * 32, 1024, T::kGroupBytes), (h | kk) != 0);
-      mma_commit(s_full + 8 * t);
-    };
-    for (int t = 0; t < n_tiles; ++t)
-      if (!bar_wait(q_ready + 8 * t, 0)) failed = true;
-    if (!failed && !bar_wait(r_full, 0)) failed = true;  // K of step 0: tile 0, slot 0
-    if (!failed) {
-      if (lane == 0) {
+          for (int kk = 0; kk < 4; ++kk)
+            mma_bf16<kIdS>(tmem + col_s(t), sdesc(qt + h * T::kQHalf + kk * 32),
+                           sdesc(kt + h * 1024 + kk * 32, 1024, T::kGroupBytes), (h | kk) != 0);
+        mma_commit(s_full + 8 * t);
+      };
+      for (int t = 0; t < n_tiles; ++t)
+        if (!bar_poll(q_ready + 8 * t, 0)) failed = true;
+      if (!failed && !bar_poll(r_full, 0)) failed = true;  // K of step 0: tile 0, slot 0
+      if (!failed) {
         tc_after_sync();
         for (int t = 0; t < n_tiles; ++t) issue_s(t, 0);
         mma_commit(r_empty);
       }
-      __syncwarp();
-    }
-    for (int j = 0; j < nsteps && !failed; ++j) {
-      const int nv = 2 * j + 1, sv = nv % kRing;       // V of step j
-      const int nk = 2 * j + 2, sk = nk % kRing;       // K of step j + 1
-      const bool last = j == nsteps - 1;
-      if (!(last && tail ? bar_wait(v_tail, 0) : bar_wait(r_full + 8 * sv, (nv / kRing) & 1))) {
-        failed = true;
-        break;
-      }
-      const uint32_t vt = s_base + T::kOffKV + sv * T::kTile;
-      for (int t = 0; t < n_tiles && !failed; ++t) {
-        if (!bar_wait(p_full + 8 * t, j & 1)) {
+      for (int j = 0; j < nsteps && !failed; ++j) {
+        const int nv = 2 * j + 1, sv = nv % kRing;  // V of step j
+        const int nk = 2 * j + 2, sk = nk % kRing;  // K of step j + 1
+        const bool last = j == nsteps - 1;
+        if (!(last && tail ? bar_poll(v_tail, 0) : bar_poll(r_full + 8 * sv, (nv / kRing) & 1)) ||
+            (!last && !bar_poll(r_full + 8 * sk, (nk / kRing) & 1))) {
           failed = true;
           break;
         }
-        if (lane == 0) {
+        const uint32_t vt = kv_base + sv * T::kTile;
+        for (int t = 0; t < n_tiles; ++t) {
+          if (!bar_poll(p_full + 8 * t, j & 1)) {
+            failed = true;
+            break;
+          }
           tc_after_sync();
           const uint32_t d_s = tmem + col_s(t);
 #pragma unroll
@@ -541,29 +567,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           // The last reader of this V slot is issued: release it as soon as that P.V retires, not
           // after the S of the next step, so that the producer can refill it sooner.
           if (t == n_tiles - 1) mma_commit(r_empty + 8 * sv);
+          if (!last) issue_s(t, j + 1);  // overwrites P only after the P.V above (same issuer, in order)
         }
-        __syncwarp();
-        if (!last) {
-          if (t == 0 && !bar_wait(r_full + 8 * sk, (nk / kRing) & 1)) {
-            failed = true;
-            break;
-          }
-          if (lane == 0) {
-            tc_after_sync();
-            issue_s(t, j + 1);  // overwrites P only after the P.V above (same issuer, in order)
-          }
-          __syncwarp();
-        }
+        if (failed) break;
+        if (!last) mma_commit(r_empty + 8 * sk);  // both tiles' S of step j + 1 are in
       }
-      if (failed) break;
-      if (lane == 0 && !last) mma_commit(r_empty + 8 * sk);  // both tiles' S of step j + 1 are in
-      __syncwarp();
-    }
-    if (failed && lane == 0) atomicOr(p.err, kErrTimeout);
-    // Every MMA this warp issued must have completed before the TMEM is freed.
-    if (lane == 0) {
+      if (failed) atomicOr(p.err, kErrTimeout);
+      // Every MMA this lane issued must have completed before the TMEM is freed.
       mma_commit(mma_drained);
-      bar_wait(mma_drained, 0);
+      bar_poll(mma_drained, 0);
     }
     __syncwarp();
   } else if ((warp >> 2) < n_tiles) {
