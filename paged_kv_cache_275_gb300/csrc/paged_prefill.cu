@@ -522,16 +522,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdS = idesc_bf16(kKeys, false);
       constexpr uint32_t kIdPV = idesc_bf16(D, true);
-      const uint32_t q_base = s_base + T::kOffQ, kv_base = s_base + T::kOffKV;
+      const uint32_t kv_base = s_base + T::kOffKV;
+      // A descriptor's address field is (address >> 4) in 14 bits and every address here is below
+      // 256 KB, so the descriptor of base + offset is the base's descriptor + (offset >> 4): one add
+      // of a constant per MMA operand.
+      const uint64_t d_q = sdesc(s_base + T::kOffQ), d_kv = sdesc(kv_base, 1024, T::kGroupBytes);
       auto issue_s = [&](int t, int j) {
-        const uint32_t kt = kv_base + ((2 * j) % kRing) * T::kTile;
-        const uint32_t qt = q_base + t * T::kQTile;
+        const uint64_t q = d_q + static_cast<uint32_t>((t * T::kQTile) >> 4);
+        const uint64_t k = d_kv + static_cast<uint32_t>((((2 * j) % kRing) * T::kTile) >> 4);
 #pragma unroll
         for (int h = 0; h < T::kHalves; ++h)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_bf16<kIdS>(tmem + col_s(t), sdesc(qt + h * T::kQHalf + kk * 32),
-                           sdesc(kt + h * 1024 + kk * 32, 1024, T::kGroupBytes), (h | kk) != 0);
+            mma_bf16<kIdS>(tmem + col_s(t), q + static_cast<uint32_t>((h * T::kQHalf + kk * 32) >> 4),
+                           k + static_cast<uint32_t>((h * 1024 + kk * 32) >> 4), (h | kk) != 0);
         mma_commit(s_full + 8 * t);
       };
       for (int t = 0; t < n_tiles; ++t)
@@ -551,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           failed = true;
           break;
         }
-        const uint32_t vt = kv_base + sv * T::kTile;
+        const uint64_t v = d_kv + static_cast<uint32_t>((sv * T::kTile) >> 4);
         for (int t = 0; t < n_tiles; ++t) {
           if (!bar_poll(p_full + 8 * t, j & 1)) {
             failed = true;
@@ -561,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t d_s = tmem + col_s(t);
 #pragma unroll
           for (int kk = 0; kk < kKeys / 16; ++kk)
-            mma_bf16_ts<kIdPV>(tmem + col_o(t), d_s + kk * 8, sdesc(vt + kk * T::kPageBytes, 1024, T::kGroupBytes),
+            mma_bf16_ts<kIdPV>(tmem + col_o(t), d_s + kk * 8, v + static_cast<uint32_t>((kk * T::kPageBytes) >> 4),
                                (j | kk) != 0);
           if (last) mma_commit(o_full + 8 * t);
           // The last reader of this V slot is issued: release it as soon as that P.V retires, not
