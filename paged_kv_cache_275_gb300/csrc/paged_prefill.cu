@@ -217,6 +217,38 @@ __device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       "r"(a_tmem), "l"(b), "r"(acc), "n"(kIdesc)
       : "memory");
 }
+// Four MMAs in one block, operand i at base + i * step (descriptor units of 16 bytes, or tensor
+// memory columns for an A in tensor memory); only the first may start a fresh accumulation.
+template <uint32_t kIdesc, uint32_t kAStep, uint32_t kBStep>
+__device__ __forceinline__ void mma4_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc_first) {
+  asm volatile(
+      "{\n\t.reg .pred pf, pt;\n\t.reg .b64 a1, a2, a3, b1, b2, b3;\n\t"
+      "setp.ne.b32 pf, %3, 0;\n\tsetp.eq.b32 pt, %3, %3;\n\t"
+      "add.s64 a1, %1, %5;\n\tadd.s64 a2, %1, %6;\n\tadd.s64 a3, %1, %7;\n\t"
+      "add.s64 b1, %2, %8;\n\tadd.s64 b2, %2, %9;\n\tadd.s64 b3, %2, %10;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %4, pf;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a1, b1, %4, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a2, b2, %4, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], a3, b3, %4, pt;\n\t}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(acc_first), "n"(kIdesc), "n"(kAStep), "n"(2 * kAStep), "n"(3 * kAStep), "n"(kBStep),
+      "n"(2 * kBStep), "n"(3 * kBStep)
+      : "memory");
+}
+template <uint32_t kIdesc, uint32_t kAStep, uint32_t kBStep>
+__device__ __forceinline__ void mma4_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t acc_first) {
+  asm volatile(
+      "{\n\t.reg .pred pf, pt;\n\t.reg .b32 a1, a2, a3;\n\t.reg .b64 b1, b2, b3;\n\t"
+      "setp.ne.b32 pf, %3, 0;\n\tsetp.eq.b32 pt, %3, %3;\n\t"
+      "add.u32 a1, %1, %5;\n\tadd.u32 a2, %1, %6;\n\tadd.u32 a3, %1, %7;\n\t"
+      "add.s64 b1, %2, %8;\n\tadd.s64 b2, %2, %9;\n\tadd.s64 b3, %2, %10;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, pf;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], b1, %4, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], b2, %4, pt;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], b3, %4, pt;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(acc_first), "n"(kIdesc), "n"(kAStep), "n"(2 * kAStep), "n"(3 * kAStep), "n"(kBStep),
+      "n"(2 * kBStep), "n"(3 * kBStep)
+      : "memory");
+}
 __device__ __forceinline__ void mma_commit(uint32_t b) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(b) : "memory");
 }
@@ -531,11 +563,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t q = d_q + static_cast<uint32_t>((t * T::kQTile) >> 4);
         const uint64_t k = d_kv + static_cast<uint32_t>((((2 * j) % kRing) * T::kTile) >> 4);
 #pragma unroll
-        for (int h = 0; h < T::kHalves; ++h)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_bf16<kIdS>(tmem + col_s(t), q + static_cast<uint32_t>((h * T::kQHalf + kk * 32) >> 4),
-                           k + static_cast<uint32_t>((h * 1024 + kk * 32) >> 4), (h | kk) != 0);
+        for (int h = 0; h < T::kHalves; ++h)  // four K steps of 16 dims (32 bytes) per 64-dim half
+          mma4_ss<kIdS, 2, 2>(tmem + col_s(t), q + static_cast<uint32_t>((h * T::kQHalf) >> 4),
+                              k + static_cast<uint32_t>((h * 1024) >> 4), h != 0);
         mma_commit(s_full + 8 * t);
       };
       for (int t = 0; t < n_tiles; ++t)
@@ -564,9 +594,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_after_sync();
           const uint32_t d_s = tmem + col_s(t);
 #pragma unroll
-          for (int kk = 0; kk < kKeys / 16; ++kk)
-            mma_bf16_ts<kIdPV>(tmem + col_o(t), d_s + kk * 8, v + static_cast<uint32_t>((kk * T::kPageBytes) >> 4),
-                               (j | kk) != 0);
+          for (int g = 0; g < kKeys / 64; ++g)  // four pages of 16 keys each: P columns 8 apart
+            mma4_ts<kIdPV, 8, T::kPageBytes / 16>(tmem + col_o(t), d_s + g * 32,
+                                                  v + static_cast<uint32_t>((g * 4 * T::kPageBytes) >> 4), (j | g) != 0);
           if (last) mma_commit(o_full + 8 * t);
           // The last reader of this V slot is issued: release it as soon as that P.V retires, not
           // after the S of the next step, so that the producer can refill it sooner.
