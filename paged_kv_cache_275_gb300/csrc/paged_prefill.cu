@@ -439,6 +439,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (32 + lane < npages) raw_next = __ldg(table + 32 + lane);
   }
 
+  // Stage Q (zero rows past the chunk) in the swizzled K-major layout, issued before the set-up
+  // so that its latency overlaps the barrier and tensor-memory set-up.  The tile's 128 threads
+  // copy it together, consecutive threads taking consecutive 16-byte chunks of a row, so that a
+  // warp reads two whole rows (a token's G head rows are contiguous); the copies go global ->
+  // shared directly, all sixteen of a thread in flight at once.  The Q area is not used by the
+  // sequence ranking above.
+  if ((warp >> 2) < n_tiles && warp < kProducerWarp) {
+    constexpr int kChunks = D / 8;
+    const int t = warp >> 2, r = tid & (kRows - 1);
+    const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q);
+    const uint32_t qt = s_base + T::kOffQ + t * T::kQTile;
+#pragma unroll
+    for (int c = r; c < kRows * kChunks; c += kRows) {
+      const int rr = c / kChunks, ch = c % kChunks;
+      const int ii = i0 + t * kTokens + rr / G;
+      const bool in_chunk = ii < C;
+      const __nv_bfloat16* src =
+          in_chunk ? qg + (static_cast<size_t>(q0 + ii) * p.num_q_heads + kvh * G + rr % G) * D + ch * 8 : qg;
+      cp_async_16(qt + (ch / 8) * T::kQHalf + swz(rr, ch % 8), src, in_chunk ? 16u : 0u);
+    }
+  }
+
   if (tid == 0) {
     for (int s = 0; s < kRing; ++s) {
       bar_init(r_full + 8 * s, 1);
@@ -618,27 +640,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = tid & (kRows - 1);
     const int i = i0 + t * kTokens + r / G;  // chunk token of this row
     const bool row_ok = i < C;
-    // Stage Q (zero rows past the chunk) in the swizzled K-major layout.  The tile's 128
-    // threads copy it together, consecutive threads taking consecutive 16-byte chunks of a
-    // row, so that a warp reads two whole rows (a token's G head rows are contiguous); the
-    // copies go global -> shared directly, all sixteen of a thread in flight at once.
+    // Q's copies were issued before the set-up barrier (see there).
     constexpr int kChunks = D / 8;  // 16-byte chunks of a row
-    const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q);
-    {
-      const uint32_t qt = s_base + T::kOffQ + t * T::kQTile;
-#pragma unroll
-      for (int c = r; c < kRows * kChunks; c += kRows) {
-        const int rr = c / kChunks, ch = c % kChunks;
-        const int ii = i0 + t * kTokens + rr / G;
-        const bool in_chunk = ii < C;
-        const __nv_bfloat16* src =
-            in_chunk ? qg + (static_cast<size_t>(q0 + ii) * p.num_q_heads + kvh * G + rr % G) * D + ch * 8 : qg;
-        cp_async_16(qt + (ch / 8) * T::kQHalf + swz(rr, ch % 8), src, in_chunk ? 16u : 0u);
-      }
-      cp_async_wait_all();
-      fence_async_smem();
-      bar_arrive(q_ready + 8 * t);
-    }
+    cp_async_wait_all();
+    fence_async_smem();
+    bar_arrive(q_ready + 8 * t);
     const float qk = p.scale * kLog2e;
     const int limit = row_ok ? prefix + i + 1 : 0;  // keys this row may see
     float m_used = -INFINITY, l = 0.f;
