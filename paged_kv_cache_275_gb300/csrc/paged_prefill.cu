@@ -461,11 +461,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
 
-  if (tid == 0) {
-    for (int s = 0; s < kRing; ++s) {
-      bar_init(r_full + 8 * s, 1);
-      bar_init(r_empty + 8 * s, 1);
+  // The producer sets up its ring barriers itself and sends K of step 0 (slot 0) before the
+  // set-up barrier, so that the first tile's copies also overlap the set-up; everyone else
+  // touches the ring barriers only after that barrier.  Step 0's pages are lanes 0..7 of the
+  // first block-id window.
+  if (warp == kProducerWarp) {
+    if (lane == 0) {
+      for (int s = 0; s < kRing; ++s) {
+        bar_init(r_full + 8 * s, 1);
+        bar_init(r_empty + 8 * s, 1);
+      }
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    __syncwarp();
+    const int pages0 = min(kPages, npages);
+    if (lane == 0) bar_expect_tx(r_full, static_cast<uint32_t>(pages0 * T::kPageBytes));
+    __syncwarp();
+    if (lane < pages0) {
+      const int id = (raw_cur < 0 || raw_cur >= p.num_blocks) ? 0 : raw_cur;  // flagged by the producer below
+      tma_load_4d(s_base + T::kOffKV + lane * T::kPageBytes, &map_k, 2 * (id * p.num_kv_heads + kvh), r_full);
+    }
+  }
+  if (tid == 0) {
     bar_init(v_tail, 1);
     for (int t = 0; t < kTiles; ++t) {
       bar_init(s_full + 8 * t, 1);
@@ -532,7 +549,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         my_id = __shfl_sync(0xffffffffu, id_cur, (first_page % 32) + min(my_pg, kPages - 1));
       }
-      issue(jn, my_id, s_base + T::kOffKV + slot * T::kTile, (n & 1) ? &map_v : &map_k, r_full + 8 * slot);
+      if (n > 0)  // K of step 0 went out before the set-up barrier
+        issue(jn, my_id, s_base + T::kOffKV + slot * T::kTile, (n & 1) ? &map_v : &map_k, r_full + 8 * slot);
       issued = n + 1;
     }
     if (!failed && tail) {
