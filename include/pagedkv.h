@@ -286,12 +286,14 @@ pkv_status pkv_decode_step(const void* q, const void* k_new, const void* v_new, 
  * with K_j / V_j found through block_tables as in paged decode (kv head h / G).
  * bf16 in and out; S = q K^T and O = P V run as tcgen05 MMAs with fp32
  * accumulation, P is rounded to bf16 for the second product (the softmax
- * denominator sums the same rounded values).
+ * denominator sums the fp32 weights, within 2^-9 relative of the rounded ones).
  *
  *   q, out        device, bf16 [T][num_q_heads][head_dim], T = query_start[num_seqs]
  *   query_start   device, int32 [num_seqs + 1], non-decreasing, query_start[0] = 0
- *   max_query_len host: at least every C_b (sizes the grid)
- * No workspace.  num_seqs == 0 or max_query_len == 0 is a no-op.  Device-side:
+ *   max_query_len host: at least every C_b (sizes the grid); at most 65535 CTAs
+ *                 of 256 / G chunk tokens (G = num_q_heads / num_kv_heads), else
+ *                 PKV_ERR_UNSUPPORTED
+ * num_seqs at most 65535, else PKV_ERR_UNSUPPORTED.  No workspace.  num_seqs == 0 or max_query_len == 0 is a no-op.  Device-side:
  * C_b > max_query_len or C_b > context_lens[b] sets
  * PKV_DEVERR_CONTEXT_LEN_TOO_LONG (that sequence is skipped or cut); a bad
  * block id sets PKV_DEVERR_BLOCK_ID_OUT_OF_RANGE (block 0 is read instead).

@@ -350,6 +350,11 @@ pkv_status pkv_paged_prefill_attention(const void* q, const void* k_cache, const
                 (long long)num_blocks);
   if (!std::isfinite(scale)) return fail(PKV_ERR_INVALID_ARGUMENT, "scale must be finite");
   if (max_query_len < 0) return fail(PKV_ERR_INVALID_ARGUMENT, "max_query_len must be >= 0 (got %d)", max_query_len);
+  // A CTA takes two 128-row tiles of 128 / G chunk tokens each; its sequence's tiles are one grid dimension.
+  const int32_t cta_tokens = 256 / (num_q_heads / num_kv_heads);
+  if ((static_cast<int64_t>(max_query_len) + cta_tokens - 1) / cta_tokens > 65535)
+    return fail(PKV_ERR_UNSUPPORTED, "max_query_len %d exceeds 65535 CTAs of %d chunk tokens", max_query_len,
+                cta_tokens);
   if (num_seqs == 0 || max_query_len == 0) return ok();
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start || !out)
     return fail(PKV_ERR_INVALID_ARGUMENT, "null pointer argument");

@@ -348,15 +348,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   pdl_trigger();
   pdl_wait();
 
-  const int tile = static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x);  // longest tiles first
-  const int kvh = blockIdx.y;
+  const int tile = static_cast<int>(gridDim.y) - 1 - static_cast<int>(blockIdx.y);  // longest tiles first
+  const int kvh = blockIdx.x;
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int lane = tid & 31;
-  // Longest sequences first: CTAs start in blockIdx order (x fastest), so z indexes the
-  // sequences by decreasing context length (ties by index); with x = tiles from the
-  // longest, the launch order approximates longest-processing-time-first and the last
-  // wave holds the shortest tiles.  Ranked in shared memory when num_seqs <= kThreads,
+  // Longest first: CTAs start in blockIdx order (x fastest), so z indexes the sequences by
+  // decreasing context length (ties by index), y counts a sequence's tiles from the longest
+  // (the last rows of a chunk see the most keys) and x is the kv head: all kv heads of a
+  // sequence's longest tile go out before its next tile.  The launch order approximates
+  // longest-processing-time-first, and the last wave holds the shortest tiles.  Ranked in shared memory when num_seqs <= kThreads,
   // in the V ring (not yet in use) and a spare word of the barrier area.
   // The sequences' chunk starts are staged beside the lengths in the same pass, so that the
   // picked sequence's q0, C and L need no second round trip to memory.
@@ -909,7 +910,7 @@ cudaError_t launch_t(const PrefillParams& p, int max_query_len, cudaStream_t str
   int64_t tokens = static_cast<int64_t>(p.num_seqs) * max_query_len;
   if (tokens > INT32_MAX) tokens = INT32_MAX;
   if ((e = out_map(&mo, p.out, tokens, p.num_q_heads, D, G, kRows / G)) != cudaSuccess) return e;
-  const dim3 grid((max_query_len + kCtaTokens - 1) / kCtaTokens, p.num_kv_heads, p.num_seqs);
+  const dim3 grid(p.num_kv_heads, (max_query_len + kCtaTokens - 1) / kCtaTokens, p.num_seqs);
   return launch_pdl(paged_prefill_kernel<D, G>, grid, dim3(kThreads), Pf<D>::kSmem, stream, p, mk, mv, mo);
 }
 

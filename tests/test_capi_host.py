@@ -110,6 +110,24 @@ def test_attention_rejects_bad_arguments(lib):
     assert attention(lib, wsb=16) == 1 and "workspace too small" in msg(lib)
 
 
+def prefill(lib, **kw):
+    a = dict(q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, W=8, cl=FAKE, qs=FAKE, mql=512, B=4, hq=32, hkv=8, d=128, nb=100,
+             bs=16, scale=0.088, out=FAKE, stream=None)
+    a.update(kw)
+    return lib.pkv_paged_prefill_attention(a["q"], a["kc"], a["vc"], a["bt"], a["W"], a["cl"], a["qs"], a["mql"], a["B"],
+                                           a["hq"], a["hkv"], a["d"], a["nb"], a["bs"], a["scale"], a["out"],
+                                           a["stream"])
+
+
+def test_prefill_rejects_grids_it_cannot_launch(lib):
+    """A sequence's CTAs (256 / G chunk tokens each) are one grid dimension, at most 65535."""
+    assert prefill(lib, B=65536) == 2 and "65535" in msg(lib)
+    assert prefill(lib, mql=65535 * 64 + 1) == 2 and "max_query_len" in msg(lib)      # G = 4: 64 tokens a CTA
+    assert prefill(lib, mql=65535 * 32 + 1, hq=64) == 2 and "32 chunk tokens" in msg(lib)   # G = 8
+    assert prefill(lib, mql=-1) == 1
+    assert prefill(lib, mql=0, q=None, out=None) == 0                                   # a no-op before the pointers
+
+
 def test_attention_zero_sequences_is_a_noop(lib):
     assert attention(lib, B=0, q=None, out=None) == 0
 
