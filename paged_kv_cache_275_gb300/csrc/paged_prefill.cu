@@ -27,10 +27,13 @@
 //     accumulate): S = Q_t K^T into tile t's TMEM S buffer (M 128, N 128); once
 //     the softmax has written P over S, O_t += P V (M 128, N = D, P read from
 //     TMEM) and at once S of the next step.  The two tiles alternate, so one
-//     tile's softmax overlaps the other's MMAs.  The warp also allocates and
-//     frees the 512 TMEM columns.
+//     tile's softmax overlaps the other's MMAs.  Lane 0 runs the loop alone and
+//     polls its waits: the softmax warps sharing its SM sub-partition leave it
+//     few issue slots, and the pipe idles while the issuer is late at a group
+//     boundary.  The warp also allocates and frees the 512 TMEM columns.
 //   * warps 0-7 (one row each; warps 4t..4t+3 serve tile t, each warp the TMEM
-//     lanes 32 (warp % 4) .. + 31): stage Q, then per key step read S
+//     lanes 32 (warp % 4) .. + 31): stage Q (copies issued before the set-up
+//     barrier, as is the producer's first K tile), then per key step read S
 //     (tcgen05.ld), apply the causal and length mask, run the online softmax in
 //     base 2 (lazy rescale: O is rescaled only when a row's max grows by more than
 //     2^8), write P as bf16 pairs into TMEM over the S values just read; finally
