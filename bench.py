@@ -964,7 +964,7 @@ def run_component(args) -> dict:
                            "seq_layers": seq_layers, "algorithmic_bytes": bytes_total}}
     if args.component == "prefill":
         from workloads import make_prefill_case, prefill_flops
-        c = make_prefill_case("prefill_llama3_8b", seed=0).to("cuda")
+        c = make_prefill_case(args.prefill_workload, seed=0).to("cuda")
         pkv.kv_append(c.new_k, c.new_v, c.slot_mapping, c.k_cache, c.v_cache)
         out = torch.empty_like(c.q)
         max_q = max(c.spec.chunk_lens)
@@ -1016,7 +1016,7 @@ def run_component(args) -> dict:
                              "frac_of_burst": round(tf / burst_peak, 4), "timed_seconds": round(t_stop - t_start, 2),
                              "fastest_pass_tflops": round(flops / min(pass_sec) / 1e12, 2),
                              "algorithmic_flops_per_launch": flops,
-                             "traffic": recorded_traffic("paged_prefill_kernel", "prefill_llama3_8b"),
+                             "traffic": recorded_traffic("paged_prefill_kernel", args.prefill_workload),
                              "traffic_source": "ncu dram__bytes_read.sum + dram__bytes_write.sum, profiles/traffic.txt "
                                                f"(kernel source {source_hash('paged_prefill_kernel')})",
                              "compulsory_bytes_per_launch": prefill_compulsory_bytes(c)}}
@@ -1075,6 +1075,8 @@ def main(argv=None) -> int:
                     help="seconds the reference arm's warm-up + timed steps should take")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per partition launch from an ncu capture of the current kernel")
+    ap.add_argument("--prefill-workload", choices=("prefill_llama3_8b", "prefill_qwen3_0.6b"), default="prefill_llama3_8b",
+                    help="chunked-prefill workload of --component prefill")
     ap.add_argument("--component", choices=("copy_blocks", "block_manager", "prefill", "trace", "kv_append", "chain"),
                     default=None, help="measure one component instead of the decode step")
     ap.add_argument("--chain-partitions", default="0",
