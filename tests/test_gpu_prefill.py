@@ -99,6 +99,16 @@ def test_prefill_long_prefix():
     assert device_errors() == 0
 
 
+def test_prefill_long_chunk_spans_many_grid_rows():
+    """A 2048-token chunk at G = 8 (32 chunk tokens a CTA): 64 CTAs of one sequence and kv head along the
+    grid's tile dimension, launched longest first, beside a short chunk whose tiles run out early."""
+    spec = PrefillSpec("long_chunk", "", 8, 1, 64, (2048, 45), (0, 0), 140)
+    c = make_prefill_case(spec, seed=21, prefixes=[100, 7])
+    _, out = _run(c)
+    assert_close(out, _ref(c), "long chunk")
+    assert device_errors() == 0
+
+
 @pytest.mark.parametrize("seed", range(8))
 def test_prefill_random_shapes(seed):
     """Seeded random layouts: head dim, group size, sequence count, chunk and prefix lengths (chunks from
