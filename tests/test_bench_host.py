@@ -124,3 +124,18 @@ def test_e2e_is_the_pipelined_drive_whichever_is_faster():
     assert short_step["mode"] == "pipelined" and short_step["value"] == round(2.3e12 / 1e9, 2)
     assert short_step["serial"]["value"] > short_step["value"]
     assert short_step["h2d_bytes_per_step"] == 10 and short_step["d2h_bytes_per_step"] == 20
+
+
+def test_bf16_peak_burst_and_sustained(tmp_path, monkeypatch):
+    """A kernel timed alone is compared with the burst GEMM rate, one timed in a second-long loop with the
+    sustained one; without the measured file the fallbacks are used and said to be."""
+    import json
+    import bench
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"bf16_tflops": 1913.6, "bf16_tflops_sustained": 1696.8}))
+    monkeypatch.setattr(bench, "ROOT", tmp_path)
+    assert bench.bf16_peak_tflops() == (1913.6, "measured")
+    assert bench.bf16_peak_tflops(sustained=True) == (1696.8, "measured")
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"bf16_tflops": 1913.6}))
+    assert bench.bf16_peak_tflops(sustained=True) == (1913.6, "measured")   # no sustained figure measured
+    (tmp_path / "MEASURED_PEAKS.json").unlink()
+    assert bench.bf16_peak_tflops()[1] == "fallback" and bench.bf16_peak_tflops(True)[1] == "fallback"
