@@ -202,26 +202,9 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int n, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (b_mn_major ? (1u << 16) : 0u) | ((static_cast<uint32_t>(n) >> 3) << 17) |
          ((128u >> 4) << 24);
 }
-// The instruction descriptor is an immediate operand.
-template <uint32_t kIdesc>
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %3, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %4, p;\n\t}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(acc), "n"(kIdesc)
-      : "memory");
-}
-// Same, with A read from tensor memory (128 lanes = rows, K along the columns as bf16 pairs).
-template <uint32_t kIdesc>
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t acc) {
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %3, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %4, p;\n\t}" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b), "r"(acc), "n"(kIdesc)
-      : "memory");
-}
 // Four MMAs in one block, operand i at base + i * step (descriptor units of 16 bytes, or tensor
-// memory columns for an A in tensor memory); only the first may start a fresh accumulation.
+// memory columns for an A in tensor memory, 128 lanes = rows, K along the columns as bf16 pairs);
+// only the first may start a fresh accumulation.  The instruction descriptor is an immediate.
 template <uint32_t kIdesc, uint32_t kAStep, uint32_t kBStep>
 __device__ __forceinline__ void mma4_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t acc_first) {
   asm volatile(
