@@ -969,9 +969,18 @@ def run_component(args) -> dict:
         out = torch.empty_like(c.q)
         max_q = max(c.spec.chunk_lens)
 
+        if args.prefill_splits == 0:  # the library's one-wave choice
+            args.prefill_splits = pkv.prefill_default_splits(c.context_lens.shape[0], max_q, c.spec.num_q_heads,
+                                                             c.spec.num_kv_heads)
+        ws = None
+        if args.prefill_splits > 1:
+            ws = torch.empty(pkv.prefill_workspace_size(c.context_lens.shape[0], max_q, c.spec.num_q_heads,
+                                                        c.spec.num_kv_heads, c.spec.head_dim, args.prefill_splits),
+                             dtype=torch.uint8, device="cuda")
+
         def call():
             pkv.paged_prefill_attention(c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens, c.query_start,
-                                        max_q, c.scale, out)
+                                        max_q, c.scale, out, num_splits=args.prefill_splits, workspace=ws)
 
         for _ in range(args.warmup):
             call()
@@ -1009,6 +1018,7 @@ def run_component(args) -> dict:
                 "us_per_launch_min_max": [round(min(pass_sec) * 1e6, 2), round(max(pass_sec) * 1e6, 2)],
                 "timing": "median of the passes, each `steps` launches between CUDA events", "clocks": clocks,
                 "config": {"workload": c.spec.description, "tokens": int(c.q.shape[0]),
+                           "num_splits": args.prefill_splits,
                            "context_lens": c.context_lens.tolist()},
                 "roofline": {"bound": "tensor", "achieved": round(tf, 2), "peak": bf16_peak, "unit": "TFLOP/s",
                              "frac": round(tf / bf16_peak, 4),
@@ -1075,8 +1085,11 @@ def main(argv=None) -> int:
                     help="seconds the reference arm's warm-up + timed steps should take")
     ap.add_argument("--traffic", type=float, default=None,
                     help="DRAM bytes per partition launch from an ncu capture of the current kernel")
-    ap.add_argument("--prefill-workload", choices=("prefill_llama3_8b", "prefill_qwen3_0.6b"), default="prefill_llama3_8b",
-                    help="chunked-prefill workload of --component prefill")
+    ap.add_argument("--prefill-workload", choices=("prefill_llama3_8b", "prefill_qwen3_0.6b", "prefill_llama3_8b_one"),
+                    default="prefill_llama3_8b", help="chunked-prefill workload of --component prefill")
+    ap.add_argument("--prefill-splits", type=int, default=1,
+                    help="split each tile pair's key steps over this many CTAs (merge pass after); 0: the "
+                         "library's choice (one wave)")
     ap.add_argument("--component", choices=("copy_blocks", "block_manager", "prefill", "trace", "kv_append", "chain"),
                     default=None, help="measure one component instead of the decode step")
     ap.add_argument("--chain-partitions", default="0",

@@ -306,6 +306,49 @@ pkv_status pkv_paged_prefill_attention(const void* q, const void* k_cache, const
                                        float scale, void* out, pkv_stream_t stream);
 
 /*
+ * The same computation with each (tile pair, kv head, sequence) split over
+ * num_splits CTAs, each taking a contiguous share of the key steps (keys 128 at
+ * a time), and a merge pass that combines their fp32 partial states: for a row,
+ * M = max m_s, out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s (the split-K
+ * reduction of paged decode).  For calls whose CTAs do not fill the GPU (few
+ * sequences, short chunks); a split with no key step only marks its rows empty.
+ * Results equal the unsplit call's within fp32 rounding.
+ *
+ *   num_splits       host, 1..32; 1 is pkv_paged_prefill_attention (no workspace)
+ *   workspace        device, 16-byte aligned, at least pkv_prefill_workspace_size
+ *                    bytes; owned by the caller, fully overwritten, unused after the
+ *                    call's kernels finish (two launches on `stream`)
+ * Errors as pkv_paged_prefill_attention, plus: num_splits out of range, a null or
+ * short workspace (PKV_ERR_INVALID_ARGUMENT); num_seqs * num_splits above 65535
+ * (PKV_ERR_UNSUPPORTED).  On a device-side timeout the outputs are undefined.
+ */
+pkv_status pkv_paged_prefill_attention_split(const void* q, const void* k_cache, const void* v_cache,
+                                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                             const int32_t* context_lens, const int32_t* query_start,
+                                             int32_t max_query_len, int32_t num_seqs, int32_t num_q_heads,
+                                             int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
+                                             int32_t block_size, float scale, void* out, int32_t num_splits,
+                                             void* workspace, size_t workspace_bytes, pkv_stream_t stream);
+
+/*
+ * A split count for pkv_paged_prefill_attention_split: the most splits that
+ * keep the call's CTAs (num_seqs * num_kv_heads * ceil(max_query_len / (256 / G)))
+ * within one CTA per SM of the current device, at most 32; 1 when the call already
+ * fills the GPU.  A heuristic on host-known sizes only (the chunks and cached
+ * lengths are on the device).  Queries the current device; writes *num_splits.
+ */
+pkv_status pkv_prefill_default_splits(int32_t num_seqs, int32_t max_query_len, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t* num_splits);
+
+/*
+ * Workspace bytes of pkv_paged_prefill_attention_split: num_splits * num_seqs *
+ * R * num_q_heads * (head_dim + 2) * 4, R = max_query_len rounded up to the CTA's
+ * 256 / G chunk tokens (0 for num_splits = 1).  Host only; writes *bytes.
+ */
+pkv_status pkv_prefill_workspace_size(int32_t num_seqs, int32_t max_query_len, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t head_dim, int32_t num_splits, size_t* bytes);
+
+/*
  * Copy whole KV blocks inside the pool: the copy half of copy-on-write for
  * blocks shared between sequences.  The pages let requests share a prompt's
  * KV blocks ("v0版本介绍", section "为什么需要推理框架") and plan a prefix

@@ -51,6 +51,9 @@ EXPORTS = (
     "pkv_copy_blocks",
     "pkv_decode_step",
     "pkv_paged_prefill_attention",
+    "pkv_paged_prefill_attention_split",
+    "pkv_prefill_workspace_size",
+    "pkv_prefill_default_splits",
     "pkv_bm_create",
     "pkv_bm_destroy",
     "pkv_bm_num_free",
@@ -103,6 +106,10 @@ def load(path: Path | str | None = None) -> ctypes.CDLL:
                                         ctypes.c_float, V, V, SZ, V]
         lib.pkv_paged_prefill_attention.argtypes = [V, V, V, V, I32, V, V, I32, I32, I32, I32, I32, I64, I32,
                                                     ctypes.c_float, V, V]
+        lib.pkv_paged_prefill_attention_split.argtypes = [V, V, V, V, I32, V, V, I32, I32, I32, I32, I32, I64, I32,
+                                                          ctypes.c_float, V, I32, V, SZ, V]
+        lib.pkv_prefill_workspace_size.argtypes = [I32, I32, I32, I32, I32, I32, ctypes.POINTER(SZ)]
+        lib.pkv_prefill_default_splits.argtypes = [I32, I32, I32, I32, ctypes.POINTER(I32)]
         lib.pkv_bm_create.argtypes = [I64, V, ctypes.POINTER(V)]
         lib.pkv_bm_destroy.argtypes = [V]
         lib.pkv_bm_num_free.argtypes = [V, ctypes.POINTER(I64)]
@@ -118,6 +125,7 @@ def load(path: Path | str | None = None) -> ctypes.CDLL:
                      "pkv_paged_decode_attention", "pkv_paged_decode_attention_split",
                      "pkv_paged_decode_attention_static", "pkv_get_and_clear_device_error",
                      "pkv_selftest_wait_timeout", "pkv_copy_blocks", "pkv_decode_step", "pkv_paged_prefill_attention",
+                     "pkv_paged_prefill_attention_split", "pkv_prefill_workspace_size", "pkv_prefill_default_splits",
                      "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_num_free", "pkv_bm_add_sequence",
                      "pkv_bm_append_slots", "pkv_bm_fork", "pkv_bm_free_sequence", "pkv_bm_block_tables",
                      "pkv_bm_ref_count"):
@@ -393,12 +401,32 @@ def decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor, k_cac
     return out
 
 
+def prefill_workspace_size(num_seqs: int, max_query_len: int, num_q_heads: int, num_kv_heads: int, head_dim: int,
+                           num_splits: int) -> int:
+    """Bytes of the workspace of a split prefill call (0 for num_splits = 1)."""
+    n = ctypes.c_size_t(0)
+    _check(load().pkv_prefill_workspace_size(num_seqs, max_query_len, num_q_heads, num_kv_heads, head_dim, num_splits,
+                                             ctypes.byref(n)))
+    return n.value
+
+
+def prefill_default_splits(num_seqs: int, max_query_len: int, num_q_heads: int, num_kv_heads: int) -> int:
+    """The split count that keeps the call's CTAs in one wave on the current device (1 when it fills it)."""
+    n = ctypes.c_int32(0)
+    _check(load().pkv_prefill_default_splits(num_seqs, max_query_len, num_q_heads, num_kv_heads, ctypes.byref(n)))
+    return n.value
+
+
 def paged_prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                             block_tables: torch.Tensor, context_lens: torch.Tensor, query_start: torch.Tensor,
                             max_query_len: int, scale: float, out: torch.Tensor,
-                            stream: torch.cuda.Stream | None = None) -> torch.Tensor:
+                            stream: torch.cuda.Stream | None = None, num_splits: int = 1,
+                            workspace: torch.Tensor | None = None) -> torch.Tensor:
     """Chunked prefill: q / out [T, Hq, D] bf16, query_start [B + 1] int32; causal over each sequence's
-    context_lens[b] - (chunk length) cached tokens plus the chunk.  Returns ``out``."""
+    context_lens[b] - (chunk length) cached tokens plus the chunk.  ``num_splits`` > 1 splits each CTA's keys
+    over that many CTAs and merges their partial states (a uint8 ``workspace`` of ``prefill_workspace_size``
+    bytes, allocated here if not given); ``prefill_default_splits`` gives a count for calls that do not fill
+    the GPU.  Returns ``out``."""
     _require(q, "q", torch.bfloat16, 3)
     dev = q.device
     _require(k_cache, "k_cache", torch.bfloat16, 4, dev)
@@ -413,9 +441,21 @@ def paged_prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
     if out.shape != q.shape or query_start.shape[0] != B + 1 or block_tables.shape[0] != B:
         raise ValueError("shape mismatch")
     with torch.cuda.device(dev):
-        _check(load().pkv_paged_prefill_attention(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-                                                  block_tables.data_ptr(), block_tables.shape[1],
-                                                  context_lens.data_ptr(), query_start.data_ptr(), int(max_query_len),
-                                                  B, hq, hkv, d, nb, bs, float(scale), out.data_ptr(),
-                                                  _stream_handle(stream)))
+        if num_splits == 1:
+            _check(load().pkv_paged_prefill_attention(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                                      block_tables.data_ptr(), block_tables.shape[1],
+                                                      context_lens.data_ptr(), query_start.data_ptr(),
+                                                      int(max_query_len), B, hq, hkv, d, nb, bs, float(scale),
+                                                      out.data_ptr(), _stream_handle(stream)))
+            return out
+        if workspace is None:
+            workspace = torch.empty(prefill_workspace_size(B, int(max_query_len), hq, hkv, d, int(num_splits)),
+                                    dtype=torch.uint8, device=dev)
+        _require(workspace, "workspace", torch.uint8, 1, dev)
+        _check(load().pkv_paged_prefill_attention_split(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                                        block_tables.data_ptr(), block_tables.shape[1],
+                                                        context_lens.data_ptr(), query_start.data_ptr(),
+                                                        int(max_query_len), B, hq, hkv, d, nb, bs, float(scale),
+                                                        out.data_ptr(), int(num_splits), workspace.data_ptr(),
+                                                        workspace.numel(), _stream_handle(stream)))
     return out

@@ -332,14 +332,19 @@ pkv_status pkv_selftest_wait_timeout(uint64_t limit_ns, pkv_stream_t stream) {
   return ok();
 }
 
-pkv_status pkv_paged_prefill_attention(const void* q, const void* k_cache, const void* v_cache,
-                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                       const int32_t* context_lens, const int32_t* query_start,
-                                       int32_t max_query_len, int32_t num_seqs, int32_t num_q_heads,
-                                       int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks, int32_t block_size,
-                                       float scale, void* out, pkv_stream_t stream) {
-  if (num_seqs > 65535)
-    return fail(PKV_ERR_UNSUPPORTED, "num_seqs %d exceeds 65535 (one grid row of CTAs per sequence)", num_seqs);
+namespace {
+constexpr int32_t kMaxPrefillSplits = 32;  // the merge reads one split per lane
+
+pkv_status prefill_impl(const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+                        int32_t max_blocks_per_seq, const int32_t* context_lens, const int32_t* query_start,
+                        int32_t max_query_len, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                        int32_t head_dim, int64_t num_blocks, int32_t block_size, float scale, void* out,
+                        int32_t num_splits, void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+  if (num_splits < 1 || num_splits > kMaxPrefillSplits)
+    return fail(PKV_ERR_INVALID_ARGUMENT, "num_splits must be in [1, %d] (got %d)", kMaxPrefillSplits, num_splits);
+  if (static_cast<int64_t>(num_seqs) * num_splits > 65535)
+    return fail(PKV_ERR_UNSUPPORTED, "num_seqs * num_splits = %lld exceeds 65535 (one grid row of CTAs each)",
+                static_cast<long long>(num_seqs) * num_splits);
   if (pkv_status st = check_shapes(num_seqs, num_seqs, num_q_heads, num_kv_heads, head_dim, max_blocks_per_seq);
       st != PKV_OK)
     return st;
@@ -362,6 +367,13 @@ pkv_status pkv_paged_prefill_attention(const void* q, const void* k_cache, const
       (reinterpret_cast<uintptr_t>(block_tables) & 3u) || (reinterpret_cast<uintptr_t>(context_lens) & 3u) ||
       (reinterpret_cast<uintptr_t>(query_start) & 3u))
     return fail(PKV_ERR_INVALID_ARGUMENT, "q, caches and out must be 16-byte aligned");
+  if (num_splits > 1) {
+    const size_t need =
+        pkv::prefill_workspace_bytes(num_seqs, max_query_len, num_q_heads, num_kv_heads, head_dim, num_splits);
+    if (!workspace || workspace_bytes < need)
+      return fail(PKV_ERR_INVALID_ARGUMENT, "workspace too small: %zu bytes given, %zu needed", workspace_bytes, need);
+    if (!aligned16(workspace)) return fail(PKV_ERR_INVALID_ARGUMENT, "workspace must be 16-byte aligned");
+  }
   unsigned* err = nullptr;
   if (pkv_status st = device_state(&err, nullptr); st != PKV_OK) return st;
   pkv::PrefillParams p{};
@@ -380,10 +392,68 @@ pkv_status pkv_paged_prefill_attention(const void* q, const void* k_cache, const
   p.max_blocks_per_seq = max_blocks_per_seq;
   p.max_query_len = max_query_len;
   p.scale = scale;
+  if (num_splits > 1) {
+    p.num_splits = num_splits;
+    p.ws = static_cast<float*>(workspace);
+  }
   const cudaError_t e = pkv::launch_paged_prefill(p, head_dim, num_q_heads / num_kv_heads, max_query_len,
                                                   reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "prefill kernel launch");
-  g_launches.fetch_add(1);
+  g_launches.fetch_add(num_splits > 1 ? 2 : 1);
+  return ok();
+}
+}  // namespace
+
+pkv_status pkv_paged_prefill_attention(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                       const int32_t* context_lens, const int32_t* query_start,
+                                       int32_t max_query_len, int32_t num_seqs, int32_t num_q_heads,
+                                       int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks, int32_t block_size,
+                                       float scale, void* out, pkv_stream_t stream) {
+  return prefill_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, query_start, max_query_len,
+                      num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, out, 1, nullptr, 0,
+                      stream);
+}
+
+pkv_status pkv_paged_prefill_attention_split(const void* q, const void* k_cache, const void* v_cache,
+                                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                             const int32_t* context_lens, const int32_t* query_start,
+                                             int32_t max_query_len, int32_t num_seqs, int32_t num_q_heads,
+                                             int32_t num_kv_heads, int32_t head_dim, int64_t num_blocks,
+                                             int32_t block_size, float scale, void* out, int32_t num_splits,
+                                             void* workspace, size_t workspace_bytes, pkv_stream_t stream) {
+  return prefill_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, query_start, max_query_len,
+                      num_seqs, num_q_heads, num_kv_heads, head_dim, num_blocks, block_size, scale, out, num_splits,
+                      workspace, workspace_bytes, stream);
+}
+
+pkv_status pkv_prefill_default_splits(int32_t num_seqs, int32_t max_query_len, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t* num_splits) {
+  if (!num_splits) return fail(PKV_ERR_INVALID_ARGUMENT, "num_splits is null");
+  if (num_seqs < 0 || max_query_len < 0) return fail(PKV_ERR_INVALID_ARGUMENT, "num_seqs and max_query_len must be >= 0");
+  if (pkv_status st = check_shapes(num_seqs, num_seqs, num_q_heads, num_kv_heads, 128, 1); st != PKV_OK) return st;
+  int sms = 0;
+  if (pkv_status st = device_state(nullptr, &sms); st != PKV_OK) return st;
+  // The most splits that keep every CTA of the call in one wave (one CTA per SM), at most 32, and
+  // within the 65535 grid rows; 1 when the call already fills the GPU.
+  const int64_t cta = pkv::prefill_cta_tokens(num_q_heads / num_kv_heads);
+  const int64_t ctas = static_cast<int64_t>(num_seqs) * num_kv_heads * ((max_query_len + cta - 1) / cta);
+  int64_t n = ctas > 0 ? sms / ctas : 1;
+  if (n > kMaxPrefillSplits) n = kMaxPrefillSplits;
+  if (num_seqs > 0 && n > 65535 / num_seqs) n = 65535 / num_seqs;
+  if (n < 1) n = 1;
+  *num_splits = static_cast<int32_t>(n);
+  return ok();
+}
+
+pkv_status pkv_prefill_workspace_size(int32_t num_seqs, int32_t max_query_len, int32_t num_q_heads,
+                                      int32_t num_kv_heads, int32_t head_dim, int32_t num_splits, size_t* bytes) {
+  if (!bytes) return fail(PKV_ERR_INVALID_ARGUMENT, "bytes must not be null");
+  if (num_seqs < 0 || max_query_len < 0) return fail(PKV_ERR_INVALID_ARGUMENT, "num_seqs and max_query_len must be >= 0");
+  if (num_splits < 1 || num_splits > kMaxPrefillSplits)
+    return fail(PKV_ERR_INVALID_ARGUMENT, "num_splits must be in [1, %d] (got %d)", kMaxPrefillSplits, num_splits);
+  if (pkv_status st = check_shapes(num_seqs, num_seqs, num_q_heads, num_kv_heads, head_dim, 1); st != PKV_OK) return st;
+  *bytes = pkv::prefill_workspace_bytes(num_seqs, max_query_len, num_q_heads, num_kv_heads, head_dim, num_splits);
   return ok();
 }
 

@@ -322,7 +322,7 @@ __device__ __forceinline__ uint32_t kv_off(int r, int h, int chunk) {
 // ---------------------------------------------------------------------------
 // The kernel
 // ---------------------------------------------------------------------------
-template <int D, int G>
+template <int D, int G, bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     paged_prefill_kernel(const PrefillParams p, const __grid_constant__ CUtensorMap map_k,
                          const __grid_constant__ CUtensorMap map_v, const __grid_constant__ CUtensorMap map_out) {
@@ -347,7 +347,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // in the V ring (not yet in use) and a spare word of the barrier area.
   // The sequences' chunk starts are staged beside the lengths in the same pass, so that the
   // picked sequence's q0, C and L need no second round trip to memory.
-  int b = blockIdx.z;
+  // z = (sequence rank) * num_splits + split: a sequence's splits go out together.
+  const int split = kSplit ? static_cast<int>(blockIdx.z) % p.num_splits : 0;
+  const int zrank = kSplit ? static_cast<int>(blockIdx.z) / p.num_splits : static_cast<int>(blockIdx.z);
+  int b = zrank;
   int q0, C, L;
   if (p.num_seqs <= kThreads) {
     int* s_lens = reinterpret_cast<int*>(smem + T::kOffKV + (kRing - 1) * T::kTile);
@@ -366,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int other = s_lens[u];
         rank += (other > mine) || (other == mine && u < tid);
       }
-      if (rank == static_cast<int>(blockIdx.z)) s_pick = tid;
+      if (rank == zrank) s_pick = tid;
     }
     __syncthreads();
     b = s_pick;
@@ -394,8 +397,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int i_last = min(C, i0 + kCtaTokens) - 1;
   const int n_tiles = (i0 + kTokens < C) ? 2 : 1;  // the second tile only if it holds chunk rows
   const int kv_end = prefix + i_last + 1;          // keys the CTA's last row sees
-  const int nsteps = (kv_end + kKeys - 1) / kKeys;
-  const bool tail = kv_end < nsteps * kKeys;       // the last step has keys past the end
+  // This CTA's key steps: [j0, j0 + nsteps) of the tile pair's steps_all, split evenly over the
+  // num_splits CTAs of the pair (a split with no step only marks its rows empty).
+  const int steps_all = (kv_end + kKeys - 1) / kKeys;
+  const int j0 = kSplit ? static_cast<int>(static_cast<int64_t>(split) * steps_all / p.num_splits) : 0;
+  const int nsteps =
+      kSplit ? static_cast<int>(static_cast<int64_t>(split + 1) * steps_all / p.num_splits) - j0 : steps_all;
+  const bool tail = j0 + nsteps == steps_all && kv_end < steps_all * kKeys;  // the last step has keys past the end
+  constexpr bool partial = kSplit;  // O, m and l go to the workspace for the merge
+  if (kSplit && nsteps == 0) {  // uniform for the CTA: nothing allocated yet
+    for (int x = tid; x < kCtaTokens * G; x += kThreads) {
+      const int i = i0 + x / G;
+      if (i < C)
+        reinterpret_cast<float2*>(p.ws + static_cast<size_t>(p.num_splits) * p.num_seqs * p.ws_rows * p.num_q_heads *
+                                             D)[((static_cast<size_t>(split) * p.num_seqs + b) * p.ws_rows + i) *
+                                                    p.num_q_heads + kvh * G + x % G] = make_float2(-INFINITY, 0.f);
+    }
+    return;
+  }
 
   // Barriers.  K/V ring: a slot frees when every tile's MMA that reads it has
   // retired.  Per tile: S ready, P ready, O final, Q staged, MMAs drained.  Each
@@ -420,10 +439,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kPages = kKeys / kBlockTokens;  // pages per step
   const int npages = (kv_end + kBlockTokens - 1) / kBlockTokens;
   const int32_t* table = p.block_tables + static_cast<size_t>(b) * p.max_blocks_per_seq;
+  const int w0 = (j0 * kPages) / 32;  // the block-id window holding the CTA's first step
   int raw_cur = 0, raw_next = 0;
   if (warp == kProducerWarp) {
-    if (lane < npages) raw_cur = __ldg(table + lane);
-    if (32 + lane < npages) raw_next = __ldg(table + 32 + lane);
+    if (32 * w0 + lane < npages) raw_cur = __ldg(table + 32 * w0 + lane);
+    if (32 * (w0 + 1) + lane < npages) raw_next = __ldg(table + 32 * (w0 + 1) + lane);
   }
 
   // Stage Q (zero rows past the chunk) in the swizzled K-major layout, issued before the set-up
@@ -461,11 +481,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncwarp();
-    const int pages0 = min(kPages, npages);
+    const int first0 = j0 * kPages;  // the first step's pages: lanes first0 % 32 .. + 7 of window w0
+    const int pages0 = min(kPages, npages - first0);
+    const int id0 = __shfl_sync(0xffffffffu, raw_cur, (first0 % 32) + min(lane, kPages - 1));
     if (lane == 0) bar_expect_tx(r_full, static_cast<uint32_t>(pages0 * T::kPageBytes));
     __syncwarp();
     if (lane < pages0) {
-      const int id = (raw_cur < 0 || raw_cur >= p.num_blocks) ? 0 : raw_cur;  // flagged by the producer below
+      const int id = (id0 < 0 || id0 >= p.num_blocks) ? 0 : id0;  // flagged by the producer below
       tma_load_4d(s_base + T::kOffKV + lane * T::kPageBytes, &map_k, 2 * (id * p.num_kv_heads + kvh), r_full);
     }
   }
@@ -507,14 +529,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       return id;
     };
     auto fetch = [&](int page) -> int { return page < npages ? check(page, __ldg(table + page)) : 0; };
-    int win = 0;
-    int id_cur = check(lane, raw_cur), id_next = check(32 + lane, raw_next);
+    int win = w0;
+    int id_cur = check(32 * w0 + lane, raw_cur), id_next = check(32 * (w0 + 1) + lane, raw_next);
     int issued = 0;  // ring tiles issued
     // One copy per lane, lane = page of the step: a thread's tensor copies issue one
     // after another, slowly, while copies from different lanes go out together.  A
     // copy moves a whole page of the kv head (both dims halves, 4 KB at D = 128).
     const int my_pg = lane;
-    auto issue = [&](int j, int my_id, uint32_t dst, const CUtensorMap* map, uint32_t full) {
+    auto issue = [&](int j, int my_id, uint32_t dst, const CUtensorMap* map, uint32_t full) {  // j: absolute step
       const int pages = min(kPages, npages - j * kPages);
       if (lane == 0) bar_expect_tx(full, static_cast<uint32_t>(pages * T::kPageBytes));
       __syncwarp();
@@ -528,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       if ((n & 1) == 0) {
-        const int first_page = jn * kPages;
+        const int first_page = (j0 + jn) * kPages;
         if (first_page / 32 != win) {  // slide the window
           ++win;
           id_cur = id_next;
@@ -536,8 +558,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         my_id = __shfl_sync(0xffffffffu, id_cur, (first_page % 32) + min(my_pg, kPages - 1));
       }
-      if (n > 0)  // K of step 0 went out before the set-up barrier
-        issue(jn, my_id, s_base + T::kOffKV + slot * T::kTile, (n & 1) ? &map_v : &map_k, r_full + 8 * slot);
+      if (n > 0)  // K of the first step went out before the set-up barrier
+        issue(j0 + jn, my_id, s_base + T::kOffKV + slot * T::kTile, (n & 1) ? &map_v : &map_k, r_full + 8 * slot);
       issued = n + 1;
     }
     if (!failed && tail) {
@@ -547,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int jv = nsteps - 1, nv = 2 * jv + 1;
       if (__all_sync(0xffffffffu, bar_wait(r_full + 8 * (nv % kRing), (nv / kRing) & 1))) {
         unsigned char* vt = smem + T::kOffKV + (nv % kRing) * T::kTile;
-        const int first = kv_end - jv * kKeys;
+        const int first = kv_end - (j0 + jv) * kKeys;
         for (int idx = lane; idx < (kKeys - first) * T::kHalves * 8; idx += 32) {
           const int r = first + idx / (T::kHalves * 8);
           const int rem = idx % (T::kHalves * 8);
@@ -652,6 +674,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     bar_arrive(q_ready + 8 * t);
     const float qk = p.scale * kLog2e;
     const int limit = row_ok ? prefix + i + 1 : 0;  // keys this row may see
+    // A row sees a key of this CTA's steps unless a split's range starts past its causal limit;
+    // a row that sees none keeps m = -inf, l = 0 (all its p are 0).
+    const bool sees = kSplit ? limit > j0 * kKeys : row_ok;
     float m_used = -INFINITY, l = 0.f;
     // A warp reaches the TMEM lanes 32 * (warp % 4) .. + 31: rows r of either tile.
     const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
@@ -667,9 +692,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_ld64(s_cols, *reinterpret_cast<float(*)[64]>(&s[0]));
       tmem_ld64(s_cols + 64, *reinterpret_cast<float(*)[64]>(&s[64]));
       // Causal / length mask, only on steps that some row of the warp does not see whole.
-      if (__any_sync(0xffffffffu, (j + 1) * kKeys > limit)) {
+      const int ja = j0 + j;  // absolute key step
+      if (__any_sync(0xffffffffu, (ja + 1) * kKeys > limit)) {
 #pragma unroll
-        for (int x = 0; x < kKeys; ++x) s[x] = (j * kKeys + x) < limit ? s[x] : -INFINITY;
+        for (int x = 0; x < kKeys; ++x) s[x] = (ja * kKeys + x) < limit ? s[x] : -INFINITY;
       }
       // Row max: eight chains of three-input maxima, then their maximum.
       static_assert(kKeys % 8 == 0 && kKeys >= 24, "row max layout");
@@ -687,10 +713,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float row_max = fmax3(fmax3(mc[0], mc[1], mc[2]), fmax3(mc[3], mc[4], mc[5]), fmaxf(mc[6], mc[7]));
       const float bm = row_max * qk;  // the scale is positive: the max of the scaled scores
-      const bool raise = row_ok && bm > m_used + kSlack;
+      const bool raise = sees && bm > m_used + kSlack;
       const float m_new = raise ? bm : m_used;
       const float alpha = raise ? ex2_approx(m_used - m_new) : 1.f;  // 0 on the first raise
-      const float neg_m = row_ok ? -m_new : 0.f;                      // rows past the chunk: all p = 0
+      const float neg_m = sees ? -m_new : 0.f;                        // rows seeing no key: all p = 0
       float2 acc4[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
                         make_float2(0.f, 0.f)};
       uint32_t packed[kKeys / 2];
@@ -732,55 +758,97 @@ __global__ void __launch_bounds__(kThreads, 1)
     // rows ordered token-major, head-minor, which is a tensor box of the output.  A tile whose
     // rows all lie in the chunk then leaves as one tensor store per half; the last, partial tile
     // of a chunk is stored by the tile's 128 threads together, a warp two whole rows at a time.
-    bool staged = false;
-    unsigned char* ot = smem + T::kOffQ + t * T::kQTile;
-    if (!failed && __all_sync(0xffffffffu, bar_wait(o_full + 8 * t, 0))) {
-      tc_after_sync();
-      const float inv = l > 0.f ? 1.f / l : 0.f;
+    if constexpr (partial) {
+      // Split call: the tile's rows leave as fp32 partial states, O unnormalised with the running
+      // max m (base 2) and sum l they were formed against, for the merge kernel.
+      // A thread holds one row; the warp's 32 rows go out through its own 4 KB of the tile's Q buffer
+      // (free: every S that read it has retired), 32 columns at a time: written a row per lane with
+      // the 16-byte chunks rotated by the row (no bank conflict), read back a quarter-row per lane,
+      // so that each store instruction writes four 128-byte row segments.
+      if (!failed && __all_sync(0xffffffffu, bar_wait(o_full + 8 * t, 0))) {
+        tc_after_sync();
+        const size_t row =
+            ((static_cast<size_t>(split) * p.num_seqs + b) * p.ws_rows + i) * p.num_q_heads + kvh * G + r % G;
+        float* scratch = reinterpret_cast<float*>(smem + T::kOffQ + t * T::kQTile) + (warp & 3) * 32 * 32;
+        const size_t seq_row0 = (static_cast<size_t>(split) * p.num_seqs + b) * p.ws_rows;  // chunk row 0
 #pragma unroll
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        float o[32];
-        tmem_ld32(o_cols + c0, o);
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float o[32];
+          tmem_ld32(o_cols + c0, o);
 #pragma unroll
-        for (int x = 0; x < 32; x += 8) {
-          const int ch = (c0 + x) / 8;
-          *reinterpret_cast<uint4*>(ot + (ch / 8) * T::kQHalf + swz(r, ch % 8)) =
-              make_uint4(pack_bf16(o[x] * inv, o[x + 1] * inv), pack_bf16(o[x + 2] * inv, o[x + 3] * inv),
-                         pack_bf16(o[x + 4] * inv, o[x + 5] * inv), pack_bf16(o[x + 6] * inv, o[x + 7] * inv));
+          for (int q4 = 0; q4 < 8; ++q4)
+            *reinterpret_cast<float4*>(scratch + lane * 32 + ((q4 + lane) & 7) * 4) =
+                make_float4(o[4 * q4], o[4 * q4 + 1], o[4 * q4 + 2], o[4 * q4 + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int rr = 4 * k + (lane >> 3), q4 = lane & 7;  // the warp's row rr, its chunk q4
+            const float4 v = *reinterpret_cast<const float4*>(scratch + rr * 32 + ((q4 + rr) & 7) * 4);
+            const int tr = (warp & 3) * 32 + rr;        // tile row
+            const int ii = i0 + t * kTokens + tr / G;  // its chunk token
+            if (ii < C)
+              *reinterpret_cast<float4*>(p.ws + ((seq_row0 + ii) * p.num_q_heads + kvh * G + tr % G) * D + c0 +
+                                         q4 * 4) = v;
+          }
+          __syncwarp();
         }
+        if (row_ok)
+          reinterpret_cast<float2*>(p.ws + static_cast<size_t>(p.num_splits) * p.num_seqs * p.ws_rows *
+                                               p.num_q_heads * D)[row] = make_float2(m_used, l);
+      } else {
+        failed = true;
       }
-      fence_async_smem();  // the tensor store reads the rows through the async proxy
-      staged = true;
     } else {
-      failed = true;
-    }
-    // Every thread of the tile arrives, staged or not, so that the bounded wait below ends.
-    bar_arrive(o_staged + 8 * t);
-    if (__all_sync(0xffffffffu, staged && bar_wait(o_staged + 8 * t, 0))) {
-      const int tok0 = i0 + t * kTokens;
-      // The tensor map spans num_seqs * max_query_len tokens; a chunk longer than max_query_len (an
-      // error the device flags) can put rows past that, which the threads store instead.
-      const int64_t map_tokens = static_cast<int64_t>(p.num_seqs) * p.max_query_len;
-      if (tok0 + kTokens <= C && static_cast<int64_t>(q0) + tok0 + kTokens <= (map_tokens < INT32_MAX ? map_tokens : INT32_MAX)) {
-        if (r == 0) {
-#pragma unroll
-          for (int h = 0; h < T::kHalves; ++h)
-            tma_store_3d(&map_out, 64 * h, kvh * G, q0 + tok0, s_base + T::kOffQ + t * T::kQTile + h * T::kQHalf);
-          tma_store_commit_and_wait_read();  // the buffer is read before the CTA may leave
+      bool staged = false;
+      unsigned char* ot = smem + T::kOffQ + t * T::kQTile;
+      if (!failed && __all_sync(0xffffffffu, bar_wait(o_full + 8 * t, 0))) {
+        tc_after_sync();
+        const float inv = l > 0.f ? 1.f / l : 0.f;
+  #pragma unroll
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float o[32];
+          tmem_ld32(o_cols + c0, o);
+  #pragma unroll
+          for (int x = 0; x < 32; x += 8) {
+            const int ch = (c0 + x) / 8;
+            *reinterpret_cast<uint4*>(ot + (ch / 8) * T::kQHalf + swz(r, ch % 8)) =
+                make_uint4(pack_bf16(o[x] * inv, o[x + 1] * inv), pack_bf16(o[x + 2] * inv, o[x + 3] * inv),
+                           pack_bf16(o[x + 4] * inv, o[x + 5] * inv), pack_bf16(o[x + 6] * inv, o[x + 7] * inv));
+          }
+        }
+        fence_async_smem();  // the tensor store reads the rows through the async proxy
+        staged = true;
+      } else {
+        failed = true;
+      }
+      // Every thread of the tile arrives, staged or not, so that the bounded wait below ends.
+      bar_arrive(o_staged + 8 * t);
+      if (__all_sync(0xffffffffu, staged && bar_wait(o_staged + 8 * t, 0))) {
+        const int tok0 = i0 + t * kTokens;
+        // The tensor map spans num_seqs * max_query_len tokens; a chunk longer than max_query_len (an
+        // error the device flags) can put rows past that, which the threads store instead.
+        const int64_t map_tokens = static_cast<int64_t>(p.num_seqs) * p.max_query_len;
+        if (tok0 + kTokens <= C && static_cast<int64_t>(q0) + tok0 + kTokens <= (map_tokens < INT32_MAX ? map_tokens : INT32_MAX)) {
+          if (r == 0) {
+  #pragma unroll
+            for (int h = 0; h < T::kHalves; ++h)
+              tma_store_3d(&map_out, 64 * h, kvh * G, q0 + tok0, s_base + T::kOffQ + t * T::kQTile + h * T::kQHalf);
+            tma_store_commit_and_wait_read();  // the buffer is read before the CTA may leave
+          }
+        } else {
+          __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.out);
+  #pragma unroll 4
+          for (int c = r; c < kRows * kChunks; c += kRows) {
+            const int rr = c / kChunks, ch = c % kChunks;
+            const int ii = tok0 + rr / G;
+            if (ii < C)
+              reinterpret_cast<uint4*>(og + (static_cast<size_t>(q0 + ii) * p.num_q_heads + kvh * G + rr % G) * D)[ch] =
+                  *reinterpret_cast<const uint4*>(ot + (ch / 8) * T::kQHalf + swz(rr, ch % 8));
+          }
         }
       } else {
-        __nv_bfloat16* og = static_cast<__nv_bfloat16*>(p.out);
-#pragma unroll 4
-        for (int c = r; c < kRows * kChunks; c += kRows) {
-          const int rr = c / kChunks, ch = c % kChunks;
-          const int ii = tok0 + rr / G;
-          if (ii < C)
-            reinterpret_cast<uint4*>(og + (static_cast<size_t>(q0 + ii) * p.num_q_heads + kvh * G + rr % G) * D)[ch] =
-                *reinterpret_cast<const uint4*>(ot + (ch / 8) * T::kQHalf + swz(rr, ch % 8));
-        }
+        failed = true;
       }
-    } else {
-      failed = true;
     }
     if (failed && lane == 0) atomicOr(p.err, kErrTimeout);
   }
@@ -791,6 +859,86 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == kMmaWarp) {
     tc_after_sync();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+}
+
+
+// Merge of a split call (the split-K reduction, as in decode): for every chunk row, over the splits
+// whose m is finite, M = max m_s and out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s, rounded to
+// bf16.  A warp takes four (chunk token, q head) rows at a time; lane s reads split s's (m, l).  Rows of a sequence
+// the attention kernel rejected are left untouched, as the unsplit call leaves them.
+template <int D>
+__global__ void __launch_bounds__(256) paged_prefill_merge_kernel(const PrefillParams p) {
+  pdl_trigger();
+  pdl_wait();
+  static_assert(D % 64 == 0, "a lane takes D / 32 contiguous columns, an even count");
+  constexpr int kCols = D / 32;
+  const int b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q0 = p.query_start[b];
+  const int C = p.query_start[b + 1] - q0;
+  const int L = p.context_lens[b];
+  if (C < 0 || L < C || L > p.max_blocks_per_seq * kBlockTokens) return;  // flagged by the attention kernel
+  const int rows = min(C, p.ws_rows) * p.num_q_heads;
+  const size_t split_stride = static_cast<size_t>(p.num_seqs) * p.ws_rows * p.num_q_heads;  // rows per split
+  const float2* ml =
+      reinterpret_cast<const float2*>(p.ws + static_cast<size_t>(p.num_splits) * split_stride * D);
+  __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+  constexpr int kRowsPerWarp = 4;  // loads of four rows in flight at once
+  for (int row4 = (blockIdx.x * 8 + warp) * kRowsPerWarp; row4 < rows; row4 += gridDim.x * 8 * kRowsPerWarp) {
+    const size_t r0 = static_cast<size_t>(b) * p.ws_rows * p.num_q_heads + row4;  // the first row in split 0
+    float m[kRowsPerWarp], l[kRowsPerWarp];
+#pragma unroll
+    for (int k = 0; k < kRowsPerWarp; ++k) {
+      m[k] = -INFINITY;
+      l[k] = 0.f;
+      if (lane < p.num_splits && row4 + k < rows) {
+        const float2 v = ml[lane * split_stride + r0 + k];
+        m[k] = v.x;
+        l[k] = v.y;
+      }
+    }
+    float w[kRowsPerWarp], inv[kRowsPerWarp];
+#pragma unroll
+    for (int k = 0; k < kRowsPerWarp; ++k) {
+      float mx = m[k];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+      w[k] = m[k] == -INFINITY ? 0.f : exp2f(m[k] - mx);
+      float den = w[k] * l[k];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) den += __shfl_xor_sync(0xffffffffu, den, off);
+      inv[k] = den > 0.f ? 1.f / den : 0.f;
+    }
+    float acc[kRowsPerWarp][kCols];
+#pragma unroll
+    for (int k = 0; k < kRowsPerWarp; ++k)
+#pragma unroll
+      for (int c = 0; c < kCols; ++c) acc[k][c] = 0.f;
+    for (int sp = 0; sp < p.num_splits; ++sp) {
+#pragma unroll
+      for (int k = 0; k < kRowsPerWarp; ++k) {
+        const float wsp = __shfl_sync(0xffffffffu, w[k], sp);
+        if (wsp == 0.f) continue;  // the same for the whole warp
+        const float* o = p.ws + (sp * split_stride + r0 + k) * D + lane * kCols;
+#pragma unroll
+        for (int c = 0; c < kCols; c += 2) {
+          const float2 v = *reinterpret_cast<const float2*>(o + c);
+          acc[k][c] += wsp * v.x;
+          acc[k][c + 1] += wsp * v.y;
+        }
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kRowsPerWarp; ++k) {
+      if (row4 + k >= rows) break;
+      const int i = (row4 + k) / p.num_q_heads, h = (row4 + k) % p.num_q_heads;
+      __nv_bfloat162* dst = reinterpret_cast<__nv_bfloat162*>(
+          out + (static_cast<size_t>(q0 + i) * p.num_q_heads + h) * D + lane * kCols);
+#pragma unroll
+      for (int c = 0; c < kCols; c += 2)
+        dst[c / 2] = __floats2bfloat162_rn(acc[k][c] * inv[k], acc[k][c + 1] * inv[k]);
+    }
   }
 }
 
@@ -872,7 +1020,7 @@ cudaError_t out_map(CUtensorMap* map, void* out, int64_t tokens, int num_q_heads
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int D, int G>
+template <int D, int G, bool kSplit>
 cudaError_t launch_t(const PrefillParams& p, int max_query_len, cudaStream_t stream) {
   constexpr int kCtaTokens = kTiles * kRows / G;
   static std::mutex mu;
@@ -883,7 +1031,8 @@ cudaError_t launch_t(const PrefillParams& p, int max_query_len, cudaStream_t str
   {
     std::lock_guard<std::mutex> lock(mu);
     if (!(dev < 64 && ((ready >> dev) & 1u))) {
-      e = cudaFuncSetAttribute(&paged_prefill_kernel<D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, Pf<D>::kSmem);
+      e = cudaFuncSetAttribute(&paged_prefill_kernel<D, G, kSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               Pf<D>::kSmem);
       if (e != cudaSuccess) return e;
       if (dev < 64) ready |= uint64_t{1} << dev;
     }
@@ -896,8 +1045,20 @@ cudaError_t launch_t(const PrefillParams& p, int max_query_len, cudaStream_t str
   int64_t tokens = static_cast<int64_t>(p.num_seqs) * max_query_len;
   if (tokens > INT32_MAX) tokens = INT32_MAX;
   if ((e = out_map(&mo, p.out, tokens, p.num_q_heads, D, G, kRows / G)) != cudaSuccess) return e;
-  const dim3 grid(p.num_kv_heads, (max_query_len + kCtaTokens - 1) / kCtaTokens, p.num_seqs);
-  return launch_pdl(paged_prefill_kernel<D, G>, grid, dim3(kThreads), Pf<D>::kSmem, stream, p, mk, mv, mo);
+  const int tiles = (max_query_len + kCtaTokens - 1) / kCtaTokens;
+  if constexpr (!kSplit) {
+    const dim3 grid(p.num_kv_heads, tiles, p.num_seqs);
+    return launch_pdl(paged_prefill_kernel<D, G, false>, grid, dim3(kThreads), Pf<D>::kSmem, stream, p, mk, mv, mo);
+  } else {
+    PrefillParams q = p;
+    q.ws_rows = tiles * kCtaTokens;
+    const dim3 grid(p.num_kv_heads, tiles, p.num_seqs * p.num_splits);
+    e = launch_pdl(paged_prefill_kernel<D, G, true>, grid, dim3(kThreads), Pf<D>::kSmem, stream, q, mk, mv, mo);
+    if (e != cudaSuccess) return e;
+    const int64_t row_blocks = (static_cast<int64_t>(q.ws_rows) * p.num_q_heads + 31) / 32;  // 8 warps x 4 rows
+    const dim3 mgrid(static_cast<unsigned>(row_blocks < 65535 ? row_blocks : 65535), p.num_seqs);
+    return launch_pdl(paged_prefill_merge_kernel<D>, mgrid, dim3(256), 0, stream, q);
+  }
 }
 
 }  // namespace
@@ -908,15 +1069,19 @@ cudaError_t encode_cache_map(CUtensorMap_st* map, const void* cache, int64_t row
 
 cudaError_t launch_paged_prefill(const PrefillParams& p, int head_dim, int group, int max_query_len,
                                  cudaStream_t stream) {
+  const bool split = p.num_splits > 1;
   switch (head_dim * 16 + group) {
-    case 64 * 16 + 1: return launch_t<64, 1>(p, max_query_len, stream);
-    case 64 * 16 + 2: return launch_t<64, 2>(p, max_query_len, stream);
-    case 64 * 16 + 4: return launch_t<64, 4>(p, max_query_len, stream);
-    case 64 * 16 + 8: return launch_t<64, 8>(p, max_query_len, stream);
-    case 128 * 16 + 1: return launch_t<128, 1>(p, max_query_len, stream);
-    case 128 * 16 + 2: return launch_t<128, 2>(p, max_query_len, stream);
-    case 128 * 16 + 4: return launch_t<128, 4>(p, max_query_len, stream);
-    case 128 * 16 + 8: return launch_t<128, 8>(p, max_query_len, stream);
+#define PKV_PREFILL_CASE(d, g) \
+  case d * 16 + g: return split ? launch_t<d, g, true>(p, max_query_len, stream) : launch_t<d, g, false>(p, max_query_len, stream);
+    PKV_PREFILL_CASE(64, 1)
+    PKV_PREFILL_CASE(64, 2)
+    PKV_PREFILL_CASE(64, 4)
+    PKV_PREFILL_CASE(64, 8)
+    PKV_PREFILL_CASE(128, 1)
+    PKV_PREFILL_CASE(128, 2)
+    PKV_PREFILL_CASE(128, 4)
+    PKV_PREFILL_CASE(128, 8)
+#undef PKV_PREFILL_CASE
     default: return cudaErrorInvalidValue;
   }
 }

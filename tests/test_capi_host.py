@@ -128,6 +128,44 @@ def test_prefill_rejects_grids_it_cannot_launch(lib):
     assert prefill(lib, mql=0, q=None, out=None) == 0                                   # a no-op before the pointers
 
 
+def prefill_split(lib, **kw):
+    a = dict(q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, W=8, cl=FAKE, qs=FAKE, mql=512, B=4, hq=32, hkv=8, d=128, nb=100,
+             bs=16, scale=0.088, out=FAKE, S=2, ws=FAKE, wsb=1 << 30, stream=None)
+    a.update(kw)
+    return lib.pkv_paged_prefill_attention_split(a["q"], a["kc"], a["vc"], a["bt"], a["W"], a["cl"], a["qs"], a["mql"],
+                                                 a["B"], a["hq"], a["hkv"], a["d"], a["nb"], a["bs"], a["scale"],
+                                                 a["out"], a["S"], a["ws"], a["wsb"], a["stream"])
+
+
+def test_prefill_workspace_size(lib):
+    n = ctypes.c_size_t(0)
+    # 3 splits x 4 sequences x 512 rows (a multiple of G = 4's 64 chunk tokens) x 32 q heads x (128 + 2) floats
+    assert lib.pkv_prefill_workspace_size(4, 512, 32, 8, 128, 3, ctypes.byref(n)) == 0
+    assert n.value == 3 * 4 * 512 * 32 * 130 * 4
+    assert lib.pkv_prefill_workspace_size(2, 33, 16, 8, 64, 2, ctypes.byref(n)) == 0   # G = 2: 128-token CTAs
+    assert n.value == 2 * 2 * 128 * 16 * 66 * 4
+    assert lib.pkv_prefill_workspace_size(4, 512, 32, 8, 128, 1, ctypes.byref(n)) == 0 and n.value == 0
+    assert lib.pkv_prefill_workspace_size(4, 512, 32, 8, 128, 33, ctypes.byref(n)) == 1
+    assert lib.pkv_prefill_workspace_size(4, 512, 30, 8, 128, 2, ctypes.byref(n)) == 1
+
+
+def test_prefill_default_splits_checks_arguments_before_the_device(lib):
+    n = ctypes.c_int32(0)
+    assert lib.pkv_prefill_default_splits(1, 512, 32, 8, None) == 1 and "null" in msg(lib)
+    assert lib.pkv_prefill_default_splits(1, 512, 30, 8, ctypes.byref(n)) == 1
+    assert lib.pkv_prefill_default_splits(-1, 512, 32, 8, ctypes.byref(n)) == 1
+
+
+def test_prefill_split_rejects_bad_arguments(lib):
+    assert prefill_split(lib, S=0) == 1 and "num_splits" in msg(lib)
+    assert prefill_split(lib, S=33) == 1 and "num_splits" in msg(lib)
+    assert prefill_split(lib, B=40000, S=2) == 2 and "num_splits" in msg(lib)            # 80000 grid rows
+    assert prefill_split(lib, wsb=16) == 1 and "workspace too small" in msg(lib)
+    assert prefill_split(lib, ws=None) == 1 and "workspace too small" in msg(lib)
+    assert prefill_split(lib, ws=FAKE + 8) == 1 and "aligned" in msg(lib)
+    assert prefill_split(lib, mql=0, q=None, out=None, ws=None) == 0                   # a no-op before the pointers
+
+
 def test_attention_zero_sequences_is_a_noop(lib):
     assert attention(lib, B=0, q=None, out=None) == 0
 

@@ -179,3 +179,95 @@ def test_prefill_host_errors_raise_before_launch():
         pkv.paged_prefill_attention(c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens, c.query_start, 40,
                                     float("nan"), torch.empty_like(c.q))
     assert pkv.kernel_launch_count() == before
+
+
+# ---- Split-K over the key steps (pkv_paged_prefill_attention_split) ----
+
+def _run_split(c, num_splits):
+    g = c.to("cuda")
+    pkv.kv_append(g.new_k, g.new_v, g.slot_mapping, g.k_cache, g.v_cache)
+    out = torch.full_like(g.q, float("nan"))
+    max_q = int(max(c.spec.chunk_lens))
+    pkv.paged_prefill_attention(g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens, g.query_start, max_q,
+                                g.scale, out, num_splits=num_splits)
+    torch.cuda.synchronize()
+    return g, out
+
+
+@pytest.mark.parametrize("num_splits", [2, 3, 7])
+@pytest.mark.parametrize("head_dim,hq,hkv", [(128, 32, 8), (128, 16, 8), (64, 4, 4), (128, 64, 8)])
+def test_prefill_split_every_layout_ragged(head_dim, hq, hkv, num_splits):
+    """Chunks of 1..130 tokens after 0..500 cached ones: one to five key steps a tile, so with 7 splits most
+    CTAs of a short tile have no step and only mark their rows empty."""
+    spec = PrefillSpec("ragged", "", hq, hkv, head_dim, (1, 7, 37, 130, 16), (0, 0), 60)
+    c = make_prefill_case(spec, seed=6, prefixes=[0, 3, 100, 500, 64])
+    _, out = _run_split(c, num_splits)
+    assert_close(out, _ref(c), f"split {num_splits} D{head_dim} {hq}/{hkv}")
+    assert device_errors() == 0
+
+
+def test_prefill_split_qwen3_chunks_agree_with_the_unsplit_call():
+    c = make_prefill_case("prefill_qwen3_0.6b", seed=3)
+    _, whole = _run(c)
+    _, split = _run_split(c, 3)
+    ref = _ref(c)
+    assert_close(split, ref, "prefill_qwen3_0.6b split 3")
+    # Same math, fp32 partial states merged in another order: a bf16 step apart at most.
+    assert (split.float() - whole.float()).abs().max().item() <= 2 * 2 ** -7 * max(1.0, whole.float().abs().max().item())
+    assert device_errors() == 0
+
+
+def test_prefill_split_long_prefix():
+    """A 20 000-token prefix split five ways: each CTA's block-id window starts mid-table."""
+    spec = PrefillSpec("long", "", 8, 2, 128, (16, 3, 200), (0, 0), 1270)
+    c = make_prefill_case(spec, seed=13, prefixes=[20000, 5000, 300])
+    _, out = _run_split(c, 5)
+    assert_close(out, _ref(c), "long prefix split 5")
+    assert device_errors() == 0
+
+
+def test_prefill_split_long_chunk():
+    spec = PrefillSpec("long_chunk", "", 8, 1, 64, (2048, 45), (0, 0), 140)
+    c = make_prefill_case(spec, seed=22, prefixes=[100, 7])
+    _, out = _run_split(c, 4)
+    assert_close(out, _ref(c), "long chunk split 4")
+    assert device_errors() == 0
+
+
+def test_prefill_split_graph_replay_is_bit_identical():
+    c = make_prefill_case("prefill_tiny", seed=4).to("cuda")
+    pkv.kv_append(c.new_k, c.new_v, c.slot_mapping, c.k_cache, c.v_cache)
+    max_q = int(max(c.spec.chunk_lens))
+    B, hq, d = c.context_lens.shape[0], c.q.shape[1], c.q.shape[2]
+    ws = torch.empty(pkv.prefill_workspace_size(B, max_q, hq, c.k_cache.shape[1], d, 3), dtype=torch.uint8,
+                     device="cuda")
+    eager = torch.empty_like(c.q)
+    call = lambda o, s=None: pkv.paged_prefill_attention(c.q, c.k_cache, c.v_cache, c.block_tables, c.context_lens,
+                                                         c.query_start, max_q, c.scale, o, stream=s, num_splits=3,
+                                                         workspace=ws)
+    call(eager)
+    torch.cuda.synchronize()
+    out = torch.zeros_like(c.q)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call(out, s)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call(out, s)
+    for _ in range(2):
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, eager)
+    assert device_errors() == 0
+
+
+def test_prefill_default_splits_fill_one_wave():
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    # One LLaMA-3 chunk of 512: 8 kv heads x 8 CTAs of 64 tokens.
+    assert pkv.prefill_default_splits(1, 512, 32, 8) == max(1, min(32, sms // 64))
+    assert pkv.prefill_default_splits(8, 512, 32, 8) == max(1, min(32, sms // 512))   # already fills the GPU
+    assert pkv.prefill_default_splits(1, 16, 8, 1) == min(32, sms)                       # a single CTA

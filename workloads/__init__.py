@@ -389,6 +389,9 @@ PREFILL_SPECS = {
                                 (0, 40), 6),
     "prefill_qwen3_0.6b": PrefillSpec("prefill_qwen3_0.6b", "Qwen3-0.6B layer: 4 chunks of 512 after 0..2048 cached",
                                       16, 8, 128, (512, 512, 512, 512), (0, 2048), 160),
+    "prefill_llama3_8b_one": PrefillSpec("prefill_llama3_8b_one",
+                                         "LLaMA-3-8B layer: one chunk of 512 after 2048..3584 cached (32 q / 8 kv)",
+                                         32, 8, 128, (512,), (2048, 3584), 256),
     "prefill_llama3_8b": PrefillSpec("prefill_llama3_8b",
                                      "LLaMA-3-8B layer: 8 chunks of 512 after 0..3584 cached (32 q / 8 kv)",
                                      32, 8, 128, (512,) * 8, (0, 3584), 256),
