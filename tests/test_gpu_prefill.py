@@ -147,7 +147,8 @@ def test_prefill_poisoned_unused_slots_do_not_leak():
     assert device_errors() == 0
 
 
-def test_prefill_device_errors_are_flagged_and_the_gpu_stays_usable():
+@pytest.mark.parametrize("num_splits", [1, 2], ids=["unsplit", "split2"])
+def test_prefill_device_errors_are_flagged_and_the_gpu_stays_usable(num_splits):
     c = make_prefill_case("prefill_tiny", seed=9)
     g = c.to("cuda")
     pkv.kv_append(g.new_k, g.new_v, g.slot_mapping, g.k_cache, g.v_cache)
@@ -155,16 +156,17 @@ def test_prefill_device_errors_are_flagged_and_the_gpu_stays_usable():
     assert device_errors() == 0
     bt = g.block_tables.clone()
     bt[1, 0] = 10 ** 6
-    pkv.paged_prefill_attention(g.q, g.k_cache, g.v_cache, bt, g.context_lens, g.query_start, 40, g.scale, out)
+    pkv.paged_prefill_attention(g.q, g.k_cache, g.v_cache, bt, g.context_lens, g.query_start, 40, g.scale, out,
+                                num_splits=num_splits)
     assert device_errors() & pkv.DEVERR_BLOCK_ID_OUT_OF_RANGE
     # max_query_len smaller than a chunk: that chunk's rows past the grid are not covered, and it is flagged.
     pkv.paged_prefill_attention(g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens, g.query_start, 8,
-                                g.scale, out)
+                                g.scale, out, num_splits=num_splits)
     bits = device_errors()
     assert bits & pkv.DEVERR_CONTEXT_LEN_TOO_LONG and not bits & pkv.DEVERR_SMEM_ALIGNMENT
     # A clean call afterwards is correct.
     pkv.paged_prefill_attention(g.q, g.k_cache, g.v_cache, g.block_tables, g.context_lens, g.query_start, 40,
-                                g.scale, out)
+                                g.scale, out, num_splits=num_splits)
     assert_close(out, _ref(c), "after errors")
     assert device_errors() == 0
 
