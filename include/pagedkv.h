@@ -312,11 +312,13 @@ pkv_status pkv_paged_prefill_attention(const void* q, const void* k_cache, const
  * M = max m_s, out = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s (the split-K
  * reduction of paged decode).  For calls whose CTAs do not fill the GPU (few
  * sequences, short chunks); a split with no key step only marks its rows empty.
- * Results equal the unsplit call's within fp32 rounding.
+ * The fp32 partial states are merged in another order than the unsplit call's
+ * single accumulation, so results may differ from it by a bf16 step.
  *
  *   num_splits       host, 1..32; 1 is pkv_paged_prefill_attention (no workspace)
  *   workspace        device, 16-byte aligned, at least pkv_prefill_workspace_size
- *                    bytes; owned by the caller, fully overwritten, unused after the
+ *                    bytes; owned by the caller; the call writes the partial states
+ *                    of the rows it covers and reads them back; not used after the
  *                    call's kernels finish (two launches on `stream`)
  * Errors as pkv_paged_prefill_attention, plus: num_splits out of range, a null or
  * short workspace (PKV_ERR_INVALID_ARGUMENT); num_seqs * num_splits above 65535
